@@ -1,0 +1,235 @@
+"""Pins for the oracle's logits processors and draw (CPU only).
+
+Each test checks the oracle against something other than itself: published
+known-answer vectors, the facts the pages state about the processor chain,
+closed forms, or brute force over a tiny vocabulary.
+"""
+import ctypes
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from synth import RowSampling
+
+V = 3072
+EOS = 2150
+
+
+def sp(**kw):
+    base = dict(repetition_penalty=1.0, min_new_tokens=0)
+    base.update(kw)
+    return RowSampling(**base)
+
+
+def test_page_ids(golden_dir):
+    facts = json.load(open(os.path.join(golden_dir, "page_facts.json")))
+    d = synth.DIMS_06B
+    assert facts["codec_special_ids"]["eos"] == d.eos_id == EOS
+    assert facts["codec_special_ids"]["codec_vocab"] == d.codec_vocab
+    assert facts["suppress"]["lo"] == d.suppress_lo and facts["suppress"]["hi_inclusive"] + 1 == d.suppress_hi
+    assert facts["structure"]["predictor_tables"] == d.n_groups - 1
+    assert facts["natural_eos_run"]["talker_selections"] == facts["natural_eos_run"]["frames"] + 1
+    assert facts["natural_eos_run"]["predictor_runs"] == facts["natural_eos_run"]["frames"] * 15
+    for k in ("natural_eos_run", "prefix_run", "two_frame_run", "ncnn_e2e_run"):
+        f = facts[k]
+        codes = f.get("codes", f.get("short_codes"))
+        frames = f.get("frames", f.get("short_frames"))
+        assert codes == 16 * frames
+
+
+def test_philox_known_answers(golden_dir):
+    L = oracle.lib()
+    n = 0
+    for line in open(os.path.join(golden_dir, "philox4x32_10_kat.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        v = [int(x, 16) for x in line.split()]
+        ctr = np.array(v[0:4], np.uint32)
+        key = np.array(v[4:6], np.uint32)
+        out = np.zeros(4, np.uint32)
+        L.oracle_philox(ctr.ctypes.data, key.ctypes.data, out.ctypes.data)
+        assert list(out) == v[6:10]
+        n += 1
+    assert n == 3
+
+
+def test_spec_exp_error_bound():
+    L = oracle.lib()
+    xs = np.concatenate([np.linspace(-86, 0, 20001), -np.geomspace(1e-8, 86, 5000)]).astype(np.float32)
+    got = np.array([L.oracle_spec_expf(float(x)) for x in xs], np.float64)
+    ref = np.exp(xs.astype(np.float64))
+    assert np.max(np.abs(got - ref) / ref) < 2.5e-7      # about 2 ulp of fp32
+    assert L.oracle_spec_expf(0.0) == 1.0
+    assert L.oracle_spec_expf(-87.0) == 0.0
+    # monotone on a fine grid (the draw relies on w ordering following l ordering)
+    grid = np.linspace(-20, 0, 4001).astype(np.float32)
+    g = np.array([L.oracle_spec_expf(float(x)) for x in grid])
+    assert np.all(np.diff(g) >= 0)
+
+
+def test_spec_log_error_bound():
+    L = oracle.lib()
+    us = np.concatenate([np.linspace(2 ** -24, 1 - 2 ** -24, 20001), np.geomspace(2 ** -24, 0.999, 5000)])
+    us = us.astype(np.float32)
+    got = np.array([L.oracle_spec_logf(float(u)) for u in us], np.float64)
+    ref = np.log(us.astype(np.float64))
+    assert np.max(np.abs(got - ref) / np.abs(ref)) < 4e-7
+    assert L.oracle_spec_logf(0.5) == pytest.approx(-math.log(2), rel=1e-7)
+
+
+def test_noise_uniform_properties():
+    L = oracle.lib()
+    us = np.array([L.oracle_noise_uniform(7, 0, 0, 0, t) for t in range(20000)], np.float64)
+    assert us.min() > 0 and us.max() < 1
+    scaled = us * 2 ** 24
+    assert np.all(scaled == np.round(scaled)) and np.all(scaled.astype(np.int64) % 2 == 1)
+    assert abs(us.mean() - 0.5) < 0.01
+    # each counter component changes the draw
+    a = L.oracle_noise_uniform(7, 1, 2, 3, 4)
+    for args in [(8, 1, 2, 3, 4), (7, 0, 2, 3, 4), (7, 1, 0, 3, 4), (7, 1, 2, 0, 4), (7, 1, 2, 3, 0)]:
+        assert L.oracle_noise_uniform(*args) != a
+
+
+def test_greedy_ties_go_to_lowest_index():
+    lg = np.zeros(V, np.float32)
+    lg[[17, 5, 900]] = 3.0
+    err, idx, margin, _ = oracle.sample(lg, sp(), talker=True)
+    assert err == 0 and idx == 5 and margin == 0.0
+    err, idx, _, _ = oracle.sample(lg[:2048], sp(), talker=False, eos=-1, sup_lo=0, sup_hi=0)
+    assert idx == 5
+
+
+@pytest.mark.parametrize("bad", [np.nan, np.inf])
+def test_nan_fails_closed(bad):
+    lg = np.random.default_rng(0).standard_normal(V).astype(np.float32)
+    lg[1234] = bad
+    for do_sample in (0, 1):
+        err, _, _, _ = oracle.sample(lg, sp(do_sample=do_sample), talker=True)
+        assert err == oracle.ERR_NAN
+    lg[1234] = -np.inf   # -inf is a legal (masked) logit
+    assert oracle.sample(lg, sp(), talker=True)[0] == 0
+
+
+def test_min_new_tokens_masks_eos_then_next_best():
+    lg = np.linspace(-1, 1, V).astype(np.float32)[::-1].copy()  # id 0 is the best code
+    lg[EOS] = 5.0
+    lg[7] = 4.0
+    s = sp(min_new_tokens=2)
+    for k, want in ((0, 7), (1, 7), (2, EOS), (3, EOS)):
+        err, idx, _, proc = oracle.sample(lg, s, talker=True, sel_index=k)
+        assert err == 0 and idx == want
+        assert (proc[EOS] == -np.inf) == (k < 2)
+
+
+def test_suppression_keeps_eos_only():
+    lg = np.random.default_rng(1).standard_normal(V).astype(np.float32)
+    lg[2500] = 10.0
+    err, idx, _, proc = oracle.sample(lg, sp(), talker=True)
+    assert idx != 2500 and idx < 2048 or idx == EOS
+    sup = np.r_[2048:3072]
+    sup = sup[sup != EOS]
+    assert np.all(proc[sup] == -np.inf)
+    assert proc[EOS] == lg[EOS]
+    assert np.array_equal(proc[:2048], lg[:2048])
+    # the predictor has no suppression: id 2047 can win there
+    lg2 = np.zeros(2048, np.float32)
+    lg2[2047] = 1.0
+    assert oracle.sample(lg2, sp(), talker=False, eos=-1, sup_lo=0, sup_hi=0)[1] == 2047
+
+
+def test_repetition_penalty_is_sign_aware():
+    rng = np.random.default_rng(2)
+    lg = rng.standard_normal(V).astype(np.float32)
+    seen = np.zeros(V, np.uint8)
+    ids = rng.choice(2048, 200, replace=False)
+    seen[ids] = 1
+    pen = np.float32(1.05)
+    err, _, _, proc = oracle.sample(lg, sp(repetition_penalty=1.05), talker=True, seen=seen)
+    want = lg.copy()
+    want[ids] = np.where(lg[ids] < 0, lg[ids] * pen, lg[ids] / pen).astype(np.float32)
+    sup = np.r_[2048:3072]
+    want[sup[sup != EOS]] = -np.inf
+    assert np.array_equal(proc, want)
+    # a seen id with the top logit loses to a close unseen one
+    lg = np.zeros(V, np.float32)
+    lg[10], lg[11] = 1.00, 0.97
+    seen = np.zeros(V, np.uint8)
+    seen[10] = 1
+    assert oracle.sample(lg, sp(repetition_penalty=1.05), talker=True, seen=seen)[1] == 11
+    assert oracle.sample(lg, sp(repetition_penalty=1.0), talker=True, seen=seen)[1] == 10
+    # negative logits move away from zero (become less likely)
+    lg = np.full(V, -5.0, np.float32)
+    lg[3], lg[4] = -1.00, -1.03
+    seen[:] = 0
+    seen[3] = 1
+    assert oracle.sample(lg, sp(repetition_penalty=1.05), talker=True, seen=seen)[1] == 4
+
+
+def _brute_kept(lg, T, top_k, top_p):
+    """Kept set of temperature -> top-k -> top-p, by sorting in fp64."""
+    l = lg.astype(np.float32) / np.float32(T)
+    l = l.astype(np.float64)
+    n = len(l)
+    keep = np.ones(n, bool)
+    if 0 < top_k < n:
+        kth = np.sort(l)[::-1][top_k - 1]
+        keep &= l >= kth
+    order = sorted(np.nonzero(keep)[0], key=lambda i: (-l[i], i))
+    p = np.exp(l[order] - l[order[0]])
+    p /= p.sum()
+    if top_p < 1:
+        c = np.concatenate([[0.0], np.cumsum(p)[:-1]])
+        ok = (c < top_p)
+        ok[0] = True
+        # avoid sets whose boundary sits within rounding of top_p
+        assert np.all(np.abs(c - top_p) > 1e-6)
+        order = [i for i, o in zip(order, ok) if o]
+    q = np.exp(l[order] - l[order[0]])
+    return np.array(order), q / q.sum()
+
+
+@pytest.mark.parametrize("T,top_k,top_p", [(1.0, 0, 1.0), (0.9, 5, 1.0), (0.7, 0, 0.8), (1.3, 6, 0.9)])
+def test_draw_follows_kept_softmax(T, top_k, top_p):
+    Vs = 12
+    rng = np.random.default_rng(3)
+    lg = (rng.standard_normal(Vs) * 0.8).astype(np.float32)
+    kept, p = _brute_kept(lg, T, top_k, top_p)
+    s = sp(do_sample=1, temperature=T, top_k=top_k, top_p=top_p, cp_do_sample=1, cp_temperature=T, cp_top_k=top_k,
+           cp_top_p=top_p)
+    n = 40000
+    counts = np.zeros(Vs, np.int64)
+    for f in range(n):
+        err, idx, _, _ = oracle.sample(lg, s, talker=False, eos=-1, sup_lo=0, sup_hi=0, row=1, frame=f, step=3)
+        assert err == 0
+        counts[idx] += 1
+    assert set(np.nonzero(counts)[0]) == set(kept.tolist())
+    exp = p * n
+    chi2 = float(np.sum((counts[kept] - exp) ** 2 / exp))
+    dof = len(kept) - 1
+    # 1e-4 upper tail of chi2(dof) is below dof + 8*sqrt(2 dof) + 20 for dof <= 12
+    assert chi2 < dof + 8 * math.sqrt(2 * max(dof, 1)) + 20, (chi2, dof)
+
+
+def test_topk_keeps_ties_at_threshold():
+    lg = np.array([3, 2, 2, 2, 1, 0], np.float32)
+    s = sp(do_sample=1, top_k=2, cp_do_sample=1, cp_top_k=2)
+    seen_ids = set()
+    for f in range(3000):
+        seen_ids.add(oracle.sample(lg, s, talker=False, eos=-1, sup_lo=0, sup_hi=0, frame=f)[1])
+    assert seen_ids == {0, 1, 2, 3}
+
+
+def test_same_seed_same_draws_and_seed_matters():
+    rng = np.random.default_rng(4)
+    lg = rng.standard_normal(V).astype(np.float32)
+    s1 = sp(do_sample=1, temperature=0.9, top_k=50, top_p=0.95, seed=7)
+    s2 = sp(do_sample=1, temperature=0.9, top_k=50, top_p=0.95, seed=8)
+    a = [oracle.sample(lg, s1, True, frame=f)[1] for f in range(200)]
+    b = [oracle.sample(lg, s1, True, frame=f)[1] for f in range(200)]
+    c = [oracle.sample(lg, s2, True, frame=f)[1] for f in range(200)]
+    assert a == b and a != c
