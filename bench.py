@@ -1,0 +1,334 @@
+#!/usr/bin/env python
+"""Benchmark of the Qwen3-TTS 12 Hz frame loop on one GB300 (or N replicas).
+
+A step is one talker step of the whole batch: the code predictor completes
+the pending frame of every live row (2-token prefill + 14 steps, 15 draws),
+the next talker input is assembled, the 28-layer talker runs and codebook 0
+is selected.  Metric: 16-code frames per second (frames emitted by all rows).
+
+Default workload: 0.6B-shaped model in bf16, batch 1, 128-row prompt, 64 text
+rows then tts_pad, 100 greedy frames (the latency path).  --workload 3/4/5
+select the 1.7B batch-1, batch-32 and batch-256 workloads.
+
+Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+ROWSTATE_BYTES = 16 * 4 + 128 * 4     # per-row state read back at the end of every call
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", type=int, default=2)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-frames", type=int, default=0, help="oracle frames timed for the CPU baseline (0: auto)")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- byte model
+def step_bytes(wl, live_pos):
+    """Algorithmic bytes of one step: every weight streamed once per use plus
+    the KV cache read (and written) by attention.  live_pos: talker position of
+    each live row's new token."""
+    d = wl.dims
+    wb = synth.weight_bytes(d, wl.dtype)
+    e = 4 if wl.dtype == synth.F32 else 2
+    G1 = d.n_groups - 1
+    weights = (d.n_layers * wb["talker_layer"] + wb["codec_head"] + wb["final_norm"]
+               + G1 * (d.cp_layers * wb["cp_layer"] + wb["cp_head"] + wb["cp_final_norm"] + wb["cp_proj"]))
+    per_pos = d.n_kv_heads * d.head_dim * 2 * e          # K and V of one position, one layer
+    kv = 0
+    cp_positions = 3 + sum(s + 2 for s in range(1, G1))  # prefill reads 1+2 positions, step s reads s+2
+    for p in live_pos:
+        kv += d.n_layers * ((p + 1) + 1) * per_pos         # read 0..p, write p
+        kv += d.cp_layers * (cp_positions + 16) * per_pos
+        kv += (d.n_groups + 1) * d.hidden * e              # embedding gathers
+    return weights, kv
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"q3_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---------------------------------------------------------------- oracle (CPU baseline / reference arm)
+def oracle_rate(wl, w, inp, n_frames):
+    """Oracle frames/s on row 0 of the workload: prefill (untimed), then n_frames steps."""
+    import oracle
+    rows = [0]
+    lens = [wl.prompt_lens[0]]
+    po = inp["prompt_offsets"]
+    to = inp["text_offsets"]
+    T = wl.frames
+    o = oracle.Oracle(wl.dims, wl.dtype, w, 1, wl.max_ctx, T, capture=False)
+    o.prefill(inp["prompt"][po[0]:po[1]], np.array([0, lens[0]], np.int32), inp["text"][to[0]:to[1]],
+              np.array([0, to[1] - to[0]], np.int32), inp["tts_pad"], [wl.rows[0]], rows)
+    n = min(n_frames, T)
+    t0 = time.perf_counter()
+    o.step(n)
+    dt = time.perf_counter() - t0
+    done = int(o.get("frames")[0])
+    return done / dt, done, dt
+
+
+def omp_threads():
+    v = os.environ.get("OMP_NUM_THREADS")
+    return int(v) if v else os.cpu_count()
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, wl, rank, world):
+    import torch
+    import speech_lm_decode_gb300 as q3
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = synth.make_weights(wl.dims, wl.dtype, wl.weight_seed)
+    inp = synth.make_inputs(wl)
+    dw = q3.to_device_weights(w, dev)
+    stream = torch.cuda.Stream(dev)
+    q = q3.Q3TTS(wl.dims, wl.dtype, dw, wl.batch, wl.max_ctx, max(max(wl.n_text), 1), stream=stream)
+    d_inp = {k: (torch.from_numpy(v).to(dev) if k in ("prompt", "text", "tts_pad") else v) for k, v in inp.items()}
+    codes_dev = torch.empty((wl.batch, wl.frames, wl.dims.n_groups), dtype=torch.int32, device=dev)
+    lens = np.array(wl.prompt_lens)
+
+    def prefill():
+        q.prefill(d_inp["prompt"], inp["prompt_offsets"], d_inp["text"], inp["text_offsets"], d_inp["tts_pad"],
+                  wl.rows)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    prefill()
+    steps_done = 0
+    frames = np.zeros(wl.batch, np.int32)
+    reasons = np.zeros(wl.batch, np.int32)
+    if args.warmup:
+        _, frames, reasons = q.step_frames(min(args.warmup, wl.frames), codes_out=codes_dev.view(-1))
+        steps_done = min(args.warmup, wl.frames)
+    kernels_per_step = q.step_kernel_count()
+    remaining = args.steps
+    total_ms = 0.0
+    total_frames = 0
+    wbytes_total = 0
+    kvbytes_total = 0
+    timed_steps = 0
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index)
+    with clocks:
+        while remaining > 0:
+            budget = wl.frames - steps_done
+            if budget <= 0 or np.all(reasons != q3.Q3_RUNNING):
+                prefill()
+                steps_done = 0
+                frames = np.zeros(wl.batch, np.int32)
+                reasons = np.zeros(wl.batch, np.int32)
+                continue
+            n = min(remaining, budget)
+            live_before = reasons == q3.Q3_RUNNING
+            f_before = frames.copy()
+            barrier()
+            ev0.record(stream)
+            _, frames, reasons = q.step_frames(n, codes_out=codes_dev.view(-1)[: wl.batch * n * wl.dims.n_groups])
+            ev1.record(stream)
+            barrier()
+            total_ms += ev0.elapsed_time(ev1)
+            total_frames += int(np.sum(frames - f_before))
+            # bytes: every step streams the weights; each row live at a step reads its cache
+            for j in range(n):
+                k = steps_done + j + 1
+                live = [int(lens[r] + k - 1) for r in range(wl.batch)
+                        if live_before[r] and (frames[r] > f_before[r] + j or (reasons[r] != q3.Q3_RUNNING and
+                                                                               frames[r] == f_before[r] + j))]
+                wb, kb = step_bytes(wl, live)
+                wbytes_total += wb
+                kvbytes_total += kb
+            steps_done += n
+            timed_steps += n
+            remaining -= n
+    times = torch.tensor([total_ms, float(total_frames), float(timed_steps)], dtype=torch.float64, device=dev)
+    if world > 1:
+        t = times.clone()
+        torch.distributed.all_reduce(t[0:1], op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(t[1:2], op=torch.distributed.ReduceOp.SUM)
+        times = t
+    max_ms, all_frames = float(times[0]), float(times[1])
+    res = dict(ms=max_ms, frames=all_frames, local_frames=total_frames, steps=timed_steps,
+               wbytes=wbytes_total, kvbytes=kvbytes_total, kernels_per_step=kernels_per_step,
+               clocks=clocks.summary(), local_ms=total_ms)
+
+    # e2e: the whole request through the C ABI from pinned host buffers, one call per step,
+    # codes read back to pinned host memory after every step
+    if not args.no_e2e:
+        h_prompt = torch.from_numpy(inp["prompt"]).pin_memory()
+        h_text = torch.from_numpy(inp["text"]).pin_memory()
+        h_pad = torch.from_numpy(inp["tts_pad"]).pin_memory()
+        h_codes = torch.empty((wl.batch, 1, wl.dims.n_groups), dtype=torch.int32).pin_memory()
+        barrier()
+        t0 = time.perf_counter()
+        q.prefill(h_prompt, inp["prompt_offsets"], h_text, inp["text_offsets"], h_pad, wl.rows)
+        nsteps = 0
+        fr = np.zeros(wl.batch, np.int32)
+        for _ in range(wl.frames):
+            _, fr, rs = q.step_frames(1, codes_out=h_codes)
+            nsteps += 1
+            if np.all(rs != q3.Q3_RUNNING):
+                break
+        barrier()
+        e2e_s = time.perf_counter() - t0
+        in_bytes = inp["prompt"].nbytes + inp["text"].nbytes + inp["tts_pad"].nbytes
+        res["e2e"] = dict(frames=int(fr.sum()), seconds=e2e_s, steps=nsteps,
+                          h2d_per_step=in_bytes / nsteps,
+                          d2h_per_step=wl.batch * wl.dims.n_groups * 4 + wl.batch * ROWSTATE_BYTES + 16)
+    q.close()
+    return res, w, inp
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    wl = synth.workload(args.workload)
+    metric = "16-code frames/sec"
+    unit = "frames/s"
+    config = {"workload": f"config {args.workload}: {wl.name}", "batch": wl.batch,
+              "prompt_rows": (wl.prompt_lens[0] if len(set(wl.prompt_lens)) == 1
+                              else f"{min(wl.prompt_lens)}..{max(wl.prompt_lens)}"),
+              "frames_per_request": wl.frames, "max_ctx": wl.max_ctx,
+              "l2": "no flush: every step streams >3 GB of weights, far above the 129 MB L2"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w = synth.make_weights(wl.dims, wl.dtype, wl.weight_seed)
+        inp = synth.make_inputs(wl)
+        n = max(1, min(args.steps, 40))
+        rate, done, dt = oracle_rate(wl, w, inp, n)
+        sample = f"row 0 of the workload, {done} frames after its prefill (untimed), {dt:.1f} s"
+        line = {"impl": "reference", "metric": metric, "value": rate, "unit": unit, "n_gpus": args.gpus,
+                "steps": done, "warmup": 0, "ms_per_step": 1000.0 * dt / max(done, 1), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded random init)",
+                "config": config,
+                "cpu_baseline": {"value": rate, "unit": unit, "cores": omp_threads(), "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": rate, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    res, w, inp = run_ours(args, wl, rank, world)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    pk, pk_kind = peaks()
+    sec = res["ms"] / 1000.0
+    value = res["frames"] / sec
+    bytes_total = res["wbytes"] + res["kvbytes"]
+    achieved = bytes_total / (res["local_ms"] / 1000.0) / 1e9
+    line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": res["steps"],
+            "warmup": args.warmup, "ms_per_step": res["ms"] / max(res["steps"], 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == synth.BF16 else "f32",
+            "data": "synthetic (seeded random-init weights, N(0,1) prompts)", "config": config,
+            "us_per_frame": 1e6 * sec / max(res["frames"], 1),
+            "roofline": {"bound": "hbm", "kernel": "frame step (all kernels of one talker step)",
+                         "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / pk["hbm_gbs"], "peak_kind": pk_kind,
+                         "traffic": None, "algorithmic_bytes_per_step": bytes_total / max(res["steps"], 1)},
+            "gpu_launches": res["kernels_per_step"] * res["steps"],
+            "clocks": res["clocks"]}
+    if "e2e" in res:
+        e = res["e2e"]
+        line["e2e"] = {"value": e["frames"] / e["seconds"], "unit": unit,
+                       "h2d_bytes_per_step": e["h2d_per_step"], "d2h_bytes_per_step": e["d2h_per_step"],
+                       "note": "prefill from pinned host + one q3tts_step_frames(1) per step, codes to pinned host"}
+    if not args.no_cpu_baseline and world == 1:
+        n = args.cpu_frames or (20 if wl.dims.hidden <= 1024 else 10)
+        rate, done, dt = oracle_rate(wl, w, inp, n)
+        line["cpu_baseline"] = {"value": rate, "unit": unit, "cores": omp_threads(), "kind": "oracle",
+                                "sample": f"row 0, {done} frames after prefill, {dt:.1f} s"}
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

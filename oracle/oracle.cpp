@@ -136,16 +136,36 @@ void rmsnorm(const double* x, const float* w, int n, double eps, double* y) {
     for (int i = 0; i < n; ++i) y[i] = x[i] * r * (double)w[i];
 }
 
-// Y[m][n] = sum_k W[n][k] * X[m][k]   (W row-major [N][K])
+// Y[m][n] = sum_k W[n][k] * X[m][k]   (W row-major [N][K]); every output
+// accumulates over k in increasing order.  With several tokens the running
+// sums of all tokens advance together (same order per output, same result).
 void linear(const Mat& W, size_t w_off, int N, int K, const double* X, int M, double* Y) {
-    #pragma omp parallel for schedule(static)
-    for (int n = 0; n < N; ++n) {
-        const size_t row = w_off + (size_t)n * K;
-        for (int m = 0; m < M; ++m) {
-            const double* x = X + (size_t)m * K;
+    if (M == 1) {
+        #pragma omp parallel for schedule(static)
+        for (int n = 0; n < N; ++n) {
+            const size_t row = w_off + (size_t)n * K;
             double acc = 0.0;
-            for (int k = 0; k < K; ++k) acc += W.at(row + k) * x[k];
-            Y[(size_t)m * N + n] = acc;
+            for (int k = 0; k < K; ++k) acc += W.at(row + k) * X[k];
+            Y[n] = acc;
+        }
+        return;
+    }
+    std::vector<double> Xt((size_t)K * M);   // X transposed: [K][M]
+    for (int m = 0; m < M; ++m)
+        for (int k = 0; k < K; ++k) Xt[(size_t)k * M + m] = X[(size_t)m * K + k];
+    #pragma omp parallel
+    {
+        std::vector<double> acc(M);
+        #pragma omp for schedule(static)
+        for (int n = 0; n < N; ++n) {
+            const size_t row = w_off + (size_t)n * K;
+            std::fill(acc.begin(), acc.end(), 0.0);
+            for (int k = 0; k < K; ++k) {
+                const double w = W.at(row + k);
+                const double* xk = &Xt[(size_t)k * M];
+                for (int m = 0; m < M; ++m) acc[m] += w * xk[m];
+            }
+            for (int m = 0; m < M; ++m) Y[(size_t)m * N + n] = acc[m];
         }
     }
 }
@@ -341,10 +361,15 @@ int sample_one(const float* logits_in, int V, const SampleParams& sp, bool talke
     if (sp.temperature != 1.0f)
         for (int i = 0; i < V; ++i) l[i] = l[i] / sp.temperature;
 
+    // Decision margin of a draw, in units of processed logits: the score ratio
+    // ln(s1/s2) of the winner, and how close the top-k / top-p boundaries are
+    // (a kept-set change under small logit errors can change the winner).
+    double boundary = INFINITY;
     if (sp.top_k > 0 && sp.top_k < V) {
         std::vector<float> sorted(l);
         std::sort(sorted.begin(), sorted.end(), [](float a, float b) { return a > b; });
         float vk = sorted[sp.top_k - 1];
+        if (sorted[sp.top_k] != -INFINITY) boundary = (double)vk - (double)sorted[sp.top_k];
         for (int i = 0; i < V; ++i)
             if (l[i] < vk) l[i] = -INFINITY;
     }
@@ -369,6 +394,7 @@ int sample_one(const float* logits_in, int V, const SampleParams& sp, bool talke
         int64_t C = 0;
         for (size_t j = 0; j < kept.size(); ++j) {
             if (j == 0 || (double)C < limit) nk.push_back(kept[j]);
+            if (j > 0 && C > 0 && limit > 0) boundary = std::min(boundary, std::fabs(std::log((double)C / limit)));
             C += W[kept[j]];
         }
         kept.swap(nk);
@@ -390,7 +416,7 @@ int sample_one(const float* logits_in, int V, const SampleParams& sp, bool talke
         }
     }
     *out_id = best;
-    *out_margin = have2 ? std::log((double)bs / (double)second) : INFINITY;
+    *out_margin = std::min(have2 ? std::log((double)bs / (double)second) : INFINITY, boundary);
     return ERR_OK;
 }
 

@@ -1,0 +1,240 @@
+"""GB300 (sm_103a) Qwen3-TTS 12 Hz frame loop: Python binding of libq3tts.so.
+
+Argument marshalling only: every step of the frame loop runs in the library's
+CUDA kernels.  PyTorch provides device memory and the stream.  The library
+must have been built (``speech_lm_decode_gb300.build.build()``); importing the
+binding without it raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libq3tts.so")
+
+Q3_OK, Q3_ERR_ARG, Q3_ERR_CUDA, Q3_ERR_CAPACITY, Q3_ERR_STATE, Q3_ERR_NAN, Q3_ERR_TIMEOUT, Q3_ERR_BOUNDS = range(8)
+Q3_F32, Q3_BF16 = 0, 1
+Q3_RUNNING, Q3_FINISHED_EOS, Q3_FINISHED_LENGTH, Q3_FINISHED_ERROR = 0, 1, 2, 3
+
+EXPORTS = ("q3tts_workspace_bytes", "q3tts_create", "q3tts_prefill", "q3tts_step_frames", "q3tts_set_capture",
+           "q3tts_sample_logits", "q3tts_step_kernel_count", "q3tts_last_error", "q3tts_destroy")
+
+
+class Q3Error(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"q3tts error {code}: {msg}")
+        self.code = code
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("n_layers", "hidden", "n_q_heads", "n_kv_heads", "head_dim", "ffn",
+                                            "codec_vocab", "cp_layers", "cp_hidden", "cp_ffn", "cp_vocab",
+                                            "n_groups", "eos_id", "suppress_lo", "suppress_hi")] + \
+              [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)] + \
+              [(n, ctypes.c_int) for n in ("dtype", "max_batch", "max_ctx", "max_text")]
+
+
+class BlockWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("attn_norm", "wqkv", "q_norm", "k_norm", "wo", "mlp_norm", "wgu",
+                                               "wd", "final_norm")]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("talker", BlockWeights), ("codec_emb", ctypes.c_void_p), ("codec_head", ctypes.c_void_p),
+                ("cp", BlockWeights), ("cp_emb", ctypes.c_void_p), ("cp_heads", ctypes.c_void_p),
+                ("cp_proj_w", ctypes.c_void_p), ("cp_proj_b", ctypes.c_void_p)]
+
+
+class Sampling(ctypes.Structure):
+    _fields_ = [("do_sample", ctypes.c_int), ("temperature", ctypes.c_float), ("top_k", ctypes.c_int),
+                ("top_p", ctypes.c_float), ("repetition_penalty", ctypes.c_float), ("min_new_tokens", ctypes.c_int),
+                ("seed", ctypes.c_uint64), ("max_frames", ctypes.c_int), ("force_eos_at_frame", ctypes.c_int),
+                ("cp_do_sample", ctypes.c_int), ("cp_temperature", ctypes.c_float), ("cp_top_k", ctypes.c_int),
+                ("cp_top_p", ctypes.c_float)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libq3tts.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with speech_lm_decode_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32 = ctypes.c_void_p, ctypes.c_int
+        L.q3tts_workspace_bytes.restype = ctypes.c_size_t
+        L.q3tts_workspace_bytes.argtypes = [ctypes.POINTER(Config)]
+        L.q3tts_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), vp, ctypes.c_size_t, vp,
+                                   ctypes.POINTER(vp)]
+        L.q3tts_prefill.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp]
+        L.q3tts_step_frames.argtypes = [vp, i32, vp, vp, vp]
+        L.q3tts_set_capture.argtypes = [vp, i32, vp, vp, vp, i32]
+        L.q3tts_sample_logits.argtypes = [vp, i32, vp, i32, vp, vp, vp, i32, vp, vp]
+        L.q3tts_step_kernel_count.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+        L.q3tts_last_error.restype = ctypes.c_char_p
+        L.q3tts_last_error.argtypes = [vp]
+        L.q3tts_destroy.argtypes = [vp]
+        _lib = L
+    return _lib
+
+
+def make_config(dims, dtype: int, max_batch: int, max_ctx: int, max_text: int) -> Config:
+    c = Config()
+    for f, _ in Config._fields_:
+        if f == "dtype":
+            c.dtype = dtype
+        elif f == "max_batch":
+            c.max_batch = max_batch
+        elif f == "max_ctx":
+            c.max_ctx = max_ctx
+        elif f == "max_text":
+            c.max_text = max_text
+        else:
+            setattr(c, f, getattr(dims, f))
+    return c
+
+
+def make_sampling(r) -> Sampling:
+    s = Sampling()
+    for f, _ in Sampling._fields_:
+        setattr(s, f, getattr(r, f))
+    return s
+
+
+def to_device_weights(w: dict, device="cuda") -> dict:
+    """Host weight arrays (bf16 as uint16 bit patterns) -> device tensors of the same layout."""
+    import torch
+
+    def dev(a):
+        if a is None:
+            return None
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            t = t.view(torch.bfloat16)
+        return t.to(device)
+    out = {}
+    for k, v in w.items():
+        out[k] = {kk: dev(vv) for kk, vv in v.items()} if isinstance(v, dict) else dev(v)
+    return out
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr()
+    return t.ctypes.data
+
+
+def make_weights(dw: dict) -> Weights:
+    ws = Weights()
+    for blk in ("talker", "cp"):
+        b = getattr(ws, blk)
+        for k, _ in BlockWeights._fields_:
+            setattr(b, k, _ptr(dw[blk][k]))
+    for k in ("codec_emb", "codec_head", "cp_emb", "cp_heads", "cp_proj_w", "cp_proj_b"):
+        setattr(ws, k, _ptr(dw.get(k)))
+    return ws
+
+
+class Q3TTS:
+    """One handle: model weights (borrowed device tensors), a workspace and a stream."""
+
+    def __init__(self, dims, dtype: int, device_weights: dict, max_batch: int, max_ctx: int, max_text: int,
+                 stream=None):
+        import torch
+        self._dw = device_weights
+        self.dims, self.dtype = dims, dtype
+        self.cfg = make_config(dims, dtype, max_batch, max_ctx, max_text)
+        nbytes = lib().q3tts_workspace_bytes(ctypes.byref(self.cfg))
+        if nbytes == 0:
+            raise Q3Error(Q3_ERR_ARG, "invalid configuration")
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        self._w = make_weights(device_weights)
+        h = ctypes.c_void_p()
+        rc = lib().q3tts_create(ctypes.byref(self.cfg), ctypes.byref(self._w), self.workspace.data_ptr(), nbytes,
+                                self.stream.cuda_stream, ctypes.byref(h))
+        if rc:
+            raise Q3Error(rc, "q3tts_create failed")
+        self.h = h.value
+        self.batch = 0
+
+    def _check(self, rc):
+        if rc:
+            raise Q3Error(rc, lib().q3tts_last_error(self.h).decode())
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().q3tts_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def prefill(self, prompt, prompt_offsets, text, text_offsets, tts_pad, rows, check=True):
+        """prompt/text/tts_pad: fp32 numpy arrays or torch tensors (host or cuda)."""
+        B = len(rows)
+        po = np.ascontiguousarray(prompt_offsets, dtype=np.int32)
+        to = np.ascontiguousarray(text_offsets, dtype=np.int32)
+        sp = (Sampling * B)(*[make_sampling(r) for r in rows])
+        keep = [prompt, text, tts_pad]
+        code0 = np.full(B, -1, np.int32)
+        rc = lib().q3tts_prefill(self.h, B, _ptr(prompt), po.ctypes.data,
+                                 _ptr(text) if text is not None and len(text) else None, to.ctypes.data,
+                                 _ptr(tts_pad), ctypes.cast(sp, ctypes.c_void_p), code0.ctypes.data)
+        del keep
+        if check:
+            self._check(rc)
+        self.batch = B
+        return code0 if check else (rc, code0)
+
+    def step_frames(self, n: int, codes_out=None, check=True):
+        """Run n talker steps.  codes_out: None (host numpy returned), or a
+        [B, n, G] int32 numpy array / torch tensor to fill."""
+        B, G = self.batch, self.dims.n_groups
+        out = np.empty((B, n, G), np.int32) if codes_out is None else codes_out
+        frames = np.zeros(B, np.int32)
+        reasons = np.zeros(B, np.int32)
+        rc = lib().q3tts_step_frames(self.h, n, _ptr(out), frames.ctypes.data, reasons.ctypes.data)
+        if check:
+            self._check(rc)
+            return out, frames, reasons
+        return rc, out, frames, reasons
+
+    def step_kernel_count(self) -> int:
+        n = ctypes.c_int(0)
+        self._check(lib().q3tts_step_kernel_count(self.h, ctypes.byref(n)))
+        return n.value
+
+    def set_capture(self, rows, talker_logits=None, cp_logits=None, max_frames=0):
+        r = np.ascontiguousarray(rows, dtype=np.int32)
+        self._cap = (r, talker_logits, cp_logits)
+        self._check(lib().q3tts_set_capture(self.h, len(r), r.ctypes.data if len(r) else None, _ptr(talker_logits),
+                                            _ptr(cp_logits), max_frames))
+
+    def sample_logits(self, logits, talker: bool, params, sel_index, step: int, noise_row, seen=None, check=True):
+        """Processors + draw on [n, V] fp32 logits (numpy or torch, host or cuda) -> ids [n]."""
+        n = len(params)
+        sp = (Sampling * n)(*[make_sampling(r) for r in params])
+        sel = np.ascontiguousarray(sel_index, dtype=np.int32)
+        nr = np.ascontiguousarray(noise_row, dtype=np.int32)
+        if isinstance(logits, np.ndarray):
+            logits = np.ascontiguousarray(logits, dtype=np.float32)
+        if isinstance(seen, np.ndarray):
+            seen = np.ascontiguousarray(seen, dtype=np.uint8)
+        ids = np.full(n, -1, np.int32)
+        rc = lib().q3tts_sample_logits(self.h, n, _ptr(logits), int(talker), ctypes.cast(sp, ctypes.c_void_p),
+                                       _ptr(seen), sel.ctypes.data, step, nr.ctypes.data, ids.ctypes.data)
+        if check:
+            self._check(rc)
+            return ids
+        return rc, ids

@@ -1,0 +1,300 @@
+// Tensor-core projections for many tokens at once (large batches, prefill
+// chunks): Y[m][n] (+)= sum_k W[n][k] X[m][k], bf16 operands, fp32 accumulate.
+//
+// The weight matrix is the MMA's A operand (128 weight rows per tile) and the
+// tokens are its N dimension (NT tokens per tile), so D[n][m] = W_tile . X^T
+// lives in tensor memory as 128 lanes (weight rows) x NT fp32 columns.
+//   - TMA (cp.async.bulk.tensor, 128-byte swizzle) stages 64-wide K slices of
+//     both operands into a 4-deep shared-memory ring (mbarrier completion);
+//   - one thread issues tcgen05.mma (kind::f16, M=128, N=NT, K=16 per
+//     instruction) and commits each stage back to the producer;
+//   - after the last stage, the four warps read their 32 TMEM lanes with
+//     tcgen05.ld and apply the epilogue (store / residual add / bias, or
+//     SiLU(g)*u for the stacked gate/up weights, which uses two accumulators).
+// Every mbarrier wait is bounded; an expired wait sets the timeout error bit,
+// the CTA skips its remaining work, frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace q3 {
+
+namespace {
+
+constexpr int BM = 128;        // weight rows per tile (MMA M)
+constexpr int BK = 64;         // K per stage (one 128-byte swizzle row of bf16)
+constexpr int STAGES = 4;
+constexpr long long TC_WAIT_LIMIT = 2000000000LL;
+
+__device__ __forceinline__ uint32_t s_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mb_init(uint64_t* b, unsigned n) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(s_u32(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mb_expect_tx(uint64_t* b, unsigned bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+                 ::"r"(s_u32(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mb_try(uint64_t* b, unsigned parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(s_u32(b)), "r"(parity) : "memory");
+    return ok != 0;
+}
+__device__ bool mb_wait(uint64_t* b, unsigned parity, int* err) {
+    if (mb_try(b, parity)) return true;
+    const long long t0 = clock64();
+    while (!mb_try(b, parity))
+        if (clock64() - t0 > TC_WAIT_LIMIT) {
+            atomicOr(err, ERRB_TIMEOUT);
+            return false;
+        }
+    return true;
+}
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(s_u32(dst)), "l"((uint64_t)map), "r"(x), "r"(y), "r"(s_u32(bar)) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major tile with 128-byte swizzle, rows of
+// 128 bytes, 8-row core groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);       // start address
+    d |= (uint64_t)1 << 16;                          // leading byte offset (unused for this layout)
+    d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset
+    d |= (uint64_t)1 << 46;                          // descriptor version
+    d |= (uint64_t)2 << 61;                          // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 D, bf16 A and B, both K-major.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, int acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(s_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int NT, bool GATED>
+struct TcSmem {
+    alignas(1024) bf16 a[STAGES][BM * BK];
+    alignas(1024) bf16 a2[GATED ? STAGES : 1][GATED ? BM * BK : 8];
+    alignas(1024) bf16 b[STAGES][NT * BK];
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t done;
+    uint32_t tmem;
+};
+
+template <int NT>
+constexpr uint32_t tmem_cols(bool gated) {
+    const int need = gated ? 2 * NT : NT;
+    return need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
+}
+
+template <int NT, bool GATED>
+__global__ void __launch_bounds__(128, 1) umma_linear_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                             const __grid_constant__ CUtensorMap tmX, int N, int K,
+                                                             int M, float* __restrict__ Y, int ldy,
+                                                             const float* __restrict__ bias, int accumulate, int F,
+                                                             bf16* __restrict__ Gout, int ldg, int* err) {
+    extern __shared__ __align__(1024) unsigned char raw[];
+    // 1024-byte alignment of the swizzled tiles
+    unsigned char* base = (unsigned char*)(((uintptr_t)raw + 1023) & ~(uintptr_t)1023);
+    TcSmem<NT, GATED>& s = *reinterpret_cast<TcSmem<NT, GATED>*>(base);
+    constexpr uint32_t COLS = tmem_cols<NT>(GATED);
+    constexpr uint32_t IDESC = make_idesc(BM, NT);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * BM, m0 = blockIdx.y * NT;
+    const int nk = (K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) { mb_init(&s.full[i], 1); mb_init(&s.empty[i], 1); }
+        mb_init(&s.done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(s_u32(&s.tmem)),
+                     "r"(COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s.tmem;
+    bool ok = true;
+
+    if (warp == 0 && lane == 0) {
+        // producer: K slices of W (and of the up half) and of X
+        const unsigned bytes = (unsigned)((BM * (GATED ? 2 : 1) + NT) * BK * sizeof(bf16));
+        for (int kb = 0; kb < nk && ok; ++kb) {
+            const int st = kb % STAGES;
+            const unsigned round = kb / STAGES;
+            if (round > 0 && !mb_wait(&s.empty[st], (round - 1) & 1, err)) { ok = false; break; }
+            mb_expect_tx(&s.full[st], bytes);
+            tma_2d(s.a[st], &tmW, kb * BK, n0, &s.full[st]);
+            if (GATED) tma_2d(s.a2[st], &tmW, kb * BK, F + n0, &s.full[st]);
+            tma_2d(s.b[st], &tmX, kb * BK, m0, &s.full[st]);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer
+        for (int kb = 0; kb < nk && ok; ++kb) {
+            const int st = kb % STAGES;
+            if (!mb_wait(&s.full[st], (kb / STAGES) & 1, err)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t da = sw128_desc(s_u32(s.a[st]));
+            const uint64_t db = sw128_desc(s_u32(s.b[st]));
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+                // advance 16 bf16 (32 bytes) along K inside the swizzled row
+                umma(tmem, da + 2 * kk, db + 2 * kk, IDESC, (kb | kk) != 0);
+                if (GATED) {
+                    const uint64_t da2 = sw128_desc(s_u32(s.a2[st]));
+                    umma(tmem + NT, da2 + 2 * kk, db + 2 * kk, IDESC, (kb | kk) != 0);
+                }
+            }
+            umma_commit(&s.empty[st]);
+        }
+        if (ok) umma_commit(&s.done);
+    }
+    __syncwarp();
+    // epilogue: warp w owns TMEM lanes 32w..32w+31 (weight rows n0+32w..)
+    const bool have = __all_sync(0xffffffffu, mb_wait(&s.done, 0, err));
+    tc_fence_after();
+    if (have) {
+        const int n = n0 + warp * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll 1
+        for (int c0 = 0; c0 < NT; c0 += 16) {
+            float v[16];
+            tmem_ld16(lane_base + c0, v);
+            if (GATED) {
+                float u[16];
+                tmem_ld16(lane_base + NT + c0, u);
+                if (n < F) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int m = m0 + c0 + j;
+                        if (m < M) Gout[(size_t)m * ldg + n] = __float2bfloat16_rn(v[j] / (1.0f + expf(-v[j])) * u[j]);
+                    }
+                }
+            } else if (n < N) {
+                const float bn = bias ? bias[n] : 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int m = m0 + c0 + j;
+                    if (m < M) {
+                        float* y = Y + (size_t)m * ldy + n;
+                        *y = accumulate ? *y + v[j] + bn : v[j] + bn;
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(COLS) : "memory");
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }
+    return fn;
+}
+
+// 2-D bf16 map over [rows][cols] (row stride ld elements), box [box_rows][64].
+bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int ld, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * sizeof(bf16)};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NT, bool GATED>
+cudaError_t launch_tc(const void* W, int N, int K, const void* X, int ldx, int M, float* Y, int ldy,
+                      const float* bias, int accumulate, int F, bf16* G, int ldg, int* err, cudaStream_t st) {
+    CUtensorMap mw, mx;
+    const int wrows = GATED ? 2 * F : N;
+    if (!make_map(&mw, W, wrows, K, K, BM) || !make_map(&mx, X, M, K, ldx, NT)) return cudaErrorInvalidValue;
+    const size_t smem = sizeof(TcSmem<NT, GATED>) + 1024;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(umma_linear_kernel<NT, GATED>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    dim3 grid((N + BM - 1) / BM, (M + NT - 1) / NT);
+    umma_linear_kernel<NT, GATED><<<grid, 128, smem, st>>>(mw, mx, N, K, M, Y, ldy, bias, accumulate, F, G, ldg, err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_available() { return encode_fn() != nullptr; }
+
+// Tokens per tile: the largest of 32/64/128 that still gives >= ~150 tiles.
+static int pick_nt(int N, int M) {
+    const int nt_rows = (N + BM - 1) / BM;
+    for (int nt : {128, 64})
+        if (nt <= ((M + 31) / 32) * 32 && nt_rows * ((M + nt - 1) / nt) >= 150) return nt;
+    return 32;
+}
+
+cudaError_t launch_linear_tc(const void* W, int N, int K, const void* X, int ldx, int M, float* Y, int ldy,
+                             const float* bias, int accumulate, int* err, cudaStream_t st) {
+    switch (pick_nt(N, M)) {
+        case 128: return launch_tc<128, false>(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, err, st);
+        case 64: return launch_tc<64, false>(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, err, st);
+        default: return launch_tc<32, false>(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, err, st);
+    }
+}
+
+cudaError_t launch_linear_gated_tc(const void* W, int F, int K, const void* X, int ldx, int M, void* out, int ldo,
+                                   int* err, cudaStream_t st) {
+    switch (pick_nt(F, M)) {
+        case 128: return launch_tc<128, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, (bf16*)out, ldo, err, st);
+        case 64: return launch_tc<64, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, (bf16*)out, ldo, err, st);
+        default: return launch_tc<32, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, (bf16*)out, ldo, err, st);
+    }
+}
+
+}  // namespace q3

@@ -1,0 +1,86 @@
+// Host-callable launchers of the q3tts kernels.  Every launcher enqueues on
+// `st` and returns the launch status (cudaGetLastError).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "q3tts.h"
+
+namespace q3 {
+
+struct RowState;
+
+// ---------------------------------------------------------------- linear.cu
+// Y[m][n] (+)= sum_k W[n][k] X[m][k] (+ bias[n]); W [N][K] and X [M][K] in the
+// model dtype, Y fp32.  accumulate: add into Y (residual).  M rows of X with
+// leading dimension ldx; Y leading dimension ldy.
+cudaError_t launch_linear(int dtype, const void* W, int N, int K, const void* X, int ldx, int M, float* Y, int ldy,
+                          const float* bias, int accumulate, int* err, cudaStream_t st);
+// SwiGLU projection: out[m][n] = round(silu(g) * u) with g = W[n].x, u = W[F+n].x,
+// W [2F][K]; out in the model dtype with leading dimension ldo.
+cudaError_t launch_linear_gated(int dtype, const void* W, int F, int K, const void* X, int ldx, int M, void* out,
+                                int ldo, int* err, cudaStream_t st);
+// tensor-core (tcgen05) variants for bf16 and many tokens (gemm_tc.cu)
+bool tc_available();
+cudaError_t launch_linear_tc(const void* W, int N, int K, const void* X, int ldx, int M, float* Y, int ldy,
+                             const float* bias, int accumulate, int* err, cudaStream_t st);
+cudaError_t launch_linear_gated_tc(const void* W, int F, int K, const void* X, int ldx, int M, void* out, int ldo,
+                                   int* err, cudaStream_t st);
+// minimum token count for the tensor-core path (0 disables it)
+void set_tc_min_tokens(int m);
+// out[row(m)] = round(x[m] * rsqrt(mean(x[m]^2) + eps) * w); optionally hout
+// (fp32, unrounded).  out_row: NULL = identity, else out row per input row
+// (negative: skip).
+cudaError_t launch_rmsnorm(int dtype, const float* x, int ldx, int M, const float* w, int n, float eps, void* out,
+                           int ldo, float* hout, int ldh, const int* out_row, cudaStream_t st);
+// out[m][i] = round(x[m][i]) (model dtype)
+cudaError_t launch_to_operand(int dtype, const float* x, int ldx, int M, int n, void* out, int ldo, cudaStream_t st);
+
+// ---------------------------------------------------------------- attention.cu
+// Per token m (row tok_row[m], position tok_pos[m] >= 0): per-head RMSNorm of
+// q and k, RoPE at the position, q written back in place, k and v appended to
+// the layer's cache [maxB][nkv][cap][128].  tok_pos < 0: token skipped.
+cudaError_t launch_qk_rope_kv(int dtype, float* qkv, int ldq, int M, int nq, int nkv, const float* q_norm,
+                              const float* k_norm, float eps, const float* rope_cs, int rope_rows, void* Kc, void* Vc,
+                              int cap, const int* tok_row, const int* tok_pos, int* err, cudaStream_t st);
+// Split-KV grouped-query decode attention over positions 0..tok_pos[m] of the
+// token's row, then the combine writing the O-projection operand [M][nq*128].
+cudaError_t launch_attention(int dtype, const float* qkv, int ldq, int M, int nq, int nkv, const void* Kc,
+                             const void* Vc, int cap, const int* tok_row, const int* tok_pos, int n_splits,
+                             float* part_m, float* part_l, float* part_acc, void* out, int ldo, cudaStream_t st);
+
+// ---------------------------------------------------------------- sampler.cu
+size_t sampler_smem_bytes();
+cudaError_t sampler_init();
+// Talker selection for every unfinished row of the batch (see q3tts.h).
+cudaError_t launch_talker_sample(const float* logits, int V, int B, RowState* rs, const q3tts_sampling* P, int eos,
+                                 int sup_lo, int sup_hi, int advance_pos, int* err, float* cap_logits,
+                                 const int* cap_slot, int cap_T, cudaStream_t st);
+// Predictor draw s (0..14) -> codebook s+1 of frame sel-1, for unfinished rows.
+cudaError_t launch_cp_sample(const float* logits, int V, int B, RowState* rs, const q3tts_sampling* P, int s,
+                             int32_t* codes_ws, int frames_cap, int* err, float* cap_logits, const int* cap_slot,
+                             int cap_T, int n_groups, cudaStream_t st);
+// Standalone processors + draw on given logit sets.
+cudaError_t launch_sample_sets(const float* logits, int n, int V, int talker, const q3tts_sampling* P,
+                               const uint8_t* seen, const int32_t* sel_index, int step, const int32_t* noise_row,
+                               int eos, int sup_lo, int sup_hi, int32_t* ids, int* err, cudaStream_t st);
+
+// ---------------------------------------------------------------- loop.cu
+cudaError_t launch_prepare_step(RowState* rs, int B, int* t_row, int* t_pos, int* c_row, int* c_pos, int G1,
+                                cudaStream_t st);
+cudaError_t launch_talker_embed(int dtype, const RowState* rs, int B, const void* codec_emb, const void* cp_emb,
+                                int H, int V, int cpV, int G, const int32_t* codes_ws, int frames_cap,
+                                const float* text, const float* pad, float* x, int eos, int* err, cudaStream_t st);
+// Predictor prefill tokens [h, codec_emb(code0)] -> dst rows 2b, 2b+1 (width
+// H); also writes codes_ws[b][f][0] = code0.
+cudaError_t launch_cp_embed_prefill(int dtype, RowState* rs, int B, const float* h, const void* codec_emb, int H,
+                                    int V, int32_t* codes_ws, int frames_cap, float* dst, int* err, cudaStream_t st);
+// Predictor step s (1..14) token table[s-1](code_s) -> dst row b (width H).
+cudaError_t launch_cp_embed_step(int dtype, const RowState* rs, int B, const void* cp_emb, int H, int cpV, int s,
+                                 const int32_t* codes_ws, int frames_cap, float* dst, int* err, cudaStream_t st);
+
+// dst[b*pitch + j*G + q] = codes of frame f0+j of row b (-1 past the buffer).
+cudaError_t launch_pack_codes(const int32_t* codes_ws, int frames_cap, long f0, int n, int G, int B, int32_t* dst,
+                              long pitch, cudaStream_t st);
+
+}  // namespace q3

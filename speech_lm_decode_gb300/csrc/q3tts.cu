@@ -1,0 +1,722 @@
+// Host side of the C ABI in q3tts.h: validation, workspace layout, the
+// prefill, and the per-step kernel sequence recorded once as a CUDA graph and
+// replayed for every talker step (one host synchronisation per call).
+#include <chrono>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "frame_params.h"
+#include "kernels.h"
+
+using namespace q3;
+
+namespace {
+
+constexpr size_t ALIGN = 256;
+constexpr int PREFILL_CHUNK = 512;   // prompt tokens per prefill pass
+constexpr int MAX_SPLITS = 16;       // split-KV partitions per (token, kv head)
+constexpr int MIN_SAMPLE_SETS = 256; // staging for q3tts_sample_logits
+
+struct Layout {
+    size_t kvK, kvV, ckvK, ckvV, rope, rows, params, h, x, cx, tok, opA, opB, headop, qkv, pm, pl, pacc, logits,
+        cplogits, t_row, t_pos, c_row, c_pos, last_row, codes, codes_stage, text, pad, err, s_params, s_logits, s_sel, s_row, s_ids, s_seen, cap_slot,
+        fparams, fbar, fpart, fo, fact;
+    size_t total;
+    int mmax, kA, kB, rope_rows, frames_cap, n_sets, vmax, fsplits;
+};
+
+size_t esize(int dtype) { return dtype == Q3_BF16 ? 2 : 4; }
+
+Layout make_layout(const q3tts_config& c) {
+    Layout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off += (bytes + ALIGN - 1) / ALIGN * ALIGN;
+        return o;
+    };
+    const size_t e = esize(c.dtype);
+    const size_t B = (size_t)c.max_batch, hd = (size_t)c.head_dim;
+    const int nqkv = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+    L.mmax = std::max(std::min(PREFILL_CHUNK, c.max_batch * c.max_ctx), 2 * c.max_batch);
+    L.kA = std::max(std::max(c.hidden, c.cp_hidden), c.n_q_heads * c.head_dim);
+    L.kB = std::max(std::max(c.ffn, c.cp_ffn), c.hidden);
+    L.rope_rows = std::max(c.max_ctx, 16);
+    L.frames_cap = c.max_ctx;
+    L.n_sets = std::max(c.max_batch, MIN_SAMPLE_SETS);
+    L.vmax = std::max(c.codec_vocab, c.cp_vocab);
+    const size_t kv = (size_t)c.n_layers * B * c.n_kv_heads * c.max_ctx * hd * e;
+    L.kvK = take(kv);
+    L.kvV = take(kv);
+    const size_t ckv = (size_t)c.cp_layers * B * c.n_kv_heads * 16 * hd * e;
+    L.ckvK = take(ckv);
+    L.ckvV = take(ckv);
+    L.rope = take((size_t)L.rope_rows * (hd / 2) * 2 * sizeof(float));
+    L.rows = take(B * sizeof(RowState));
+    L.params = take(B * sizeof(q3tts_sampling));
+    L.h = take(B * c.hidden * sizeof(float));
+    L.x = take((size_t)L.mmax * c.hidden * sizeof(float));
+    L.cx = take(2 * B * c.cp_hidden * sizeof(float));
+    L.tok = take(2 * B * c.hidden * sizeof(float));
+    L.opA = take((size_t)L.mmax * L.kA * e);
+    L.opB = take((size_t)L.mmax * L.kB * e);
+    L.headop = take(B * c.hidden * e);
+    L.qkv = take((size_t)L.mmax * nqkv * sizeof(float));
+    const size_t np = (size_t)L.mmax * MAX_SPLITS * c.n_q_heads;
+    L.pm = take(np * sizeof(float));
+    L.pl = take(np * sizeof(float));
+    L.pacc = take(np * hd * sizeof(float));
+    L.logits = take(B * c.codec_vocab * sizeof(float));
+    L.cplogits = take(B * c.cp_vocab * sizeof(float));
+    L.t_row = take((size_t)L.mmax * sizeof(int));
+    L.t_pos = take((size_t)L.mmax * sizeof(int));
+    L.c_row = take((size_t)MAX_GROUPS * 2 * B * sizeof(int));
+    L.c_pos = take((size_t)MAX_GROUPS * 2 * B * sizeof(int));
+    L.last_row = take((size_t)L.mmax * sizeof(int));
+    L.codes = take(B * L.frames_cap * MAX_GROUPS * sizeof(int32_t));
+    L.codes_stage = take(B * L.frames_cap * MAX_GROUPS * sizeof(int32_t));
+    L.text = take(B * std::max(c.max_text, 1) * c.hidden * sizeof(float));
+    L.pad = take(c.hidden * sizeof(float));
+    L.err = take(4 * sizeof(int));
+    L.s_params = take((size_t)L.n_sets * sizeof(q3tts_sampling));
+    L.s_logits = take((size_t)L.n_sets * L.vmax * sizeof(float));
+    L.s_sel = take((size_t)L.n_sets * sizeof(int));
+    L.s_row = take((size_t)L.n_sets * sizeof(int));
+    L.s_ids = take((size_t)L.n_sets * sizeof(int));
+    L.s_seen = take((size_t)L.n_sets * L.vmax);
+    L.cap_slot = take(B * sizeof(int));
+    // persistent frame kernel (batch 1)
+    L.fsplits = std::max(1, std::min((c.max_ctx + 47) / 48, 16));
+    L.fparams = take(sizeof(FrameParams));
+    L.fbar = take(FRAME_BAR_WORDS * sizeof(unsigned));
+    L.fpart = take((size_t)2 * c.n_kv_heads * L.fsplits * (c.n_q_heads / c.n_kv_heads) * (HD + 2) * sizeof(float));
+    L.fo = take((size_t)2 * c.n_q_heads * HD * sizeof(float));
+    L.fact = take((size_t)2 * std::max(c.ffn, c.cp_ffn) * sizeof(float));
+    L.total = off;
+    return L;
+}
+
+bool config_ok(const q3tts_config* c, std::string* why) {
+    auto bad = [&](const char* m) { if (why) *why = m; return false; };
+    if (!c) return bad("config is NULL");
+    if (c->head_dim != HD) return bad("head_dim must be 128");
+    if (c->n_layers < 1 || c->cp_layers < 1) return bad("layer counts must be >= 1");
+    if (c->n_kv_heads < 1 || c->n_q_heads % c->n_kv_heads) return bad("n_q_heads must be a multiple of n_kv_heads");
+    const int g = c->n_q_heads / c->n_kv_heads;
+    if (g != 1 && g != 2 && g != 4) return bad("n_q_heads / n_kv_heads must be 1, 2 or 4");
+    if (c->n_q_heads + c->n_kv_heads > 32) return bad("n_q_heads + n_kv_heads must be <= 32");
+    for (int v : {c->hidden, c->ffn, c->cp_hidden, c->cp_ffn})
+        if (v < 8 || v % 8) return bad("hidden / ffn widths must be positive multiples of 8");
+    if (c->n_groups < 2 || c->n_groups > MAX_GROUPS) return bad("n_groups must be in [2, 16]");
+    if (c->codec_vocab < 2 || c->codec_vocab > MAX_VOCAB || c->cp_vocab < 2 || c->cp_vocab > MAX_VOCAB)
+        return bad("vocabularies must be in [2, 4096]");
+    if (c->eos_id < 0 || c->eos_id >= c->codec_vocab) return bad("eos_id out of range");
+    if (c->suppress_lo < 0 || c->suppress_hi > c->codec_vocab || c->suppress_lo > c->suppress_hi)
+        return bad("suppress range out of range");
+    if (c->dtype != Q3_F32 && c->dtype != Q3_BF16) return bad("dtype must be Q3_F32 or Q3_BF16");
+    if (c->max_batch < 1 || c->max_ctx < 2 || c->max_text < 0) return bad("bad max_batch / max_ctx / max_text");
+    if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return bad("bad rms_eps / rope_theta");
+    return true;
+}
+
+template <typename T>
+T* at(void* base, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(base) + off); }
+
+}  // namespace
+
+struct q3tts {
+    q3tts_config c;
+    q3tts_weights w;
+    Layout L;
+    void* ws = nullptr;
+    cudaStream_t st = nullptr;
+    bool own_stream = false;
+    std::string last_error;
+    int batch = 0;
+    bool prefilled = false;
+    long steps_done = 0;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    int graph_batch = -1;
+    float* cap_t = nullptr;
+    float* cap_c = nullptr;
+    int cap_T = 0;
+    bool capturing = false;
+    int splits_t = 1;
+    bool frame_ok = false;      // the persistent frame kernel can serve batch 1
+    size_t frame_smem = 0;
+    int frame_grid = 0;
+
+    template <typename T> T* p(size_t off) const { return at<T>(ws, off); }
+    RowState* rows() const { return p<RowState>(L.rows); }
+    int* err() const { return p<int>(L.err); }
+};
+
+namespace {
+
+int fail(q3tts* h, int code, const char* fmt, ...) {
+    if (h) {
+        char buf[512];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof buf, fmt, ap);
+        va_end(ap);
+        h->last_error = buf;
+    }
+    return code;
+}
+
+#define CK(call)                                                                                    \
+    do {                                                                                            \
+        cudaError_t e_ = (call);                                                                    \
+        if (e_ != cudaSuccess) return fail(h, Q3_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+    } while (0)
+
+// Opt-in launch-by-launch check (Q3TTS_DEBUG_SYNC=1): outside graph capture,
+// wait up to 20 s for each launch, report it on stderr, and end the process if
+// it did not finish (the driver then tears the context down).
+bool g_debug_sync = false;
+void debug_wait(cudaStream_t st, const char* what) {
+    if (!g_debug_sync) return;
+    cudaStreamCaptureStatus cs;
+    if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone) return;
+    const auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        const cudaError_t e = cudaStreamQuery(st);
+        const double dt = std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+        if (e == cudaSuccess) { fprintf(stderr, "[q3tts] ok %.3f ms  %s\n", dt * 1e3, what); return; }
+        if (e != cudaErrorNotReady) { fprintf(stderr, "[q3tts] error %s after %s\n", cudaGetErrorString(e), what); return; }
+        if (dt > 20.0) { fprintf(stderr, "[q3tts] DID NOT FINISH in 20 s: %s\n", what); fflush(stderr); std::_Exit(3); }
+    }
+}
+
+void invalidate_graph(q3tts* h) {
+    if (h->exec) cudaGraphExecDestroy(h->exec);
+    if (h->graph) cudaGraphDestroy(h->graph);
+    h->exec = nullptr;
+    h->graph = nullptr;
+    h->graph_batch = -1;
+}
+
+// One decoder stack over M tokens (talker or predictor), residual x [M][H].
+int enqueue_layers(q3tts* h, bool talker, int M, float* x, const int* trow, const int* tpos) {
+    const q3tts_config& c = h->c;
+    const q3tts_block_weights& bw = talker ? h->w.talker : h->w.cp;
+    const int L = talker ? c.n_layers : c.cp_layers;
+    const int H = talker ? c.hidden : c.cp_hidden;
+    const int F = talker ? c.ffn : c.cp_ffn;
+    const int cap = talker ? c.max_ctx : 16;
+    const int nq = c.n_q_heads, nkv = c.n_kv_heads, hd = c.head_dim;
+    const int nqkv = (nq + 2 * nkv) * hd;
+    const size_t e = esize(c.dtype);
+    const size_t kv_layer = (size_t)c.max_batch * nkv * cap * hd * e;
+    char* Kc = h->p<char>(talker ? h->L.kvK : h->L.ckvK);
+    char* Vc = h->p<char>(talker ? h->L.kvV : h->L.ckvV);
+    void* opA = h->p<void>(h->L.opA);
+    void* opB = h->p<void>(h->L.opB);
+    float* qkv = h->p<float>(h->L.qkv);
+    const int splits = talker ? (M <= 2 * c.max_batch ? h->splits_t : 1) : 1;
+    const float eps = c.rms_eps;
+    for (int l = 0; l < L; ++l) {
+        const char* wqkv = (const char*)bw.wqkv + (size_t)l * nqkv * H * e;
+        const char* wo = (const char*)bw.wo + (size_t)l * H * nq * hd * e;
+        const char* wgu = (const char*)bw.wgu + (size_t)l * 2 * F * H * e;
+        const char* wd = (const char*)bw.wd + (size_t)l * H * F * e;
+        CK(launch_rmsnorm(c.dtype, x, H, M, (const float*)bw.attn_norm + (size_t)l * H, H, eps, opA, H, nullptr, 0,
+                          nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
+        CK(launch_linear(c.dtype, wqkv, nqkv, H, opA, H, M, qkv, nqkv, nullptr, 0, h->err(), h->st)); debug_wait(h->st, "launch_linear");
+        CK(launch_qk_rope_kv(c.dtype, qkv, nqkv, M, nq, nkv, (const float*)bw.q_norm + (size_t)l * hd,
+                             (const float*)bw.k_norm + (size_t)l * hd, eps, h->p<float>(h->L.rope), h->L.rope_rows,
+                             Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos, h->err(), h->st)); debug_wait(h->st, "launch_qk_rope_kv");
+        CK(launch_attention(c.dtype, qkv, nqkv, M, nq, nkv, Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos,
+                            splits, h->p<float>(h->L.pm), h->p<float>(h->L.pl), h->p<float>(h->L.pacc), opA, nq * hd,
+                            h->st)); debug_wait(h->st, "launch_attention");
+        CK(launch_linear(c.dtype, wo, H, nq * hd, opA, nq * hd, M, x, H, nullptr, 1, h->err(), h->st)); debug_wait(h->st, "launch_linear");
+        CK(launch_rmsnorm(c.dtype, x, H, M, (const float*)bw.mlp_norm + (size_t)l * H, H, eps, opA, H, nullptr, 0,
+                          nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
+        CK(launch_linear_gated(c.dtype, wgu, F, H, opA, H, M, opB, F, h->err(), h->st)); debug_wait(h->st, "launch_linear_gated");
+        CK(launch_linear(c.dtype, wd, H, F, opB, F, M, x, H, nullptr, 1, h->err(), h->st)); debug_wait(h->st, "launch_linear");
+    }
+    return Q3_OK;
+}
+
+// Predictor tokens (talker width, in h->tok) -> predictor residual cx.
+int enqueue_cp_input(q3tts* h, int M) {
+    const q3tts_config& c = h->c;
+    if (c.hidden == c.cp_hidden) return Q3_OK;  // tokens were written to cx directly
+    void* opB = h->p<void>(h->L.opB);
+    CK(launch_to_operand(c.dtype, h->p<float>(h->L.tok), c.hidden, M, c.hidden, opB, c.hidden, h->st)); debug_wait(h->st, "launch_to_operand");
+    CK(launch_linear(c.dtype, h->w.cp_proj_w, c.cp_hidden, c.hidden, opB, c.hidden, M, h->p<float>(h->L.cx),
+                     c.cp_hidden, (const float*)h->w.cp_proj_b, 0, h->err(), h->st)); debug_wait(h->st, "launch_linear");
+    return Q3_OK;
+}
+
+// One talker step for the whole batch: complete frame k-1 through the code
+// predictor, assemble the next talker input, run the talker, select code0.
+int enqueue_frame(q3tts* h) {
+    CK(cudaMemsetAsync(h->p<unsigned>(h->L.fbar), 0, FRAME_BAR_WORDS * sizeof(unsigned), h->st));
+    CK(launch_frame(h->c.dtype, h->p<FrameParams>(h->L.fparams), h->frame_grid, h->frame_smem, h->st)); debug_wait(h->st, "launch_frame");
+    return Q3_OK;
+}
+
+int enqueue_step(q3tts* h) {
+    if (h->batch == 1 && h->frame_ok) return enqueue_frame(h);
+    const q3tts_config& c = h->c;
+    const int B = h->batch, G1 = c.n_groups - 1;
+    const size_t e = esize(c.dtype);
+    RowState* rs = h->rows();
+    const q3tts_sampling* P = h->p<q3tts_sampling>(h->L.params);
+    int* t_row = h->p<int>(h->L.t_row);
+    int* t_pos = h->p<int>(h->L.t_pos);
+    int* c_row = h->p<int>(h->L.c_row);
+    int* c_pos = h->p<int>(h->L.c_pos);
+    int32_t* codes = h->p<int32_t>(h->L.codes);
+    float* cx = h->p<float>(h->L.cx);
+    float* tok = (c.hidden == c.cp_hidden) ? cx : h->p<float>(h->L.tok);
+    void* opA = h->p<void>(h->L.opA);
+    float* cpl = h->p<float>(h->L.cplogits);
+    const int* slot = h->p<int>(h->L.cap_slot);
+    int r;
+
+    CK(launch_prepare_step(rs, B, t_row, t_pos, c_row, c_pos, G1, h->st)); debug_wait(h->st, "launch_prepare_step");
+    // code predictor: 2-token prefill -> head[0] -> codebook 1
+    CK(launch_cp_embed_prefill(c.dtype, rs, B, h->p<float>(h->L.h), h->w.codec_emb, c.hidden, c.codec_vocab, codes,
+                               h->L.frames_cap, tok, h->err(), h->st)); debug_wait(h->st, "launch_cp_embed_prefill");
+    if ((r = enqueue_cp_input(h, 2 * B))) return r;
+    if ((r = enqueue_layers(h, false, 2 * B, cx, c_row, c_pos))) return r;
+    CK(launch_rmsnorm(c.dtype, cx + c.cp_hidden, 2 * c.cp_hidden, B, (const float*)h->w.cp.final_norm, c.cp_hidden,
+                      c.rms_eps, opA, c.cp_hidden, nullptr, 0, nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
+    CK(launch_linear(c.dtype, h->w.cp_heads, c.cp_vocab, c.cp_hidden, opA, c.cp_hidden, B, cpl, c.cp_vocab, nullptr,
+                     0, h->err(), h->st)); debug_wait(h->st, "launch_linear");
+    CK(launch_cp_sample(cpl, c.cp_vocab, B, rs, P, 0, codes, h->L.frames_cap, h->err(), h->cap_c, slot, h->cap_T,
+                        c.n_groups, h->st)); debug_wait(h->st, "launch_cp_sample");
+    // 14 autoregressive steps: table[s-1](code s) at position s+1 -> head[s] -> codebook s+1
+    for (int s = 1; s < G1; ++s) {
+        CK(launch_cp_embed_step(c.dtype, rs, B, h->w.cp_emb, c.hidden, c.cp_vocab, s, codes, h->L.frames_cap, tok,
+                                h->err(), h->st)); debug_wait(h->st, "launch_cp_embed_step");
+        if ((r = enqueue_cp_input(h, B))) return r;
+        if ((r = enqueue_layers(h, false, B, cx, c_row + (size_t)s * 2 * B, c_pos + (size_t)s * 2 * B))) return r;
+        CK(launch_rmsnorm(c.dtype, cx, c.cp_hidden, B, (const float*)h->w.cp.final_norm, c.cp_hidden, c.rms_eps, opA,
+                          c.cp_hidden, nullptr, 0, nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
+        const char* head = (const char*)h->w.cp_heads + (size_t)s * c.cp_vocab * c.cp_hidden * e;
+        CK(launch_linear(c.dtype, head, c.cp_vocab, c.cp_hidden, opA, c.cp_hidden, B, cpl, c.cp_vocab, nullptr, 0,
+                         h->err(), h->st)); debug_wait(h->st, "launch_linear");
+        CK(launch_cp_sample(cpl, c.cp_vocab, B, rs, P, s, codes, h->L.frames_cap, h->err(), h->cap_c, slot, h->cap_T,
+                            c.n_groups, h->st)); debug_wait(h->st, "launch_cp_sample");
+    }
+    // talker step
+    float* x = h->p<float>(h->L.x);
+    CK(launch_talker_embed(c.dtype, rs, B, h->w.codec_emb, h->w.cp_emb, c.hidden, c.codec_vocab, c.cp_vocab,
+                           c.n_groups, codes, h->L.frames_cap, h->p<float>(h->L.text), h->p<float>(h->L.pad), x,
+                           c.eos_id, h->err(), h->st)); debug_wait(h->st, "launch_talker_embed");
+    if ((r = enqueue_layers(h, true, B, x, t_row, t_pos))) return r;
+    CK(launch_rmsnorm(c.dtype, x, c.hidden, B, (const float*)h->w.talker.final_norm, c.hidden, c.rms_eps, opA,
+                      c.hidden, h->p<float>(h->L.h), c.hidden, nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
+    float* logits = h->p<float>(h->L.logits);
+    CK(launch_linear(c.dtype, h->w.codec_head, c.codec_vocab, c.hidden, opA, c.hidden, B, logits, c.codec_vocab,
+                     nullptr, 0, h->err(), h->st)); debug_wait(h->st, "launch_linear");
+    CK(launch_talker_sample(logits, c.codec_vocab, B, rs, P, c.eos_id, c.suppress_lo, c.suppress_hi, 1, h->err(),
+                            h->cap_t, slot, h->cap_T, h->st)); debug_wait(h->st, "launch_talker_sample");
+    return Q3_OK;
+}
+
+// Record one talker step of the current batch as a CUDA graph.
+int record_step_graph(q3tts* h) {
+    CK(cudaStreamBeginCapture(h->st, cudaStreamCaptureModeThreadLocal));
+    int r = enqueue_step(h);
+    cudaGraph_t g = nullptr;
+    cudaError_t e = cudaStreamEndCapture(h->st, &g);
+    if (r) { if (g) cudaGraphDestroy(g); return r; }
+    if (e != cudaSuccess) return fail(h, Q3_ERR_CUDA, "graph capture: %s", cudaGetErrorString(e));
+    h->graph = g;
+    e = cudaGraphInstantiate(&h->exec, g, 0);
+    if (e != cudaSuccess) {
+        invalidate_graph(h);
+        return fail(h, Q3_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
+    }
+    h->graph_batch = h->batch;
+    return Q3_OK;
+}
+
+// Parameters of the persistent frame kernel (device copy in the workspace).
+int upload_frame_params(q3tts* h) {
+    if (!h->frame_ok) return Q3_OK;
+    const q3tts_config& c = h->c;
+    FrameParams P{};
+    auto blk = [&](PBlk& d, const q3tts_block_weights& w, bool talker) {
+        d.attn_norm = (const float*)w.attn_norm; d.wqkv = w.wqkv; d.q_norm = (const float*)w.q_norm;
+        d.k_norm = (const float*)w.k_norm; d.wo = w.wo; d.mlp_norm = (const float*)w.mlp_norm; d.wgu = w.wgu;
+        d.wd = w.wd; d.final_norm = (const float*)w.final_norm;
+        d.Kc = h->p<void>(talker ? h->L.kvK : h->L.ckvK);
+        d.Vc = h->p<void>(talker ? h->L.kvV : h->L.ckvV);
+        d.cap = talker ? c.max_ctx : 16;
+        d.L = talker ? c.n_layers : c.cp_layers;
+        d.H = talker ? c.hidden : c.cp_hidden;
+        d.F = talker ? c.ffn : c.cp_ffn;
+    };
+    blk(P.t, h->w.talker, true);
+    blk(P.c, h->w.cp, false);
+    P.codec_emb = h->w.codec_emb; P.codec_head = h->w.codec_head; P.cp_emb = h->w.cp_emb; P.cp_heads = h->w.cp_heads;
+    P.cp_proj_w = h->w.cp_proj_w; P.cp_proj_b = (const float*)h->w.cp_proj_b;
+    P.H = c.hidden; P.Hc = c.cp_hidden; P.V = c.codec_vocab; P.cpV = c.cp_vocab; P.G = c.n_groups;
+    P.nq = c.n_q_heads; P.nkv = c.n_kv_heads; P.eos = c.eos_id; P.sup_lo = c.suppress_lo; P.sup_hi = c.suppress_hi;
+    P.n_splits = h->L.fsplits;
+    P.kmax = std::max(std::max(std::max(c.hidden, c.cp_hidden), std::max(c.ffn, c.cp_ffn)), c.n_q_heads * HD);
+    P.max_batch = c.max_batch;
+    P.eps = c.rms_eps;
+    P.rope = h->p<float2>(h->L.rope); P.rope_rows = h->L.rope_rows;
+    P.rows = h->rows(); P.P = h->p<q3tts_sampling>(h->L.params);
+    P.x = h->p<float>(h->L.x); P.cx = h->p<float>(h->L.cx); P.h = h->p<float>(h->L.h);
+    P.qkv = h->p<float>(h->L.qkv); P.part = h->p<float>(h->L.fpart); P.o = h->p<float>(h->L.fo);
+    P.act = h->p<float>(h->L.fact); P.logits = h->p<float>(h->L.logits); P.cpl = h->p<float>(h->L.cplogits);
+    P.codes = h->p<int32_t>(h->L.codes); P.frames_cap = h->L.frames_cap;
+    P.text = h->p<float>(h->L.text); P.pad = h->p<float>(h->L.pad);
+    P.bar = h->p<unsigned>(h->L.fbar); P.err = h->err();
+    P.cap_t = h->cap_t; P.cap_c = h->cap_c; P.cap_slot = h->p<int>(h->L.cap_slot); P.cap_T = h->cap_T;
+    const size_t e = esize(c.dtype);
+    P.xin_bytes = (int)std::max((size_t)2 * P.kmax * e, (size_t)(2 * HD + 4 * HD + 2 * 8 * 2 + 8 * 2 * HD) * 4);
+    CK(cudaMemcpyAsync(h->p<FrameParams>(h->L.fparams), &P, sizeof P, cudaMemcpyHostToDevice, h->st));
+    CK(cudaStreamSynchronize(h->st));
+    return Q3_OK;
+}
+
+int read_errors(q3tts* h, const int* err_host) {
+    if (err_host[0] & ERRB_BOUNDS) return fail(h, Q3_ERR_BOUNDS, "device bounds check failed (id or position)");
+    if (err_host[0] & ERRB_NAN) return fail(h, Q3_ERR_NAN, "NaN or +inf logits at a selection");
+    if (err_host[0] & ERRB_TIMEOUT) return fail(h, Q3_ERR_TIMEOUT, "a device wait timed out");
+    return Q3_OK;
+}
+
+bool weights_ok(const q3tts_config& c, const q3tts_weights* w) {
+    if (!w) return false;
+    for (const q3tts_block_weights* b : {&w->talker, &w->cp})
+        if (!b->attn_norm || !b->wqkv || !b->q_norm || !b->k_norm || !b->wo || !b->mlp_norm || !b->wgu || !b->wd ||
+            !b->final_norm)
+            return false;
+    if (!w->codec_emb || !w->codec_head || !w->cp_emb || !w->cp_heads) return false;
+    if (c.hidden != c.cp_hidden && (!w->cp_proj_w || !w->cp_proj_b)) return false;
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t q3tts_workspace_bytes(const q3tts_config* cfg) {
+    if (!config_ok(cfg, nullptr)) return 0;
+    return make_layout(*cfg).total;
+}
+
+int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspace, size_t workspace_bytes,
+                 void* stream, q3tts_t** out) {
+    if (!out) return Q3_ERR_ARG;
+    *out = nullptr;
+    std::string why;
+    if (!config_ok(cfg, &why)) return Q3_ERR_ARG;
+    if (!weights_ok(*cfg, w)) return Q3_ERR_ARG;
+    const Layout L = make_layout(*cfg);
+    if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace % ALIGN)) return Q3_ERR_ARG;
+    q3tts* h = new q3tts();
+    h->c = *cfg;
+    h->w = *w;
+    h->L = L;
+    h->ws = workspace;
+    if (stream) {
+        h->st = (cudaStream_t)stream;
+    } else {
+        if (cudaStreamCreateWithFlags(&h->st, cudaStreamNonBlocking) != cudaSuccess) { delete h; return Q3_ERR_CUDA; }
+        h->own_stream = true;
+    }
+    if (sampler_init() != cudaSuccess) { q3tts_destroy(h); return Q3_ERR_CUDA; }
+    // persistent frame kernel for batch 1: needs GQ 2, fitting shared memory and
+    // one co-resident CTA per SM (cooperative launch)
+    {
+        int dev = 0, sms = 0, coop = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+        const int kmax = std::max(std::max(std::max(cfg->hidden, cfg->cp_hidden), std::max(cfg->ffn, cfg->cp_ffn)),
+                                  cfg->n_q_heads * HD);
+        const size_t e = esize(cfg->dtype);
+        const bool tiles_fit = (size_t)cfg->hidden * e * 2 <= 24 * 1024 && (size_t)cfg->cp_hidden * e * 2 <= 24 * 1024 &&
+                               (size_t)std::max(cfg->ffn, cfg->cp_ffn) * e <= 24 * 1024 &&
+                               (size_t)cfg->n_q_heads * HD * e <= 24 * 1024;
+        h->frame_smem = frame_smem_bytes(cfg->dtype, kmax);
+        const char* env = getenv("Q3TTS_FRAME_KERNEL");
+        const bool want = !(env && env[0] == '0');
+        h->frame_ok = want && coop && sms > 0 && h->frame_smem > 0 && tiles_fit &&
+                      cfg->n_q_heads == 2 * cfg->n_kv_heads && cfg->n_kv_heads * L.fsplits <= sms * 4;
+        if (h->frame_ok && frame_setup(cfg->dtype, h->frame_smem) != cudaSuccess) { cudaGetLastError(); h->frame_ok = false; }
+        h->frame_grid = sms;
+        const char* ds = getenv("Q3TTS_DEBUG_SYNC");
+        g_debug_sync = ds && ds[0] == '1';
+        const char* tc = getenv("Q3TTS_TENSOR_CORES");
+        set_tc_min_tokens(tc && tc[0] == '0' ? 0 : 16);
+    }
+    // split-KV partitions of the talker decode attention: enough blocks to fill
+    // the GPU twice at small batch, one split at large batch
+    const int blocks = cfg->max_batch * cfg->n_kv_heads;
+    int s = std::min((cfg->max_ctx + 31) / 32, (2 * 152 + blocks - 1) / blocks);
+    h->splits_t = std::max(1, std::min(s, MAX_SPLITS));
+    // RoPE table: cos, sin of pos * inv_freq_j, inv_freq_j = theta^(-2j/128) in
+    // fp32 and the angle formed in fp32 (inv_freq kept fp32 in bf16 models).
+    std::vector<float> rope((size_t)L.rope_rows * (HD / 2) * 2);
+    for (int p = 0; p < L.rope_rows; ++p)
+        for (int j = 0; j < HD / 2; ++j) {
+            const float inv = (float)std::pow((double)cfg->rope_theta, -2.0 * j / HD);
+            const float ang = (float)p * inv;
+            rope[((size_t)p * (HD / 2) + j) * 2 + 0] = (float)std::cos((double)ang);
+            rope[((size_t)p * (HD / 2) + j) * 2 + 1] = (float)std::sin((double)ang);
+        }
+    cudaError_t e = cudaMemcpyAsync(h->p<float>(L.rope), rope.data(), rope.size() * sizeof(float),
+                                    cudaMemcpyHostToDevice, h->st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->p<int>(L.cap_slot), 0xFF, (size_t)cfg->max_batch * sizeof(int), h->st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->p<int>(L.err), 0, 4 * sizeof(int), h->st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->st);
+    if (e != cudaSuccess) { q3tts_destroy(h); return Q3_ERR_CUDA; }
+    if (upload_frame_params(h) != Q3_OK) { q3tts_destroy(h); return Q3_ERR_CUDA; }
+    *out = h;
+    return Q3_OK;
+}
+
+void q3tts_destroy(q3tts_t* h) {
+    if (!h) return;
+    if (h->st) cudaStreamSynchronize(h->st);
+    invalidate_graph(h);
+    if (h->own_stream && h->st) cudaStreamDestroy(h->st);
+    delete h;
+}
+
+const char* q3tts_last_error(const q3tts_t* h) { return h ? h->last_error.c_str() : "NULL handle"; }
+
+int q3tts_prefill(q3tts_t* h, int batch, const float* prompt, const int32_t* prompt_offsets, const float* text,
+                  const int32_t* text_offsets, const float* tts_pad, const q3tts_sampling* rows_in,
+                  int32_t* code0_out) {
+    if (!h) return Q3_ERR_ARG;
+    const q3tts_config& c = h->c;
+    if (batch < 1 || batch > c.max_batch) return fail(h, Q3_ERR_CAPACITY, "batch %d outside 1..%d", batch, c.max_batch);
+    if (!prompt || !prompt_offsets || !text_offsets || !tts_pad || !rows_in)
+        return fail(h, Q3_ERR_ARG, "NULL argument");
+    if (prompt_offsets[0] != 0 || text_offsets[0] != 0) return fail(h, Q3_ERR_ARG, "offsets must start at 0");
+    long total_text = 0;
+    for (int r = 0; r < batch; ++r) {
+        const int len = prompt_offsets[r + 1] - prompt_offsets[r];
+        const int nt = text_offsets[r + 1] - text_offsets[r];
+        const q3tts_sampling& s = rows_in[r];
+        if (len < 1) return fail(h, Q3_ERR_ARG, "row %d: empty prompt", r);
+        if (nt < 0) return fail(h, Q3_ERR_ARG, "row %d: negative text count", r);
+        if (nt > c.max_text) return fail(h, Q3_ERR_CAPACITY, "row %d: %d text rows > max_text %d", r, nt, c.max_text);
+        if (s.max_frames < 0) return fail(h, Q3_ERR_ARG, "row %d: negative max_frames", r);
+        if ((long)len + s.max_frames > c.max_ctx)
+            return fail(h, Q3_ERR_CAPACITY, "row %d: prompt %d + max_frames %d > max_ctx %d", r, len, s.max_frames,
+                        c.max_ctx);
+        if ((s.do_sample && !(s.temperature > 0.f)) || (s.cp_do_sample && !(s.cp_temperature > 0.f)))
+            return fail(h, Q3_ERR_ARG, "row %d: temperature must be > 0 when sampling", r);
+        if (!(s.repetition_penalty > 0.f)) return fail(h, Q3_ERR_ARG, "row %d: repetition_penalty must be > 0", r);
+        total_text += nt;
+    }
+    if (total_text > 0 && !text) return fail(h, Q3_ERR_ARG, "text is NULL but rows have text");
+
+    if (batch != h->graph_batch) invalidate_graph(h);
+    h->batch = batch;
+    h->prefilled = false;
+    h->steps_done = 0;
+    const int H = c.hidden;
+
+    // per-row state and settings
+    std::vector<RowState> rs(batch);
+    std::memset(rs.data(), 0, rs.size() * sizeof(RowState));
+    for (int r = 0; r < batch; ++r) {
+        rs[r].pos = prompt_offsets[r + 1] - prompt_offsets[r];
+        rs[r].code0 = -1;
+        rs[r].n_text = text_offsets[r + 1] - text_offsets[r];
+        rs[r].text_off = r * c.max_text;
+    }
+    CK(cudaMemcpyAsync(h->rows(), rs.data(), rs.size() * sizeof(RowState), cudaMemcpyHostToDevice, h->st));
+    CK(cudaMemcpyAsync(h->p<q3tts_sampling>(h->L.params), rows_in, (size_t)batch * sizeof(q3tts_sampling),
+                       cudaMemcpyHostToDevice, h->st));
+    for (int r = 0; r < batch; ++r) {
+        const int nt = text_offsets[r + 1] - text_offsets[r];
+        if (nt > 0)
+            CK(cudaMemcpyAsync(h->p<float>(h->L.text) + (size_t)r * c.max_text * H,
+                               text + (size_t)text_offsets[r] * H, (size_t)nt * H * sizeof(float), cudaMemcpyDefault,
+                               h->st));
+    }
+    CK(cudaMemcpyAsync(h->p<float>(h->L.pad), tts_pad, H * sizeof(float), cudaMemcpyDefault, h->st));
+    CK(cudaMemsetAsync(h->p<int32_t>(h->L.codes), 0xFF,
+                       (size_t)c.max_batch * h->L.frames_cap * MAX_GROUPS * sizeof(int32_t), h->st));
+    CK(cudaMemsetAsync(h->err(), 0, 4 * sizeof(int), h->st));
+
+    // prompt through the talker, in chunks of whole tokens across rows
+    const int total = prompt_offsets[batch];
+    std::vector<int> trow(h->L.mmax), tpos(h->L.mmax), last(h->L.mmax);
+    std::vector<int> tok_row(total), tok_pos(total);
+    for (int r = 0; r < batch; ++r)
+        for (int p = prompt_offsets[r]; p < prompt_offsets[r + 1]; ++p) { tok_row[p] = r; tok_pos[p] = p - prompt_offsets[r]; }
+    float* x = h->p<float>(h->L.x);
+    void* headop = h->p<void>(h->L.headop);
+    const int chunk = std::min(PREFILL_CHUNK, h->L.mmax);
+    for (int t0 = 0; t0 < total; t0 += chunk) {
+        const int M = std::min(chunk, total - t0);
+        for (int m = 0; m < M; ++m) {
+            const int t = t0 + m;
+            trow[m] = tok_row[t];
+            tpos[m] = tok_pos[t];
+            last[m] = (t + 1 == prompt_offsets[tok_row[t] + 1]) ? tok_row[t] : -1;
+        }
+        CK(cudaMemcpyAsync(h->p<int>(h->L.t_row), trow.data(), M * sizeof(int), cudaMemcpyHostToDevice, h->st));
+        CK(cudaMemcpyAsync(h->p<int>(h->L.t_pos), tpos.data(), M * sizeof(int), cudaMemcpyHostToDevice, h->st));
+        CK(cudaMemcpyAsync(h->p<int>(h->L.last_row), last.data(), M * sizeof(int), cudaMemcpyHostToDevice, h->st));
+        CK(cudaMemcpyAsync(x, prompt + (size_t)t0 * H, (size_t)M * H * sizeof(float), cudaMemcpyDefault, h->st));
+        int r = enqueue_layers(h, true, M, x, h->p<int>(h->L.t_row), h->p<int>(h->L.t_pos));
+        if (r) return r;
+        CK(launch_rmsnorm(c.dtype, x, H, M, (const float*)h->w.talker.final_norm, H, c.rms_eps, headop, H,
+                          h->p<float>(h->L.h), H, h->p<int>(h->L.last_row), h->st)); debug_wait(h->st, "launch_rmsnorm");
+        // the host vectors are reused by the next chunk: let this chunk's copies finish
+        CK(cudaStreamSynchronize(h->st));
+    }
+    float* logits = h->p<float>(h->L.logits);
+    CK(launch_linear(c.dtype, h->w.codec_head, c.codec_vocab, H, headop, H, batch, logits, c.codec_vocab, nullptr, 0,
+                     h->err(), h->st)); debug_wait(h->st, "launch_linear");
+    CK(launch_talker_sample(logits, c.codec_vocab, batch, h->rows(), h->p<q3tts_sampling>(h->L.params), c.eos_id,
+                            c.suppress_lo, c.suppress_hi, 0, h->err(), h->cap_t, h->p<int>(h->L.cap_slot), h->cap_T,
+                            h->st)); debug_wait(h->st, "launch_talker_sample");
+    int err_host[4];
+    CK(cudaMemcpyAsync(err_host, h->err(), sizeof err_host, cudaMemcpyDeviceToHost, h->st));
+    CK(cudaMemcpyAsync(rs.data(), h->rows(), rs.size() * sizeof(RowState), cudaMemcpyDeviceToHost, h->st));
+    CK(cudaStreamSynchronize(h->st));
+    if (code0_out) {
+        std::vector<int32_t> c0(batch);
+        for (int r = 0; r < batch; ++r) c0[r] = rs[r].code0;
+        CK(cudaMemcpy(code0_out, c0.data(), batch * sizeof(int32_t), cudaMemcpyDefault));
+    }
+    h->prefilled = true;
+    return read_errors(h, err_host);
+}
+
+int q3tts_step_frames(q3tts_t* h, int n_frames, int32_t* codes_out, int32_t* frames_emitted,
+                      int32_t* finish_reason) {
+    if (!h) return Q3_ERR_ARG;
+    if (!h->prefilled) return fail(h, Q3_ERR_STATE, "q3tts_step_frames before q3tts_prefill");
+    if (n_frames < 0) return fail(h, Q3_ERR_ARG, "negative n_frames");
+    const q3tts_config& c = h->c;
+    const int B = h->batch;
+    if (n_frames > 0 && !h->exec) {
+        int r = record_step_graph(h);
+        if (r) return r;
+    }
+    for (int i = 0; i < n_frames; ++i) CK(cudaGraphLaunch(h->exec, h->st));
+    const long f0 = h->steps_done;
+    if (codes_out && n_frames > 0) {
+        cudaPointerAttributes pa;
+        const bool dev = cudaPointerGetAttributes(&pa, codes_out) == cudaSuccess &&
+                         (pa.type == cudaMemoryTypeDevice || pa.type == cudaMemoryTypeManaged);
+        cudaGetLastError();
+        const int G = c.n_groups;
+        if (dev) {
+            CK(launch_pack_codes(h->p<int32_t>(h->L.codes), h->L.frames_cap, f0, n_frames, G, B, codes_out,
+                                 (long)n_frames * G, h->st)); debug_wait(h->st, "launch_pack_codes");
+        } else {
+            // through the staging area, at most frames_cap frames at a time
+            for (long j0 = 0; j0 < n_frames; j0 += h->L.frames_cap) {
+                const long nc = std::min((long)h->L.frames_cap, n_frames - j0);
+                int32_t* stage = h->p<int32_t>(h->L.codes_stage);
+                CK(launch_pack_codes(h->p<int32_t>(h->L.codes), h->L.frames_cap, f0 + j0, (int)nc, G, B, stage,
+                                     nc * G, h->st)); debug_wait(h->st, "launch_pack_codes");
+                CK(cudaMemcpy2DAsync(codes_out + j0 * G, (size_t)n_frames * G * sizeof(int32_t), stage,
+                                     (size_t)nc * G * sizeof(int32_t), (size_t)nc * G * sizeof(int32_t), B,
+                                     cudaMemcpyDeviceToHost, h->st));
+            }
+        }
+    }
+    std::vector<RowState> rs(B);
+    int err_host[4];
+    CK(cudaMemcpyAsync(rs.data(), h->rows(), (size_t)B * sizeof(RowState), cudaMemcpyDeviceToHost, h->st));
+    CK(cudaMemcpyAsync(err_host, h->err(), sizeof err_host, cudaMemcpyDeviceToHost, h->st));
+    CK(cudaStreamSynchronize(h->st));
+    h->steps_done += n_frames;
+    for (int r = 0; r < B; ++r) {
+        if (frames_emitted) frames_emitted[r] = rs[r].frames;
+        if (finish_reason) finish_reason[r] = rs[r].finished ? rs[r].reason : Q3_RUNNING;
+    }
+    return read_errors(h, err_host);
+}
+
+int q3tts_set_capture(q3tts_t* h, int n_rows, const int32_t* rows, float* talker_logits, float* cp_logits,
+                      int max_frames) {
+    if (!h) return Q3_ERR_ARG;
+    if (n_rows < 0 || n_rows > h->c.max_batch || (n_rows > 0 && (!rows || !talker_logits || !cp_logits)) ||
+        max_frames < 0)
+        return fail(h, Q3_ERR_ARG, "bad capture arguments");
+    std::vector<int> slot(h->c.max_batch, -1);
+    for (int i = 0; i < n_rows; ++i) {
+        if (rows[i] < 0 || rows[i] >= h->c.max_batch) return fail(h, Q3_ERR_ARG, "capture row out of range");
+        slot[rows[i]] = i;
+    }
+    CK(cudaMemcpyAsync(h->p<int>(h->L.cap_slot), slot.data(), slot.size() * sizeof(int), cudaMemcpyHostToDevice,
+                       h->st));
+    CK(cudaStreamSynchronize(h->st));
+    h->cap_t = n_rows ? talker_logits : nullptr;
+    h->cap_c = n_rows ? cp_logits : nullptr;
+    h->cap_T = max_frames;
+    invalidate_graph(h);
+    return upload_frame_params(h);
+}
+
+int q3tts_sample_logits(q3tts_t* h, int n, const float* logits, int talker, const q3tts_sampling* params,
+                        const uint8_t* seen, const int32_t* sel_index, int step, const int32_t* noise_row,
+                        int32_t* ids_out) {
+    if (!h) return Q3_ERR_ARG;
+    const q3tts_config& c = h->c;
+    if (n < 0 || n > h->L.n_sets) return fail(h, Q3_ERR_ARG, "n must be in 0..%d", h->L.n_sets);
+    if (n == 0) return Q3_OK;
+    if (!logits || !params || !sel_index || !noise_row || !ids_out) return fail(h, Q3_ERR_ARG, "NULL argument");
+    const int V = talker ? c.codec_vocab : c.cp_vocab;
+    float* lg = h->p<float>(h->L.s_logits);
+    uint8_t* sn = seen ? h->p<uint8_t>(h->L.s_seen) : nullptr;
+    q3tts_sampling* sp = h->p<q3tts_sampling>(h->L.s_params);
+    CK(cudaMemcpyAsync(lg, logits, (size_t)n * V * sizeof(float), cudaMemcpyDefault, h->st));
+    if (seen) CK(cudaMemcpyAsync(sn, seen, (size_t)n * V, cudaMemcpyDefault, h->st));
+    CK(cudaMemcpyAsync(sp, params, (size_t)n * sizeof(q3tts_sampling), cudaMemcpyHostToDevice, h->st));
+    CK(cudaMemcpyAsync(h->p<int>(h->L.s_sel), sel_index, (size_t)n * sizeof(int), cudaMemcpyHostToDevice, h->st));
+    CK(cudaMemcpyAsync(h->p<int>(h->L.s_row), noise_row, (size_t)n * sizeof(int), cudaMemcpyHostToDevice, h->st));
+    int* serr = h->err() + 2;   // own error word: the frame loop's word is left untouched
+    CK(cudaMemsetAsync(serr, 0, sizeof(int), h->st));
+    CK(launch_sample_sets(lg, n, V, talker, sp, sn, h->p<int>(h->L.s_sel), step,
+                          h->p<int>(h->L.s_row), c.eos_id, c.suppress_lo, c.suppress_hi, h->p<int>(h->L.s_ids),
+                          serr, h->st)); debug_wait(h->st, "launch_sample_sets");
+    int err_host[4] = {0, 0, 0, 0};
+    CK(cudaMemcpyAsync(ids_out, h->p<int>(h->L.s_ids), (size_t)n * sizeof(int), cudaMemcpyDefault, h->st));
+    CK(cudaMemcpyAsync(err_host, serr, sizeof(int), cudaMemcpyDeviceToHost, h->st));
+    CK(cudaStreamSynchronize(h->st));
+    return read_errors(h, err_host);
+}
+
+int q3tts_step_kernel_count(q3tts_t* h, int* count) {
+    if (!h || !count) return Q3_ERR_ARG;
+    if (!h->prefilled) return fail(h, Q3_ERR_STATE, "no prefill");
+    if (!h->exec) {
+        int r = record_step_graph(h);
+        if (r) return r;
+    }
+    size_t n = 0;
+    CK(cudaGraphGetNodes(h->graph, nullptr, &n));
+    std::vector<cudaGraphNode_t> nodes(n);
+    CK(cudaGraphGetNodes(h->graph, nodes.data(), &n));
+    int k = 0;
+    for (size_t i = 0; i < n; ++i) {
+        cudaGraphNodeType t;
+        CK(cudaGraphNodeGetType(nodes[i], &t));
+        if (t == cudaGraphNodeTypeKernel) ++k;
+    }
+    *count = k;
+    return Q3_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,180 @@
+"""GPU parity of the frame loop against the oracle, through the C ABI."""
+import dataclasses
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from synth import RowSampling, Workload, F32, BF16
+from parity import run_gpu, compare, TOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def q3():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import speech_lm_decode_gb300 as m
+    return m
+
+
+def small_workload(dims, dtype, frames=12, seed=21):
+    rows = [RowSampling(max_frames=frames),
+            RowSampling(max_frames=frames, do_sample=1, temperature=0.9, top_k=8, top_p=0.9, cp_do_sample=1,
+                        cp_temperature=0.8, cp_top_k=6, cp_top_p=0.95, seed=11),
+            RowSampling(max_frames=frames, force_eos_at_frame=5),
+            RowSampling(max_frames=frames - 3, do_sample=1, temperature=1.1, top_k=0, top_p=0.8, cp_do_sample=1,
+                        min_new_tokens=30)]
+    lens = [5, 9, 17, 3]
+    return Workload("small", dims, dtype, seed, len(rows), lens, [3, 0, 5, 1], frames, rows,
+                    max(lens) + frames + 3, norm_std=0.1)
+
+
+def small_weights(wl, scale=10.0):
+    w = synth.make_weights(wl.dims, wl.dtype, wl.weight_seed, norm_std=wl.norm_std)
+    if scale != 1.0:
+        # larger projections so that attention and the MLP shape the result
+        for blk in ("talker", "cp"):
+            for k in ("wqkv", "wo", "wgu", "wd"):
+                a = w[blk][k]
+                f = synth.bf16_bits_to_f32(a) if a.dtype == np.uint16 else a
+                f = (f * scale).astype(np.float32)
+                w[blk][k] = synth.round_bf16(f) if a.dtype == np.uint16 else f
+    return w
+
+
+@pytest.mark.parametrize("dims,dtype", [(synth.DIMS_SMALL, F32), (synth.DIMS_SMALL, BF16),
+                                        (synth.DIMS_SMALL_PROJ, BF16), (synth.DIMS_SMALL_PROJ, F32)])
+def test_small_model_parity(q3, dims, dtype):
+    wl = small_workload(dims, dtype)
+    w = small_weights(wl)
+    inp = synth.make_inputs(wl)
+    g = run_gpu(wl, q3.to_device_weights(w), inp, cap_rows=list(range(wl.batch)))
+    assert g.frames[2] == 5 and g.reasons[2] == q3.Q3_FINISHED_EOS
+    assert g.reasons[1] != q3.Q3_RUNNING and g.reasons[0] != q3.Q3_RUNNING
+    s = compare(wl, w, inp, g)
+    assert s["checked"] > 0.5 * s["decisions"]
+
+
+def test_chunked_steps_equal_one_call_and_repeatable(q3):
+    wl = small_workload(synth.DIMS_SMALL, BF16, frames=14)
+    w = small_weights(wl)
+    inp = synth.make_inputs(wl)
+    dw = q3.to_device_weights(w)
+    a = run_gpu(wl, dw, inp, cap_rows=[0, 1])
+    b = run_gpu(wl, dw, inp, cap_rows=[0, 1], chunks=[5, 1, 8])
+    assert np.array_equal(a.codes, b.codes)
+    assert np.array_equal(a.frames, b.frames) and np.array_equal(a.reasons, b.reasons)
+    assert np.array_equal(a.talker_logits, b.talker_logits, equal_nan=True)
+    c = run_gpu(wl, dw, inp, cap_rows=[0, 1])
+    assert np.array_equal(a.codes, c.codes)
+
+
+def test_rows_do_not_interact(q3):
+    wl = small_workload(synth.DIMS_SMALL, BF16)
+    w = small_weights(wl)
+    inp = synth.make_inputs(wl)
+    dw = q3.to_device_weights(w)
+    full = run_gpu(wl, dw, inp, cap_rows=[1])
+    # row 1 alone (batch 1) gives the same codes: the noise counter carries the row index 1
+    wl1 = dataclasses.replace(wl, batch=2, rows=[wl.rows[0], wl.rows[1]], prompt_lens=wl.prompt_lens[:2],
+                              n_text=wl.n_text[:2])
+    inp1 = dict(inp)
+    po, to = inp["prompt_offsets"], inp["text_offsets"]
+    inp1["prompt"] = inp["prompt"][:po[2]]
+    inp1["prompt_offsets"] = po[:3]
+    inp1["text"] = inp["text"][:to[2]]
+    inp1["text_offsets"] = to[:3]
+    part = run_gpu(wl1, dw, inp1, cap_rows=[1])
+    assert np.array_equal(full.codes[:2], part.codes)
+
+
+@pytest.mark.parametrize("idx", [1, 2])
+def test_full_size_workload(q3, idx):
+    wl = synth.workload(idx)
+    w = synth.make_weights(wl.dims, wl.dtype, wl.weight_seed)
+    inp = synth.make_inputs(wl)
+    g = run_gpu(wl, q3.to_device_weights(w), inp, cap_rows=[0])
+    s = compare(wl, w, inp, g)
+    print(f"workload {idx}: frames {g.frames[0]} reason {g.reasons[0]} {s}")
+
+
+def test_capacity_and_state_errors(q3):
+    wl = small_workload(synth.DIMS_SMALL, BF16)
+    w = small_weights(wl, 1.0)
+    inp = synth.make_inputs(wl)
+    q = q3.Q3TTS(wl.dims, wl.dtype, q3.to_device_weights(w), wl.batch, wl.max_ctx, 8)
+    rc, *_ = q.step_frames(1, check=False)
+    assert rc == q3.Q3_ERR_STATE
+    rows = [dataclasses.replace(r, max_frames=wl.max_ctx) for r in wl.rows]
+    rc, _ = q.prefill(inp["prompt"], inp["prompt_offsets"], inp["text"], inp["text_offsets"], inp["tts_pad"], rows,
+                      check=False)
+    assert rc == q3.Q3_ERR_CAPACITY
+    q.close()
+
+
+def test_nan_logits_fail_closed(q3):
+    wl = small_workload(synth.DIMS_SMALL, F32, frames=4)
+    w = small_weights(wl, 1.0)
+    w["codec_head"][7, 3] = np.nan      # every talker logit row then holds a NaN
+    inp = synth.make_inputs(wl)
+    q = q3.Q3TTS(wl.dims, wl.dtype, q3.to_device_weights(w), wl.batch, wl.max_ctx, 8)
+    rc, code0 = q.prefill(inp["prompt"], inp["prompt_offsets"], inp["text"], inp["text_offsets"], inp["tts_pad"],
+                          wl.rows, check=False)
+    assert rc == q3.Q3_ERR_NAN
+    rc, codes, frames, reasons = q.step_frames(2, check=False)
+    assert np.all(reasons == q3.Q3_FINISHED_ERROR) and np.all(frames == 0) and np.all(codes == -1)
+    q.close()
+
+
+def _single_row(wl, r):
+    """Row r of a workload as its own batch-1 workload (noise row index 0)."""
+    rows = [wl.rows[r]]
+    return dataclasses.replace(wl, batch=1, rows=rows, prompt_lens=[wl.prompt_lens[r]], n_text=[wl.n_text[r]])
+
+
+def _single_inputs(inp, r):
+    po, to = inp["prompt_offsets"], inp["text_offsets"]
+    return {"prompt": inp["prompt"][po[r]:po[r + 1]], "prompt_offsets": np.array([0, po[r + 1] - po[r]], np.int32),
+            "text": inp["text"][to[r]:to[r + 1]], "text_offsets": np.array([0, to[r + 1] - to[r]], np.int32),
+            "tts_pad": inp["tts_pad"]}
+
+
+@pytest.mark.parametrize("path", ["frame", "graph"])
+@pytest.mark.parametrize("dims,dtype", [(synth.DIMS_SMALL, BF16), (synth.DIMS_SMALL, F32),
+                                        (synth.DIMS_SMALL_PROJ, BF16)])
+def test_batch1_paths_parity(q3, monkeypatch, dims, dtype, path):
+    """Batch 1 runs on the persistent frame kernel (one launch per step); the
+    multi-kernel path is forced with Q3TTS_FRAME_KERNEL=0.  Both match the oracle."""
+    if path == "graph":
+        monkeypatch.setenv("Q3TTS_FRAME_KERNEL", "0")
+    else:
+        monkeypatch.delenv("Q3TTS_FRAME_KERNEL", raising=False)
+    wl = small_workload(dims, dtype, frames=10)
+    w = small_weights(wl)
+    inp = synth.make_inputs(wl)
+    dw = q3.to_device_weights(w)
+    for r in range(wl.batch):
+        wl1, inp1 = _single_row(wl, r), _single_inputs(inp, r)
+        g = run_gpu(wl1, dw, inp1, cap_rows=[0])
+        dump = os.environ.get("Q3TTS_DUMP")
+        if dump:
+            np.savez(f"{dump}_{path}_{dtype}_{r}.npz", codes=g.codes, frames=g.frames, reasons=g.reasons,
+                     tl=g.talker_logits, cl=g.cp_logits)
+        compare(wl1, w, inp1, g)
+
+
+def test_frame_kernel_chunked_and_repeatable(q3, monkeypatch):
+    monkeypatch.delenv("Q3TTS_FRAME_KERNEL", raising=False)
+    wl = _single_row(small_workload(synth.DIMS_SMALL, BF16, frames=14), 1)
+    w = small_weights(wl)
+    inp = _single_inputs(synth.make_inputs(small_workload(synth.DIMS_SMALL, BF16, frames=14)), 1)
+    dw = q3.to_device_weights(w)
+    a = run_gpu(wl, dw, inp, cap_rows=[0])
+    b = run_gpu(wl, dw, inp, cap_rows=[0], chunks=[3, 4, 7])
+    c = run_gpu(wl, dw, inp, cap_rows=[0])
+    assert np.array_equal(a.codes, b.codes) and np.array_equal(a.codes, c.codes)
+    assert np.array_equal(a.talker_logits, c.talker_logits, equal_nan=True)
