@@ -204,6 +204,32 @@ int q3tts_sample_logits(q3tts_t* h, int n, const float* logits, int talker, cons
                         const uint8_t* seen, const int32_t* sel_index, int step, const int32_t* noise_row,
                         int32_t* ids_out);
 
+/* The logits processors and draw of q3tts_sample_logits, for callers that
+ * cannot allocate device memory (no handle, no workspace): e.g. code running
+ * inside another allocator's callback, a real-time thread that must never
+ * block on an allocator, or a process whose device memory is fully reserved
+ * by another runtime.  The pages have no counterpart of this entry point.
+ *   n               logit sets, 0..1024 (more: Q3_ERR_CAPACITY, nothing done)
+ *   vocab           entries per set (2..4096)
+ *   logits          [n][vocab] f32, DEVICE memory
+ *   talker, params, sel_index, step, noise_row: as in q3tts_sample_logits
+ *                   (params / sel_index / noise_row are host arrays)
+ *   seen            [n][vocab] uint8 DEVICE memory or NULL
+ *   eos_id, suppress_lo, suppress_hi: the talker chain's specials
+ *   ids_out         [n] int32 HOST memory (-1 for a NaN set)
+ *   stream          cudaStream_t (NULL = legacy default stream); the call
+ *                   ends with one synchronisation of it
+ * Staging lives in a fixed device array (about 70 KB per GPU that loads the
+ * library, kept until the process exits); the library calls no allocator.
+ * The first call on each device looks the array's address up, so make that
+ * first call before any stream capture.  Every call reuses the same array:
+ * calls that overlap on the GPU (other streams, other threads) race and must
+ * be serialised by the caller.  Errors: Q3_ERR_CAPACITY, Q3_ERR_ARG,
+ * Q3_ERR_NAN, Q3_ERR_CUDA. */
+int q3tts_sample_logits_noalloc(int n, int vocab, const float* logits, int talker, const q3tts_sampling* params,
+                                const uint8_t* seen, const int32_t* sel_index, int step, const int32_t* noise_row,
+                                int eos_id, int suppress_lo, int suppress_hi, int32_t* ids_out, void* stream);
+
 /* Number of kernel launches one talker step of the current batch makes (the
  * kernel nodes of the step's CUDA graph, which this call records if needed).
  * Errors: Q3_ERR_STATE (no prefill), Q3_ERR_CUDA. */

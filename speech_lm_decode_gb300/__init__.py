@@ -20,7 +20,8 @@ Q3_F32, Q3_BF16 = 0, 1
 Q3_RUNNING, Q3_FINISHED_EOS, Q3_FINISHED_LENGTH, Q3_FINISHED_ERROR = 0, 1, 2, 3
 
 EXPORTS = ("q3tts_workspace_bytes", "q3tts_create", "q3tts_prefill", "q3tts_step_frames", "q3tts_set_capture",
-           "q3tts_sample_logits", "q3tts_step_kernel_count", "q3tts_last_error", "q3tts_destroy")
+           "q3tts_sample_logits", "q3tts_sample_logits_noalloc", "q3tts_step_kernel_count", "q3tts_last_error",
+           "q3tts_destroy")
 
 
 class Q3Error(RuntimeError):
@@ -76,6 +77,7 @@ def lib():
         L.q3tts_set_capture.argtypes = [vp, i32, vp, vp, vp, i32]
         L.q3tts_sample_logits.argtypes = [vp, i32, vp, i32, vp, vp, vp, i32, vp, vp]
         L.q3tts_step_kernel_count.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+        L.q3tts_sample_logits_noalloc.argtypes = [i32, i32, vp, i32, vp, vp, vp, i32, vp, i32, i32, i32, vp, vp]
         L.q3tts_last_error.restype = ctypes.c_char_p
         L.q3tts_last_error.argtypes = [vp]
         L.q3tts_destroy.argtypes = [vp]
@@ -238,3 +240,25 @@ class Q3TTS:
             self._check(rc)
             return ids
         return rc, ids
+
+
+def sample_logits_noalloc(logits, talker: bool, params, sel_index, step: int, noise_row, eos_id: int,
+                          suppress_lo: int, suppress_hi: int, seen=None, stream=None, check=True):
+    """Processors + draw without a handle or any device allocation.
+
+    For callers that cannot allocate device memory: logits ([n, V] fp32) and
+    seen ([n, V] uint8, optional) must already be CUDA tensors.  Returns the
+    ids (host numpy).  Calls that overlap on the GPU race (one shared staging
+    area per device)."""
+    n, V = int(logits.shape[0]), int(logits.shape[1])
+    sp = (Sampling * max(n, 1))(*[make_sampling(r) for r in params])
+    sel = np.ascontiguousarray(sel_index, dtype=np.int32)
+    nr = np.ascontiguousarray(noise_row, dtype=np.int32)
+    ids = np.full(max(n, 1), -1, np.int32)
+    st = None if stream is None else stream.cuda_stream
+    rc = lib().q3tts_sample_logits_noalloc(n, V, _ptr(logits), int(talker), ctypes.cast(sp, ctypes.c_void_p),
+                                           _ptr(seen), sel.ctypes.data, step, nr.ctypes.data, eos_id, suppress_lo,
+                                           suppress_hi, ids.ctypes.data, st)
+    if check and rc:
+        raise Q3Error(rc, "q3tts_sample_logits_noalloc failed")
+    return ids[:n] if check else (rc, ids[:n])
