@@ -27,10 +27,11 @@
 //    normalised separately; RoPE inv_freq stays fp32 in bf16 models.
 //
 // Numerics: activations, norms, attention and sums are fp64; weights are the
-// fp32 (or bf16-exact) values handed in.  The bf16 model's own rounding
-// points are modelled explicitly: the operand of every projection and every
-// K/V cache entry is rounded to bf16.  Logits are rounded to fp32 before the
-// logits processors, which then run in fp32 exactly as specified below.
+// fp32 (or bf16-exact) values handed in.  A bf16 model is bf16 in its weights
+// and in its K/V cache: every cache entry is rounded to bf16 when stored;
+// activations (including every projection's input) stay at full precision.
+// Logits are rounded to fp32 before the logits processors, which then run in
+// fp32 exactly as specified below.
 //
 // Parity of end-to-end logits for random-init weights is unpinned beyond the
 // invariants the tests check (the pages print no logits for any weights).
@@ -461,7 +462,8 @@ struct Oracle {
     std::vector<double> sel_margin, cp_margin;
     std::vector<float> talker_logits, cp_logits;
 
-    double operand(double v) const { return c.dtype == DT_BF16 ? bf16_round(v) : v; }
+    // projection inputs are not rounded (weights and the K/V cache carry the model dtype)
+    double operand(double v) const { return v; }
     double kvstore(double v) const { return c.dtype == DT_BF16 ? bf16_round(v) : (double)(float)v; }
 };
 

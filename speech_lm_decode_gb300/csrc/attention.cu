@@ -208,10 +208,9 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const float* __restrict
 
 // grid M, 128 threads: merge the splits of every head into the O-projection
 // operand; skipped tokens get zeros.
-template <typename T>
 __global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
                                                            const float* __restrict__ pacc, int n_splits, int nq,
-                                                           const int* __restrict__ tok_pos, T* __restrict__ out,
+                                                           const int* __restrict__ tok_pos, float* __restrict__ out,
                                                            int ldo) {
     const int m = blockIdx.x, t = threadIdx.x;
     const bool live = tok_pos[m] >= 0;
@@ -229,14 +228,14 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restri
             }
             res = num / den;
         }
-        out[(size_t)m * ldo + (size_t)h * HD + t] = from_f<T>(res);
+        out[(size_t)m * ldo + (size_t)h * HD + t] = res;
     }
 }
 
 template <typename T>
 static cudaError_t attention_impl(const float* qkv, int ldq, int M, int nq, int nkv, const T* Kc, const T* Vc, int cap,
                                   const int* tok_row, const int* tok_pos, int n_splits, float* pm, float* pl,
-                                  float* pacc, T* out, int ldo, cudaStream_t st) {
+                                  float* pacc, float* out, int ldo, cudaStream_t st) {
     dim3 grid(n_splits, nkv, M);
     const int gq = nq / nkv;
     switch (gq) {
@@ -247,19 +246,19 @@ static cudaError_t attention_impl(const float* qkv, int ldq, int M, int nq, int 
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    attn_combine_kernel<T><<<M, 128, 0, st>>>(pm, pl, pacc, n_splits, nq, tok_pos, out, ldo);
+    attn_combine_kernel<<<M, 128, 0, st>>>(pm, pl, pacc, n_splits, nq, tok_pos, out, ldo);
     return cudaGetLastError();
 }
 
 cudaError_t launch_attention(int dtype, const float* qkv, int ldq, int M, int nq, int nkv, const void* Kc,
                              const void* Vc, int cap, const int* tok_row, const int* tok_pos, int n_splits,
-                             float* part_m, float* part_l, float* part_acc, void* out, int ldo, cudaStream_t st) {
+                             float* part_m, float* part_l, float* part_acc, float* out, int ldo, cudaStream_t st) {
     if (M <= 0) return cudaSuccess;
     if (dtype == Q3_BF16)
         return attention_impl<bf16>(qkv, ldq, M, nq, nkv, (const bf16*)Kc, (const bf16*)Vc, cap, tok_row, tok_pos,
-                                    n_splits, part_m, part_l, part_acc, (bf16*)out, ldo, st);
+                                    n_splits, part_m, part_l, part_acc, out, ldo, st);
     return attention_impl<float>(qkv, ldq, M, nq, nkv, (const float*)Kc, (const float*)Vc, cap, tok_row, tok_pos,
-                                 n_splits, part_m, part_l, part_acc, (float*)out, ldo, st);
+                                 n_splits, part_m, part_l, part_acc, out, ldo, st);
 }
 
 }  // namespace q3

@@ -64,11 +64,15 @@ struct FrameParams {
 
 constexpr int FRAME_BAR_WORDS = 64;
 
-// Shared memory the frame kernel needs for these parameters (0 if the
-// configuration does not fit one SM).
-size_t frame_smem_bytes(int dtype, int kmax);
+// Shared memory the frame kernel needs with an input-vector region of
+// xin_bytes (0 if it does not fit one SM); the attention scratch that shares
+// that region needs frame_attn_scratch_bytes().
+size_t frame_smem_bytes(int dtype, int xin_bytes);
+size_t frame_attn_scratch_bytes();
 // One-time attribute setup; returns cudaSuccess when the kernel can run.
 cudaError_t frame_setup(int dtype, size_t smem);
+// CTAs of the frame kernel that fit one SM with this shared memory.
+cudaError_t frame_occupancy(int dtype, size_t smem, int* blocks);
 // Launch one talker step (cooperative, one CTA per SM).
 cudaError_t launch_frame(int dtype, const FrameParams* params_dev, int grid, size_t smem, cudaStream_t st);
 

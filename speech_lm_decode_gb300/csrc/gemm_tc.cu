@@ -1,5 +1,7 @@
 // Tensor-core projections for many tokens at once (large batches, prefill
-// chunks): Y[m][n] (+)= sum_k W[n][k] X[m][k], bf16 operands, fp32 accumulate.
+// chunks): Y[m][n] (+)= sum_k W[n][k] X[m][k], bf16 weights, fp32 inputs and
+// accumulation.  The fp32 input is split exactly enough into two bf16 parts
+// (x = hi + lo + O(2^-18 |x|)) and both parts go through the tensor cores.
 //
 // The weight matrix is the MMA's A operand (128 weight rows per tile) and the
 // tokens are its N dimension (NT tokens per tile), so D[n][m] = W_tile . X^T
@@ -7,7 +9,8 @@
 //   - TMA (cp.async.bulk.tensor, 128-byte swizzle) stages 64-wide K slices of
 //     both operands into a 4-deep shared-memory ring (mbarrier completion);
 //   - one thread issues tcgen05.mma (kind::f16, M=128, N=NT, K=16 per
-//     instruction) and commits each stage back to the producer;
+//     instruction; W x hi, then W x lo into the same accumulator) and commits
+//     each stage back to the producer;
 //   - after the last stage, the four warps read their 32 TMEM lanes with
 //     tcgen05.ld and apply the epilogue (store / residual add / bias, or
 //     SiLU(g)*u for the stacked gate/up weights, which uses two accumulators).
@@ -18,6 +21,8 @@
 
 #include "common.cuh"
 #include "kernels.h"
+
+#include <algorithm>
 
 namespace q3 {
 
@@ -107,6 +112,7 @@ struct TcSmem {
     alignas(1024) bf16 a[STAGES][BM * BK];
     alignas(1024) bf16 a2[GATED ? STAGES : 1][GATED ? BM * BK : 8];
     alignas(1024) bf16 b[STAGES][NT * BK];
+    alignas(1024) bf16 b2[STAGES][NT * BK];
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint64_t done;
@@ -121,10 +127,11 @@ constexpr uint32_t tmem_cols(bool gated) {
 
 template <int NT, bool GATED>
 __global__ void __launch_bounds__(128, 1) umma_linear_kernel(const __grid_constant__ CUtensorMap tmW,
-                                                             const __grid_constant__ CUtensorMap tmX, int N, int K,
+                                                             const __grid_constant__ CUtensorMap tmX,
+                                                             const __grid_constant__ CUtensorMap tmX2, int N, int K,
                                                              int M, float* __restrict__ Y, int ldy,
                                                              const float* __restrict__ bias, int accumulate, int F,
-                                                             bf16* __restrict__ Gout, int ldg, int* err) {
+                                                             float* __restrict__ Gout, int ldg, int* err) {
     extern __shared__ __align__(1024) unsigned char raw[];
     // 1024-byte alignment of the swizzled tiles
     unsigned char* base = (unsigned char*)(((uintptr_t)raw + 1023) & ~(uintptr_t)1023);
@@ -153,7 +160,7 @@ __global__ void __launch_bounds__(128, 1) umma_linear_kernel(const __grid_consta
 
     if (warp == 0 && lane == 0) {
         // producer: K slices of W (and of the up half) and of X
-        const unsigned bytes = (unsigned)((BM * (GATED ? 2 : 1) + NT) * BK * sizeof(bf16));
+        const unsigned bytes = (unsigned)((BM * (GATED ? 2 : 1) + 2 * NT) * BK * sizeof(bf16));
         for (int kb = 0; kb < nk && ok; ++kb) {
             const int st = kb % STAGES;
             const unsigned round = kb / STAGES;
@@ -162,6 +169,7 @@ __global__ void __launch_bounds__(128, 1) umma_linear_kernel(const __grid_consta
             tma_2d(s.a[st], &tmW, kb * BK, n0, &s.full[st]);
             if (GATED) tma_2d(s.a2[st], &tmW, kb * BK, F + n0, &s.full[st]);
             tma_2d(s.b[st], &tmX, kb * BK, m0, &s.full[st]);
+            tma_2d(s.b2[st], &tmX2, kb * BK, m0, &s.full[st]);
         }
     } else if (warp == 1 && lane == 0) {
         // MMA issuer
@@ -171,13 +179,16 @@ __global__ void __launch_bounds__(128, 1) umma_linear_kernel(const __grid_consta
             tc_fence_after();
             const uint64_t da = sw128_desc(s_u32(s.a[st]));
             const uint64_t db = sw128_desc(s_u32(s.b[st]));
+            const uint64_t db2 = sw128_desc(s_u32(s.b2[st]));
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
                 // advance 16 bf16 (32 bytes) along K inside the swizzled row
                 umma(tmem, da + 2 * kk, db + 2 * kk, IDESC, (kb | kk) != 0);
+                umma(tmem, da + 2 * kk, db2 + 2 * kk, IDESC, 1);
                 if (GATED) {
                     const uint64_t da2 = sw128_desc(s_u32(s.a2[st]));
                     umma(tmem + NT, da2 + 2 * kk, db + 2 * kk, IDESC, (kb | kk) != 0);
+                    umma(tmem + NT, da2 + 2 * kk, db2 + 2 * kk, IDESC, 1);
                 }
             }
             umma_commit(&s.empty[st]);
@@ -202,7 +213,7 @@ __global__ void __launch_bounds__(128, 1) umma_linear_kernel(const __grid_consta
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int m = m0 + c0 + j;
-                        if (m < M) Gout[(size_t)m * ldg + n] = __float2bfloat16_rn(v[j] / (1.0f + expf(-v[j])) * u[j]);
+                        if (m < M) Gout[(size_t)m * ldg + n] = v[j] / (1.0f + expf(-v[j])) * u[j];
                     }
                 }
             } else if (n < N) {
@@ -248,22 +259,43 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int ld, int 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// x -> (hi, lo): hi = bf16(x), lo = bf16(x - hi); [M][K] each, row stride K.
+__global__ void split_kernel(const float* __restrict__ X, int ldx, int M, int K, bf16* __restrict__ hi,
+                             bf16* __restrict__ lo) {
+    const long total = (long)M * K;
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+        const int m = (int)(i / K), k = (int)(i % K);
+        const float x = X[(size_t)m * ldx + k];
+        const bf16 h = __float2bfloat16_rn(x);
+        hi[i] = h;
+        lo[i] = __float2bfloat16_rn(x - __bfloat162float(h));
+    }
+}
+
 template <int NT, bool GATED>
-cudaError_t launch_tc(const void* W, int N, int K, const void* X, int ldx, int M, float* Y, int ldy,
-                      const float* bias, int accumulate, int F, bf16* G, int ldg, int* err, cudaStream_t st) {
-    CUtensorMap mw, mx;
+cudaError_t launch_tc(const void* W, int N, int K, const float* X, int ldx, int M, float* Y, int ldy,
+                      const float* bias, int accumulate, int F, float* G, int ldg, const TcScratch& tc, int* err,
+                      cudaStream_t st) {
+    bf16* hi = (bf16*)tc.base;
+    bf16* lo = hi + (size_t)M * K;
+    const long total = (long)M * K;
+    split_kernel<<<(int)std::min<long>((total + 255) / 256, 2048), 256, 0, st>>>(X, ldx, M, K, hi, lo);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap mw, mx, mx2;
     const int wrows = GATED ? 2 * F : N;
-    if (!make_map(&mw, W, wrows, K, K, BM) || !make_map(&mx, X, M, K, ldx, NT)) return cudaErrorInvalidValue;
+    if (!make_map(&mw, W, wrows, K, K, BM) || !make_map(&mx, hi, M, K, K, NT) || !make_map(&mx2, lo, M, K, K, NT))
+        return cudaErrorInvalidValue;
     const size_t smem = sizeof(TcSmem<NT, GATED>) + 1024;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(umma_linear_kernel<NT, GATED>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(umma_linear_kernel<NT, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     dim3 grid((N + BM - 1) / BM, (M + NT - 1) / NT);
-    umma_linear_kernel<NT, GATED><<<grid, 128, smem, st>>>(mw, mx, N, K, M, Y, ldy, bias, accumulate, F, G, ldg, err);
+    umma_linear_kernel<NT, GATED><<<grid, 128, smem, st>>>(mw, mx, mx2, N, K, M, Y, ldy, bias, accumulate, F, G, ldg,
+                                                            err);
     return cudaGetLastError();
 }
 
@@ -279,21 +311,21 @@ static int pick_nt(int N, int M) {
     return 32;
 }
 
-cudaError_t launch_linear_tc(const void* W, int N, int K, const void* X, int ldx, int M, float* Y, int ldy,
-                             const float* bias, int accumulate, int* err, cudaStream_t st) {
+cudaError_t launch_linear_tc(const void* W, int N, int K, const float* X, int ldx, int M, float* Y, int ldy,
+                             const float* bias, int accumulate, const TcScratch& tc, int* err, cudaStream_t st) {
     switch (pick_nt(N, M)) {
-        case 128: return launch_tc<128, false>(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, err, st);
-        case 64: return launch_tc<64, false>(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, err, st);
-        default: return launch_tc<32, false>(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, err, st);
+        case 128: return launch_tc<128, false>(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, tc, err, st);
+        case 64: return launch_tc<64, false>(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, tc, err, st);
+        default: return launch_tc<32, false>(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, tc, err, st);
     }
 }
 
-cudaError_t launch_linear_gated_tc(const void* W, int F, int K, const void* X, int ldx, int M, void* out, int ldo,
-                                   int* err, cudaStream_t st) {
-    switch (pick_nt(F, M)) {
-        case 128: return launch_tc<128, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, (bf16*)out, ldo, err, st);
-        case 64: return launch_tc<64, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, (bf16*)out, ldo, err, st);
-        default: return launch_tc<32, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, (bf16*)out, ldo, err, st);
+cudaError_t launch_linear_gated_tc(const void* W, int F, int K, const float* X, int ldx, int M, float* out, int ldo,
+                                   const TcScratch& tc, int* err, cudaStream_t st) {
+    // gate + up accumulators and two input parts: keep the tile at <= 64 tokens
+    switch (std::min(pick_nt(F, M), 64)) {
+        case 64: return launch_tc<64, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, tc, err, st);
+        default: return launch_tc<32, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, tc, err, st);
     }
 }
 

@@ -11,30 +11,36 @@ namespace q3 {
 struct RowState;
 
 // ---------------------------------------------------------------- linear.cu
-// Y[m][n] (+)= sum_k W[n][k] X[m][k] (+ bias[n]); W [N][K] and X [M][K] in the
-// model dtype, Y fp32.  accumulate: add into Y (residual).  M rows of X with
-// leading dimension ldx; Y leading dimension ldy.
-cudaError_t launch_linear(int dtype, const void* W, int N, int K, const void* X, int ldx, int M, float* Y, int ldy,
-                          const float* bias, int accumulate, int* err, cudaStream_t st);
-// SwiGLU projection: out[m][n] = round(silu(g) * u) with g = W[n].x, u = W[F+n].x,
-// W [2F][K]; out in the model dtype with leading dimension ldo.
-cudaError_t launch_linear_gated(int dtype, const void* W, int F, int K, const void* X, int ldx, int M, void* out,
-                                int ldo, int* err, cudaStream_t st);
-// tensor-core (tcgen05) variants for bf16 and many tokens (gemm_tc.cu)
+// Scratch of the tensor-core path: the fp32 operand split into bf16 high and
+// low parts ([M][K] each).
+struct TcScratch {
+    void* base = nullptr;
+    size_t bytes = 0;
+};
+inline bool tc_fits(const TcScratch& s, int M, int K) { return s.base && (size_t)M * K * 4 <= s.bytes; }
+
+// Y[m][n] (+)= sum_k W[n][k] X[m][k] (+ bias[n]); W [N][K] in the model dtype,
+// X [M][K] fp32 (leading dimension ldx), Y fp32 (leading dimension ldy).
+// accumulate: add into Y (residual).
+cudaError_t launch_linear(int dtype, const void* W, int N, int K, const float* X, int ldx, int M, float* Y, int ldy,
+                          const float* bias, int accumulate, const TcScratch& tc, int* err, cudaStream_t st);
+// SwiGLU projection: out[m][n] = silu(g) * u with g = W[n].x, u = W[F+n].x,
+// W [2F][K]; out fp32 with leading dimension ldo.
+cudaError_t launch_linear_gated(int dtype, const void* W, int F, int K, const float* X, int ldx, int M, float* out,
+                                int ldo, const TcScratch& tc, int* err, cudaStream_t st);
+// tensor-core (tcgen05) variants for bf16 weights and many tokens (gemm_tc.cu)
 bool tc_available();
-cudaError_t launch_linear_tc(const void* W, int N, int K, const void* X, int ldx, int M, float* Y, int ldy,
-                             const float* bias, int accumulate, int* err, cudaStream_t st);
-cudaError_t launch_linear_gated_tc(const void* W, int F, int K, const void* X, int ldx, int M, void* out, int ldo,
-                                   int* err, cudaStream_t st);
+cudaError_t launch_linear_tc(const void* W, int N, int K, const float* X, int ldx, int M, float* Y, int ldy,
+                             const float* bias, int accumulate, const TcScratch& tc, int* err, cudaStream_t st);
+cudaError_t launch_linear_gated_tc(const void* W, int F, int K, const float* X, int ldx, int M, float* out, int ldo,
+                                   const TcScratch& tc, int* err, cudaStream_t st);
 // minimum token count for the tensor-core path (0 disables it)
 void set_tc_min_tokens(int m);
-// out[row(m)] = round(x[m] * rsqrt(mean(x[m]^2) + eps) * w); optionally hout
-// (fp32, unrounded).  out_row: NULL = identity, else out row per input row
-// (negative: skip).
-cudaError_t launch_rmsnorm(int dtype, const float* x, int ldx, int M, const float* w, int n, float eps, void* out,
-                           int ldo, float* hout, int ldh, const int* out_row, cudaStream_t st);
-// out[m][i] = round(x[m][i]) (model dtype)
-cudaError_t launch_to_operand(int dtype, const float* x, int ldx, int M, int n, void* out, int ldo, cudaStream_t st);
+// out[row(m)] = x[m] * rsqrt(mean(x[m]^2) + eps) * w; optionally hout (a
+// second copy).  out_row: NULL = identity, else the output row of each input
+// row (negative: skip).
+cudaError_t launch_rmsnorm(const float* x, int ldx, int M, const float* w, int n, float eps, float* out, int ldo,
+                           float* hout, int ldh, const int* out_row, cudaStream_t st);
 
 // ---------------------------------------------------------------- attention.cu
 // Per token m (row tok_row[m], position tok_pos[m] >= 0): per-head RMSNorm of
@@ -47,7 +53,7 @@ cudaError_t launch_qk_rope_kv(int dtype, float* qkv, int ldq, int M, int nq, int
 // token's row, then the combine writing the O-projection operand [M][nq*128].
 cudaError_t launch_attention(int dtype, const float* qkv, int ldq, int M, int nq, int nkv, const void* Kc,
                              const void* Vc, int cap, const int* tok_row, const int* tok_pos, int n_splits,
-                             float* part_m, float* part_l, float* part_acc, void* out, int ldo, cudaStream_t st);
+                             float* part_m, float* part_l, float* part_acc, float* out, int ldo, cudaStream_t st);
 
 // ---------------------------------------------------------------- sampler.cu
 size_t sampler_smem_bytes();

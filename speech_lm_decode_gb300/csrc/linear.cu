@@ -1,10 +1,12 @@
 // Projections of the talker / code predictor and the RMSNorm that feeds them.
+// Weights are in the model dtype (bf16 or fp32); the input vectors (operands)
+// and all accumulation are fp32.
 //
 // Small batches (M <= 8 rows) are weight-streaming GEMVs: a warp owns R output
 // rows, lanes stream 16-byte chunks of the weight rows (read once, not kept
 // in L1) and keep M running sums each; a fixed-order warp reduction follows.
-// Larger M (prefill chunks, large batches) use a shared-memory tiled CUDA-core
-// GEMM; it is also the fp32-model path.
+// Larger M (prefill chunks, large batches) use the tensor-core path for bf16
+// weights (gemm_tc.cu) and a shared-memory tiled CUDA-core GEMM otherwise.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -12,10 +14,10 @@ namespace q3 {
 
 // ------------------------------------------------------------------ GEMV
 template <typename T, int M, int R, bool GATED>
-__global__ void __launch_bounds__(128) gemv_kernel(const T* __restrict__ W, int N, int K, const T* __restrict__ X,
-                                                   int ldx, float* __restrict__ Y, int ldy,
-                                                   const float* __restrict__ bias, int accumulate, int F,
-                                                   T* __restrict__ G, int ldg) {
+__global__ void __launch_bounds__(128) gemv_kernel(const T* __restrict__ W, int N, int K,
+                                                   const float* __restrict__ X, int ldx, float* __restrict__ Y,
+                                                   int ldy, const float* __restrict__ bias, int accumulate, int F,
+                                                   float* __restrict__ G, int ldg) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = (blockIdx.x * 4 + warp) * R;
     if (n0 >= N) return;
@@ -57,7 +59,7 @@ __global__ void __launch_bounds__(128) gemv_kernel(const T* __restrict__ W, int 
             float u = GATED ? warp_sum(accu[GATED ? r : 0][m]) : 0.f;
             if (lane == 0 && n < N) {
                 if (GATED) {
-                    G[(size_t)m * ldg + n] = from_f<T>(v / (1.0f + expf(-v)) * u);
+                    G[(size_t)m * ldg + n] = v / (1.0f + expf(-v)) * u;
                 } else {
                     if (bias) v += bias[n];
                     float* y = Y + (size_t)m * ldy + n;
@@ -72,10 +74,10 @@ __global__ void __launch_bounds__(128) gemv_kernel(const T* __restrict__ W, int 
 constexpr int TBM = 64, TBN = 64, TBK = 16;
 
 template <typename T, bool GATED>
-__global__ void __launch_bounds__(256) gemm_tiled(const T* __restrict__ W, int N, int K, const T* __restrict__ X,
-                                                  int ldx, int M, float* __restrict__ Y, int ldy,
-                                                  const float* __restrict__ bias, int accumulate, int F,
-                                                  T* __restrict__ G, int ldg) {
+__global__ void __launch_bounds__(256) gemm_tiled(const T* __restrict__ W, int N, int K,
+                                                  const float* __restrict__ X, int ldx, int M,
+                                                  float* __restrict__ Y, int ldy, const float* __restrict__ bias,
+                                                  int accumulate, int F, float* __restrict__ G, int ldg) {
     __shared__ float xs[TBK][TBM + 4];
     __shared__ float ws[TBK][TBN + 4];
     __shared__ float us[GATED ? TBK : 1][TBN + 4];
@@ -86,7 +88,7 @@ __global__ void __launch_bounds__(256) gemm_tiled(const T* __restrict__ W, int N
         for (int e = threadIdx.x; e < TBM * TBK; e += 256) {
             const int r = e / TBK, c = e % TBK;
             const int m = m0 + r, n = n0 + r, k = k0 + c;
-            xs[c][r] = (m < M && k < K) ? to_f(X[(size_t)m * ldx + k]) : 0.f;
+            xs[c][r] = (m < M && k < K) ? X[(size_t)m * ldx + k] : 0.f;
             ws[c][r] = (n < N && k < K) ? to_f(W[(size_t)n * K + k]) : 0.f;
             if (GATED) us[GATED ? c : 0][r] = (n < N && k < K) ? to_f(W[(size_t)(F + n) * K + k]) : 0.f;
         }
@@ -120,7 +122,7 @@ __global__ void __launch_bounds__(256) gemm_tiled(const T* __restrict__ W, int N
             if (n >= N) continue;
             float v = acc[i][j];
             if (GATED) {
-                G[(size_t)m * ldg + n] = from_f<T>(v / (1.0f + expf(-v)) * accu[i][j]);
+                G[(size_t)m * ldg + n] = v / (1.0f + expf(-v)) * accu[i][j];
             } else {
                 if (bias) v += bias[n];
                 float* y = Y + (size_t)m * ldy + n;
@@ -131,8 +133,8 @@ __global__ void __launch_bounds__(256) gemm_tiled(const T* __restrict__ W, int N
 }
 
 template <typename T, bool GATED>
-static cudaError_t linear_impl(const T* W, int N, int K, const T* X, int ldx, int M, float* Y, int ldy,
-                               const float* bias, int accumulate, int F, T* G, int ldg, cudaStream_t st) {
+static cudaError_t linear_impl(const T* W, int N, int K, const float* X, int ldx, int M, float* Y, int ldy,
+                               const float* bias, int accumulate, int F, float* G, int ldg, cudaStream_t st) {
     if (M <= 0 || N <= 0) return cudaSuccess;
     if (M <= 8) {
         // rows per warp: 2 when there are enough rows to cover the GPU twice over
@@ -161,30 +163,27 @@ static bool use_tc(int dtype, int M) {
     return dtype == Q3_BF16 && g_tc_min_tokens > 0 && M >= g_tc_min_tokens && tc_available();
 }
 
-cudaError_t launch_linear(int dtype, const void* W, int N, int K, const void* X, int ldx, int M, float* Y, int ldy,
-                          const float* bias, int accumulate, int* err, cudaStream_t st) {
-    if (use_tc(dtype, M)) return launch_linear_tc(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, err, st);
+cudaError_t launch_linear(int dtype, const void* W, int N, int K, const float* X, int ldx, int M, float* Y, int ldy,
+                          const float* bias, int accumulate, const TcScratch& tc, int* err, cudaStream_t st) {
+    if (use_tc(dtype, M) && tc_fits(tc, M, K))
+        return launch_linear_tc(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, tc, err, st);
     if (dtype == Q3_BF16)
-        return linear_impl<bf16, false>((const bf16*)W, N, K, (const bf16*)X, ldx, M, Y, ldy, bias, accumulate, 0,
-                                        nullptr, 0, st);
-    return linear_impl<float, false>((const float*)W, N, K, (const float*)X, ldx, M, Y, ldy, bias, accumulate, 0,
-                                     nullptr, 0, st);
+        return linear_impl<bf16, false>((const bf16*)W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, st);
+    return linear_impl<float, false>((const float*)W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, st);
 }
 
-cudaError_t launch_linear_gated(int dtype, const void* W, int F, int K, const void* X, int ldx, int M, void* out,
-                                int ldo, int* err, cudaStream_t st) {
-    if (use_tc(dtype, M)) return launch_linear_gated_tc(W, F, K, X, ldx, M, out, ldo, err, st);
+cudaError_t launch_linear_gated(int dtype, const void* W, int F, int K, const float* X, int ldx, int M, float* out,
+                                int ldo, const TcScratch& tc, int* err, cudaStream_t st) {
+    if (use_tc(dtype, M) && tc_fits(tc, M, K))
+        return launch_linear_gated_tc(W, F, K, X, ldx, M, out, ldo, tc, err, st);
     if (dtype == Q3_BF16)
-        return linear_impl<bf16, true>((const bf16*)W, F, K, (const bf16*)X, ldx, M, nullptr, 0, nullptr, 0, F,
-                                       (bf16*)out, ldo, st);
-    return linear_impl<float, true>((const float*)W, F, K, (const float*)X, ldx, M, nullptr, 0, nullptr, 0, F,
-                                    (float*)out, ldo, st);
+        return linear_impl<bf16, true>((const bf16*)W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, st);
+    return linear_impl<float, true>((const float*)W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, st);
 }
 
 // ------------------------------------------------------------------ RMSNorm
-template <typename T>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ x, int ldx, const float* __restrict__ w,
-                                                      int n, float eps, T* __restrict__ out, int ldo,
+                                                      int n, float eps, float* __restrict__ out, int ldo,
                                                       float* __restrict__ hout, int ldh, const int* __restrict__ out_row) {
     const int m = blockIdx.x;
     const int orow = out_row ? out_row[m] : m;
@@ -205,31 +204,15 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
     const float r = 1.0f / sqrtf(red[0] / (float)n + eps);
     for (int i = threadIdx.x; i < n; i += 256) {
         const float y = xr[i] * r * w[i];
-        out[(size_t)orow * ldo + i] = from_f<T>(y);
+        out[(size_t)orow * ldo + i] = y;
         if (hout) hout[(size_t)orow * ldh + i] = y;
     }
 }
 
-cudaError_t launch_rmsnorm(int dtype, const float* x, int ldx, int M, const float* w, int n, float eps, void* out,
-                           int ldo, float* hout, int ldh, const int* out_row, cudaStream_t st) {
+cudaError_t launch_rmsnorm(const float* x, int ldx, int M, const float* w, int n, float eps, float* out, int ldo,
+                           float* hout, int ldh, const int* out_row, cudaStream_t st) {
     if (M <= 0) return cudaSuccess;
-    if (dtype == Q3_BF16)
-        rmsnorm_kernel<bf16><<<M, 256, 0, st>>>(x, ldx, w, n, eps, (bf16*)out, ldo, hout, ldh, out_row);
-    else
-        rmsnorm_kernel<float><<<M, 256, 0, st>>>(x, ldx, w, n, eps, (float*)out, ldo, hout, ldh, out_row);
-    return cudaGetLastError();
-}
-
-template <typename T>
-__global__ void to_operand_kernel(const float* __restrict__ x, int ldx, int n, T* __restrict__ out, int ldo) {
-    const int m = blockIdx.x;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) out[(size_t)m * ldo + i] = from_f<T>(x[(size_t)m * ldx + i]);
-}
-
-cudaError_t launch_to_operand(int dtype, const float* x, int ldx, int M, int n, void* out, int ldo, cudaStream_t st) {
-    if (M <= 0) return cudaSuccess;
-    if (dtype == Q3_BF16) to_operand_kernel<bf16><<<M, 256, 0, st>>>(x, ldx, n, (bf16*)out, ldo);
-    else to_operand_kernel<float><<<M, 256, 0, st>>>(x, ldx, n, (float*)out, ldo);
+    rmsnorm_kernel<<<M, 256, 0, st>>>(x, ldx, w, n, eps, out, ldo, hout, ldh, out_row);
     return cudaGetLastError();
 }
 

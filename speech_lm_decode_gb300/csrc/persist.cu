@@ -95,16 +95,17 @@ struct FSmem {
     uint64_t full[NSLOT];
     uint64_t empty[NSLOT];
     float red[64];
+    float resid[2][32];   // residual rows this CTA adds into (ADD epilogue), read in the prologue
     int flag;
     int aborted;
-    // input vectors of the current GEMV phase (model dtype), [2][kmax]; then the
-    // draw's scratch (used by CTA 0 only)
+    // then: input vectors of the current GEMV phase, fp32 [2][kmax] (also the
+    // attention phase's scratch); then the draw's scratch (CTA 0 only)
 };
 
 __host__ __device__ constexpr size_t align128(size_t v) { return (v + 127) & ~(size_t)127; }
 template <typename T>
-__device__ __forceinline__ T* xin_ptr(FSmem<T>& s) {
-    return reinterpret_cast<T*>(reinterpret_cast<unsigned char*>(&s) + align128(sizeof(FSmem<T>)));
+__device__ __forceinline__ float* xin_ptr(FSmem<T>& s) {
+    return reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(&s) + align128(sizeof(FSmem<T>)));
 }
 template <typename T>
 __device__ __forceinline__ SampSmem& samp_ptr(FSmem<T>& s, int xin_bytes) {
@@ -150,6 +151,21 @@ __device__ __forceinline__ int rows_per_tile(const Gemv& g) {
     return max(1, TILE / unit);
 }
 
+// Cached positions [j0, j1) of a talker attention item that the producer
+// prefetches (all before the new token's position p0); false if none, or if
+// they do not fit one ring slot (then the consumer reads them directly).
+template <typename T>
+__device__ __forceinline__ bool kv_prefetch_range(const FrameParams& P, const PBlk& B, int M, int p0, int S, int item,
+                                                  int& j0, int& j1) {
+    const int m = item / (P.nkv * S);
+    const int sp = item % S;
+    const int n = p0 + m + 1;
+    const int chunk = (n + S - 1) / S;
+    j0 = sp * chunk;
+    j1 = min(min(n, j0 + chunk), p0);
+    return j1 > j0 && (size_t)(j1 - j0) * HD * sizeof(T) * 2 <= (size_t)TILE;
+}
+
 // ------------------------------------------------------------------ producer
 template <typename T>
 struct Producer {
@@ -180,11 +196,31 @@ struct Producer {
         }
     }
     __device__ void barrier() {}
-    __device__ void attention(int, const PBlk&, int, int, int) {}
+    // Talker attention: the cached K / V of positions before the new token do
+    // not depend on this step; stream each of this CTA's splits into a slot.
+    __device__ void attention(int l, const PBlk& B, int M, int p0, int S, bool talker) {
+        if (!ok || !talker) return;
+        for (int item = blockIdx.x; item < M * P.nkv * S; item += gridDim.x) {
+            int j0, j1;
+            if (!kv_prefetch_range<T>(P, B, M, p0, S, item, j0, j1)) continue;
+            const int g = (item / S) % P.nkv;
+            const int slot = seq % NSLOT;
+            const unsigned round = seq / NSLOT;
+            if (round > 0 && !mbar_wait(&s.empty[slot], (round - 1) & 1, P)) { ok = false; return; }
+            const size_t row_bytes = (size_t)HD * sizeof(T);
+            const size_t base = (((size_t)l * P.max_batch + 0) * P.nkv + g) * B.cap + j0;
+            const unsigned bytes = (unsigned)((j1 - j0) * row_bytes);
+            mbar_expect_tx(&s.full[slot], 2 * bytes);
+            bulk_g2s(s.ring[slot], (const char*)B.Kc + base * row_bytes, bytes, &s.full[slot]);
+            bulk_g2s(s.ring[slot] + bytes, (const char*)B.Vc + base * row_bytes, bytes, &s.full[slot]);
+            ++seq;
+        }
+    }
     __device__ void sample_cp(int) {}
     __device__ void sample_talker() {}
     __device__ void prepare_talker() {}
-    __device__ int talker_pos() const { return 0; }
+    __device__ int talker_pos() const { return pos; }
+    int pos = 0;
     __device__ bool live() const { return ok; }
 
     // copies issued but not yet consumed must land before the CTA exits
@@ -208,7 +244,7 @@ struct Consumer {
     int pos = 0;        // talker position of the new token
     bool ok = true;
 
-    __device__ T* xin() { return xin_ptr<T>(s); }
+    __device__ float* xin() { return xin_ptr<T>(s); }
 
     __device__ float block_sum(float v) {
         v = warp_sum(v);
@@ -289,26 +325,35 @@ struct Consumer {
         return src.f32 ? ldg(src.f32 + i) : to_f(src.tab[i]);
     }
 
-    // input vectors of a GEMV phase -> shared memory (model dtype)
+    // input vectors of a GEMV phase -> shared memory (fp32), one pass over
+    // global memory; ADD phases also fetch the residual rows they update
     __device__ void prologue(const Gemv& g) {
-        T* xs = xin();
+        float* xs = xin();
         const int K = g.K;
         const int tid = threadIdx.x;
+        if (g.epi == Epi::ADD) {
+            int n0, n1;
+            split_rows(g.N, n0, n1);
+            for (int i = tid; i < g.M * 32; i += 256) {
+                const int m = i / 32, r = i % 32;
+                if (n0 + r < n1) s.resid[m][r] = ldg(g.dst + (size_t)m * g.ld_dst + n0 + r);
+            }
+        }
         if (g.pro == Pro::LOAD) {
             for (int m = 0; m < g.M; ++m)
-                for (int i = tid; i < K; i += 256) xs[m * K + i] = from_f<T>(ldg(g.pro_src + (size_t)m * g.pro_ld + i));
+                for (int i = tid; i < K; i += 256) xs[m * K + i] = ldg(g.pro_src + (size_t)m * g.pro_ld + i);
             consumer_sync();
             return;
         }
-        if (g.pro == Pro::RAW) {   // predictor tokens into the width projection: operand of the raw token
+        if (g.pro == Pro::RAW) {   // predictor tokens into the width projection
             for (int m = 0; m < g.M; ++m) {
                 const Src src = source(g, m);
-                for (int i = tid; i < K; i += 256) xs[m * K + i] = from_f<T>(value(g, src, i));
+                for (int i = tid; i < K; i += 256) xs[m * K + i] = value(g, src, i);
             }
             consumer_sync();
             return;
         }
-        // NORM: (token -> this CTA's residual slice) -> rmsnorm * w -> operand
+        // NORM: (token -> this CTA's residual slice) -> rmsnorm * w
         int r0, r1;
         split_rows(K, r0, r1);
         for (int m = 0; m < g.M; ++m) {
@@ -317,14 +362,15 @@ struct Consumer {
             float ss = 0.f;
             for (int i = tid; i < K; i += 256) {
                 const float v = value(g, src, i);
+                xs[m * K + i] = v;
                 ss = fmaf(v, v, ss);
                 if (g.tok != Tok::NONE && i >= r0 && i < r1) resid[i] = v;
             }
             const float tot = block_sum(ss);
             const float r = 1.0f / sqrtf(tot / (float)K + P.eps);
             for (int i = tid; i < K; i += 256) {
-                const float v = value(g, src, i) * r * g.norm_w[i];
-                xs[m * K + i] = from_f<T>(v);
+                const float v = xs[m * K + i] * r * g.norm_w[i];
+                xs[m * K + i] = v;
                 if (g.hout && i >= r0 && i < r1) g.hout[i] = v;
             }
         }
@@ -365,7 +411,7 @@ struct Consumer {
         const int K = g.K;
         const size_t row_bytes = (size_t)K * sizeof(T);
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        const T* xs = xin();
+        const float* xs = xin();
         for (int r0 = n0; r0 < n1; r0 += rt) {
             const int r = min(rt, n1 - r0);
             const int slot = seq % NSLOT;
@@ -402,10 +448,9 @@ struct Consumer {
                         const int n = r0 + i;
                         float* d = g.dst + (size_t)m * g.ld_dst + n;
                         if (GATED) {
-                            // operand rounding as in the model dtype
-                            *d = to_f(from_f<T>(v / (1.0f + expf(-v)) * uu));
+                            *d = v / (1.0f + expf(-v)) * uu;
                         } else if (g.epi == Epi::ADD) {
-                            *d = ldg(d) + v;
+                            *d = s.resid[m][n - n0] + v;
                         } else if (g.epi == Epi::BIAS) {
                             *d = v + g.bias[n];
                         } else {
@@ -432,7 +477,7 @@ struct Consumer {
 
     // ---------------- attention (A4 + A5) for M new tokens at positions p0.. of a layer
     // smem use: the xin region (not needed during this phase): q [GQ][HD], k/v of new tokens [2][HD] each.
-    __device__ void attention(int l, const PBlk& B, int M, int p0, int S) {
+    __device__ void attention(int l, const PBlk& B, int M, int p0, int S, bool talker) {
         if (!ok) return;
         const int nq = P.nq, nkv = P.nkv;
         const int nqkv = (nq + 2 * nkv) * HD;
@@ -502,6 +547,18 @@ struct Consumer {
                     Vg[(size_t)pos * HD + i] = from_f<T>(sv[m * HD + i]);
                 }
             }
+            // cached positions of a talker split come from the ring (prefetched)
+            const T* kring = nullptr;
+            const T* vring = nullptr;
+            int pj0 = 0, pj1 = 0, slot = -1;
+            if (talker && kv_prefetch_range<T>(P, B, M, p0, S, item, pj0, pj1)) {
+                slot = seq % NSLOT;
+                const unsigned round = seq / NSLOT;
+                ++seq;
+                if (!mbar_wait(&s.full[slot], round & 1, P)) { ok = false; }
+                kring = (const T*)s.ring[slot];
+                vring = kring + (size_t)(pj1 - pj0) * HD;
+            }
             // online softmax over positions j0..j1-1, one position per warp step
             float mx[GQ], lsum[GQ], acc[GQ][4];
 #pragma unroll
@@ -513,7 +570,13 @@ struct Consumer {
             const float scale = 0.08838834764831845f;
             for (int j = j0 + warp; j < j1; j += NCW) {
                 float kk[4], vv[4];
-                if (j < p0) {
+                if (kring && j >= pj0 && j < pj1) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        kk[i] = to_f(kring[(size_t)(j - pj0) * HD + lane + 32 * i]);
+                        vv[i] = to_f(vring[(size_t)(j - pj0) * HD + lane + 32 * i]);
+                    }
+                } else if (j < p0) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         kk[i] = ld_kv(Kg + (size_t)j * HD + lane + 32 * i);
@@ -541,6 +604,8 @@ struct Consumer {
                     mx[hh] = mn;
                 }
             }
+            __syncwarp();
+            if (slot >= 0 && lane == 0) mbar_arrive(&s.empty[slot]);
 #pragma unroll
             for (int hh = 0; hh < GQ; ++hh) {
                 if (lane == 0) { sm_m[warp * GQ + hh] = mx[hh]; sm_l[warp * GQ + hh] = lsum[hh]; }
@@ -586,7 +651,7 @@ struct Consumer {
                         num += ldg(pq + d) * c;
                         den += ldg(pq + HD + 1) * c;
                     }
-                    P.o[(size_t)m * nq * HD + (size_t)(g * GQ + hh) * HD + d] = to_f(from_f<T>(num / den));
+                    P.o[(size_t)m * nq * HD + (size_t)(g * GQ + hh) * HD + d] = num / den;
                 }
                 if (threadIdx.x == 0) P.bar[2 + m * nkv + g] = 0u;
             }
@@ -662,7 +727,7 @@ __device__ void gemv_phase(R& r, const Gemv& g) {
 
 template <typename T, class R>
 __device__ void layer(R& r, const FrameParams& P, const PBlk& B, int l, int M, int p0, int S, float* x, Tok tok,
-                      int s_idx) {
+                      int s_idx, bool talker) {
     const size_t e = sizeof(T);
     const int nq = P.nq, nkv = P.nkv, H = B.H, F = B.F;
     const int nqkv = (nq + 2 * nkv) * HD;
@@ -673,7 +738,7 @@ __device__ void layer(R& r, const FrameParams& P, const PBlk& B, int l, int M, i
     g.norm_w = B.attn_norm + (size_t)l * H; g.dst = P.qkv; g.ld_dst = nqkv; g.s_idx = s_idx;
     gemv_phase<T>(r, g);
     // A4 + A5
-    r.attention(l, B, M, p0, S);
+    r.attention(l, B, M, p0, S, talker);
     r.barrier();
     // A6: O projection + residual
     g = Gemv{};
@@ -713,7 +778,7 @@ __device__ void frame_schedule(R& r, const FrameParams& P) {
             layer_tok = Tok::NONE;
         }
         for (int l = 0; l < P.c.L && r.live(); ++l)
-            layer<T>(r, P, P.c, l, M, 0 + (s == 0 ? 0 : s + 1), 1, P.cx, l == 0 ? layer_tok : Tok::NONE, s);
+            layer<T>(r, P, P.c, l, M, 0 + (s == 0 ? 0 : s + 1), 1, P.cx, l == 0 ? layer_tok : Tok::NONE, s, false);
         // final norm of the last token -> head[s]
         Gemv g{};
         g.W = (const char*)P.cp_heads + (size_t)s * P.cpV * P.Hc * e; g.N = P.cpV; g.K = P.Hc; g.M = 1;
@@ -726,7 +791,7 @@ __device__ void frame_schedule(R& r, const FrameParams& P) {
     // talker
     r.prepare_talker();
     for (int l = 0; l < P.t.L && r.live(); ++l)
-        layer<T>(r, P, P.t, l, 1, r.talker_pos(), P.n_splits, P.x, l == 0 ? Tok::TALK : Tok::NONE, 0);
+        layer<T>(r, P, P.t, l, 1, r.talker_pos(), P.n_splits, P.x, l == 0 ? Tok::TALK : Tok::NONE, 0, true);
     Gemv g{};
     g.W = P.codec_head; g.N = P.V; g.K = P.H; g.M = 1; g.pro = Pro::NORM; g.tok = Tok::NONE; g.epi = Epi::STORE;
     g.pro_src = P.x; g.pro_ld = P.H; g.norm_w = P.t.final_norm; g.dst = P.logits; g.ld_dst = P.V; g.hout = P.h;
@@ -750,6 +815,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) frame_kernel(const FrameParams* _
     if (warp == NCW) {
         if ((threadIdx.x & 31) == 0) {
             Producer<T> pr{s, P};
+            pr.pos = P.rows[0].pos;
             frame_schedule<T>(pr, P);
             pr.drain();
         }
@@ -771,14 +837,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) frame_kernel(const FrameParams* _
 
 // ------------------------------------------------------------------ host side
 template <typename T>
-static size_t smem_for(int kmax) {
-    const size_t attn = (size_t)(2 * HD + 4 * HD + 2 * NCW * 2 + NCW * 2 * HD) * sizeof(float);
-    const size_t xin = std::max((size_t)2 * kmax * sizeof(T), attn);
-    return align128(sizeof(FSmem<T>)) + align128(xin) + sizeof(SampSmem);
+static size_t smem_for(int xin_bytes) {
+    return align128(sizeof(FSmem<T>)) + align128((size_t)xin_bytes) + sizeof(SampSmem);
 }
 
-size_t frame_smem_bytes(int dtype, int kmax) {
-    const size_t b = dtype == Q3_BF16 ? smem_for<bf16>(kmax) : smem_for<float>(kmax);
+size_t frame_attn_scratch_bytes() { return (size_t)(2 * HD + 4 * HD + 2 * NCW * 2 + NCW * 2 * HD) * sizeof(float); }
+
+size_t frame_smem_bytes(int dtype, int xin_bytes) {
+    const size_t b = dtype == Q3_BF16 ? smem_for<bf16>(xin_bytes) : smem_for<float>(xin_bytes);
     return b <= 227 * 1024 ? b : 0;
 }
 
@@ -786,6 +852,12 @@ cudaError_t frame_setup(int dtype, size_t smem) {
     if (dtype == Q3_BF16)
         return cudaFuncSetAttribute(frame_kernel<bf16, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     return cudaFuncSetAttribute(frame_kernel<float, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+cudaError_t frame_occupancy(int dtype, size_t smem, int* blocks) {
+    if (dtype == Q3_BF16)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, frame_kernel<bf16, 2>, NTHREADS, smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, frame_kernel<float, 2>, NTHREADS, smem);
 }
 
 cudaError_t launch_frame(int dtype, const FrameParams* params_dev, int grid, size_t smem, cudaStream_t st) {

@@ -26,7 +26,7 @@ constexpr int MIN_SAMPLE_SETS = 256; // staging for q3tts_sample_logits
 struct Layout {
     size_t kvK, kvV, ckvK, ckvV, rope, rows, params, h, x, cx, tok, opA, opB, headop, qkv, pm, pl, pacc, logits,
         cplogits, t_row, t_pos, c_row, c_pos, last_row, codes, codes_stage, text, pad, err, s_params, s_logits, s_sel, s_row, s_ids, s_seen, cap_slot,
-        fparams, fbar, fpart, fo, fact;
+        fparams, fbar, fpart, fo, fact, tcs;
     size_t total;
     int mmax, kA, kB, rope_rows, frames_cap, n_sets, vmax, fsplits;
 };
@@ -64,9 +64,9 @@ Layout make_layout(const q3tts_config& c) {
     L.x = take((size_t)L.mmax * c.hidden * sizeof(float));
     L.cx = take(2 * B * c.cp_hidden * sizeof(float));
     L.tok = take(2 * B * c.hidden * sizeof(float));
-    L.opA = take((size_t)L.mmax * L.kA * e);
-    L.opB = take((size_t)L.mmax * L.kB * e);
-    L.headop = take(B * c.hidden * e);
+    L.opA = take((size_t)L.mmax * L.kA * sizeof(float));
+    L.opB = take((size_t)L.mmax * L.kB * sizeof(float));
+    L.headop = take(B * c.hidden * sizeof(float));
     L.qkv = take((size_t)L.mmax * nqkv * sizeof(float));
     const size_t np = (size_t)L.mmax * MAX_SPLITS * c.n_q_heads;
     L.pm = take(np * sizeof(float));
@@ -92,12 +92,14 @@ Layout make_layout(const q3tts_config& c) {
     L.s_seen = take((size_t)L.n_sets * L.vmax);
     L.cap_slot = take(B * sizeof(int));
     // persistent frame kernel (batch 1)
-    L.fsplits = std::max(1, std::min((c.max_ctx + 47) / 48, 16));
+    L.fsplits = 16;   // partial buffers sized for the largest split count
     L.fparams = take(sizeof(FrameParams));
     L.fbar = take(FRAME_BAR_WORDS * sizeof(unsigned));
     L.fpart = take((size_t)2 * c.n_kv_heads * L.fsplits * (c.n_q_heads / c.n_kv_heads) * (HD + 2) * sizeof(float));
     L.fo = take((size_t)2 * c.n_q_heads * HD * sizeof(float));
     L.fact = take((size_t)2 * std::max(c.ffn, c.cp_ffn) * sizeof(float));
+    // tensor-core path: bf16 high / low parts of an fp32 operand [mmax][kmax]
+    L.tcs = c.dtype == Q3_BF16 ? take((size_t)L.mmax * std::max(L.kA, L.kB) * 4) : take(256);
     L.total = off;
     return L;
 }
@@ -152,8 +154,16 @@ struct q3tts {
     bool frame_ok = false;      // the persistent frame kernel can serve batch 1
     size_t frame_smem = 0;
     int frame_grid = 0;
+    int frame_xin = 0;
+    int frame_splits = 1;
 
     template <typename T> T* p(size_t off) const { return at<T>(ws, off); }
+    TcScratch tc() const {
+        TcScratch t;
+        t.base = c.dtype == Q3_BF16 ? p<void>(L.tcs) : nullptr;
+        t.bytes = c.dtype == Q3_BF16 ? (size_t)L.mmax * std::max(L.kA, L.kB) * 4 : 0;
+        return t;
+    }
     RowState* rows() const { return p<RowState>(L.rows); }
     int* err() const { return p<int>(L.err); }
 };
@@ -218,8 +228,8 @@ int enqueue_layers(q3tts* h, bool talker, int M, float* x, const int* trow, cons
     const size_t kv_layer = (size_t)c.max_batch * nkv * cap * hd * e;
     char* Kc = h->p<char>(talker ? h->L.kvK : h->L.ckvK);
     char* Vc = h->p<char>(talker ? h->L.kvV : h->L.ckvV);
-    void* opA = h->p<void>(h->L.opA);
-    void* opB = h->p<void>(h->L.opB);
+    float* opA = h->p<float>(h->L.opA);
+    float* opB = h->p<float>(h->L.opB);
     float* qkv = h->p<float>(h->L.qkv);
     const int splits = talker ? (M <= 2 * c.max_batch ? h->splits_t : 1) : 1;
     const float eps = c.rms_eps;
@@ -228,20 +238,20 @@ int enqueue_layers(q3tts* h, bool talker, int M, float* x, const int* trow, cons
         const char* wo = (const char*)bw.wo + (size_t)l * H * nq * hd * e;
         const char* wgu = (const char*)bw.wgu + (size_t)l * 2 * F * H * e;
         const char* wd = (const char*)bw.wd + (size_t)l * H * F * e;
-        CK(launch_rmsnorm(c.dtype, x, H, M, (const float*)bw.attn_norm + (size_t)l * H, H, eps, opA, H, nullptr, 0,
+        CK(launch_rmsnorm(x, H, M, (const float*)bw.attn_norm + (size_t)l * H, H, eps, opA, H, nullptr, 0,
                           nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
-        CK(launch_linear(c.dtype, wqkv, nqkv, H, opA, H, M, qkv, nqkv, nullptr, 0, h->err(), h->st)); debug_wait(h->st, "launch_linear");
+        CK(launch_linear(c.dtype, wqkv, nqkv, H, opA, H, M, qkv, nqkv, nullptr, 0, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
         CK(launch_qk_rope_kv(c.dtype, qkv, nqkv, M, nq, nkv, (const float*)bw.q_norm + (size_t)l * hd,
                              (const float*)bw.k_norm + (size_t)l * hd, eps, h->p<float>(h->L.rope), h->L.rope_rows,
                              Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos, h->err(), h->st)); debug_wait(h->st, "launch_qk_rope_kv");
         CK(launch_attention(c.dtype, qkv, nqkv, M, nq, nkv, Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos,
                             splits, h->p<float>(h->L.pm), h->p<float>(h->L.pl), h->p<float>(h->L.pacc), opA, nq * hd,
                             h->st)); debug_wait(h->st, "launch_attention");
-        CK(launch_linear(c.dtype, wo, H, nq * hd, opA, nq * hd, M, x, H, nullptr, 1, h->err(), h->st)); debug_wait(h->st, "launch_linear");
-        CK(launch_rmsnorm(c.dtype, x, H, M, (const float*)bw.mlp_norm + (size_t)l * H, H, eps, opA, H, nullptr, 0,
+        CK(launch_linear(c.dtype, wo, H, nq * hd, opA, nq * hd, M, x, H, nullptr, 1, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
+        CK(launch_rmsnorm(x, H, M, (const float*)bw.mlp_norm + (size_t)l * H, H, eps, opA, H, nullptr, 0,
                           nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
-        CK(launch_linear_gated(c.dtype, wgu, F, H, opA, H, M, opB, F, h->err(), h->st)); debug_wait(h->st, "launch_linear_gated");
-        CK(launch_linear(c.dtype, wd, H, F, opB, F, M, x, H, nullptr, 1, h->err(), h->st)); debug_wait(h->st, "launch_linear");
+        CK(launch_linear_gated(c.dtype, wgu, F, H, opA, H, M, opB, F, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear_gated");
+        CK(launch_linear(c.dtype, wd, H, F, opB, F, M, x, H, nullptr, 1, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
     }
     return Q3_OK;
 }
@@ -250,10 +260,8 @@ int enqueue_layers(q3tts* h, bool talker, int M, float* x, const int* trow, cons
 int enqueue_cp_input(q3tts* h, int M) {
     const q3tts_config& c = h->c;
     if (c.hidden == c.cp_hidden) return Q3_OK;  // tokens were written to cx directly
-    void* opB = h->p<void>(h->L.opB);
-    CK(launch_to_operand(c.dtype, h->p<float>(h->L.tok), c.hidden, M, c.hidden, opB, c.hidden, h->st)); debug_wait(h->st, "launch_to_operand");
-    CK(launch_linear(c.dtype, h->w.cp_proj_w, c.cp_hidden, c.hidden, opB, c.hidden, M, h->p<float>(h->L.cx),
-                     c.cp_hidden, (const float*)h->w.cp_proj_b, 0, h->err(), h->st)); debug_wait(h->st, "launch_linear");
+    CK(launch_linear(c.dtype, h->w.cp_proj_w, c.cp_hidden, c.hidden, h->p<float>(h->L.tok), c.hidden, M,
+                     h->p<float>(h->L.cx), c.cp_hidden, (const float*)h->w.cp_proj_b, 0, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
     return Q3_OK;
 }
 
@@ -279,7 +287,7 @@ int enqueue_step(q3tts* h) {
     int32_t* codes = h->p<int32_t>(h->L.codes);
     float* cx = h->p<float>(h->L.cx);
     float* tok = (c.hidden == c.cp_hidden) ? cx : h->p<float>(h->L.tok);
-    void* opA = h->p<void>(h->L.opA);
+    float* opA = h->p<float>(h->L.opA);
     float* cpl = h->p<float>(h->L.cplogits);
     const int* slot = h->p<int>(h->L.cap_slot);
     int r;
@@ -290,10 +298,10 @@ int enqueue_step(q3tts* h) {
                                h->L.frames_cap, tok, h->err(), h->st)); debug_wait(h->st, "launch_cp_embed_prefill");
     if ((r = enqueue_cp_input(h, 2 * B))) return r;
     if ((r = enqueue_layers(h, false, 2 * B, cx, c_row, c_pos))) return r;
-    CK(launch_rmsnorm(c.dtype, cx + c.cp_hidden, 2 * c.cp_hidden, B, (const float*)h->w.cp.final_norm, c.cp_hidden,
+    CK(launch_rmsnorm(cx + c.cp_hidden, 2 * c.cp_hidden, B, (const float*)h->w.cp.final_norm, c.cp_hidden,
                       c.rms_eps, opA, c.cp_hidden, nullptr, 0, nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
     CK(launch_linear(c.dtype, h->w.cp_heads, c.cp_vocab, c.cp_hidden, opA, c.cp_hidden, B, cpl, c.cp_vocab, nullptr,
-                     0, h->err(), h->st)); debug_wait(h->st, "launch_linear");
+                     0, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
     CK(launch_cp_sample(cpl, c.cp_vocab, B, rs, P, 0, codes, h->L.frames_cap, h->err(), h->cap_c, slot, h->cap_T,
                         c.n_groups, h->st)); debug_wait(h->st, "launch_cp_sample");
     // 14 autoregressive steps: table[s-1](code s) at position s+1 -> head[s] -> codebook s+1
@@ -302,11 +310,11 @@ int enqueue_step(q3tts* h) {
                                 h->err(), h->st)); debug_wait(h->st, "launch_cp_embed_step");
         if ((r = enqueue_cp_input(h, B))) return r;
         if ((r = enqueue_layers(h, false, B, cx, c_row + (size_t)s * 2 * B, c_pos + (size_t)s * 2 * B))) return r;
-        CK(launch_rmsnorm(c.dtype, cx, c.cp_hidden, B, (const float*)h->w.cp.final_norm, c.cp_hidden, c.rms_eps, opA,
+        CK(launch_rmsnorm(cx, c.cp_hidden, B, (const float*)h->w.cp.final_norm, c.cp_hidden, c.rms_eps, opA,
                           c.cp_hidden, nullptr, 0, nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
         const char* head = (const char*)h->w.cp_heads + (size_t)s * c.cp_vocab * c.cp_hidden * e;
         CK(launch_linear(c.dtype, head, c.cp_vocab, c.cp_hidden, opA, c.cp_hidden, B, cpl, c.cp_vocab, nullptr, 0,
-                         h->err(), h->st)); debug_wait(h->st, "launch_linear");
+                         h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
         CK(launch_cp_sample(cpl, c.cp_vocab, B, rs, P, s, codes, h->L.frames_cap, h->err(), h->cap_c, slot, h->cap_T,
                             c.n_groups, h->st)); debug_wait(h->st, "launch_cp_sample");
     }
@@ -316,11 +324,11 @@ int enqueue_step(q3tts* h) {
                            c.n_groups, codes, h->L.frames_cap, h->p<float>(h->L.text), h->p<float>(h->L.pad), x,
                            c.eos_id, h->err(), h->st)); debug_wait(h->st, "launch_talker_embed");
     if ((r = enqueue_layers(h, true, B, x, t_row, t_pos))) return r;
-    CK(launch_rmsnorm(c.dtype, x, c.hidden, B, (const float*)h->w.talker.final_norm, c.hidden, c.rms_eps, opA,
+    CK(launch_rmsnorm(x, c.hidden, B, (const float*)h->w.talker.final_norm, c.hidden, c.rms_eps, opA,
                       c.hidden, h->p<float>(h->L.h), c.hidden, nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
     float* logits = h->p<float>(h->L.logits);
     CK(launch_linear(c.dtype, h->w.codec_head, c.codec_vocab, c.hidden, opA, c.hidden, B, logits, c.codec_vocab,
-                     nullptr, 0, h->err(), h->st)); debug_wait(h->st, "launch_linear");
+                     nullptr, 0, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
     CK(launch_talker_sample(logits, c.codec_vocab, B, rs, P, c.eos_id, c.suppress_lo, c.suppress_hi, 1, h->err(),
                             h->cap_t, slot, h->cap_T, h->st)); debug_wait(h->st, "launch_talker_sample");
     return Q3_OK;
@@ -366,7 +374,7 @@ int upload_frame_params(q3tts* h) {
     P.cp_proj_w = h->w.cp_proj_w; P.cp_proj_b = (const float*)h->w.cp_proj_b;
     P.H = c.hidden; P.Hc = c.cp_hidden; P.V = c.codec_vocab; P.cpV = c.cp_vocab; P.G = c.n_groups;
     P.nq = c.n_q_heads; P.nkv = c.n_kv_heads; P.eos = c.eos_id; P.sup_lo = c.suppress_lo; P.sup_hi = c.suppress_hi;
-    P.n_splits = h->L.fsplits;
+    P.n_splits = h->frame_splits;
     P.kmax = std::max(std::max(std::max(c.hidden, c.cp_hidden), std::max(c.ffn, c.cp_ffn)), c.n_q_heads * HD);
     P.max_batch = c.max_batch;
     P.eps = c.rms_eps;
@@ -379,8 +387,7 @@ int upload_frame_params(q3tts* h) {
     P.text = h->p<float>(h->L.text); P.pad = h->p<float>(h->L.pad);
     P.bar = h->p<unsigned>(h->L.fbar); P.err = h->err();
     P.cap_t = h->cap_t; P.cap_c = h->cap_c; P.cap_slot = h->p<int>(h->L.cap_slot); P.cap_T = h->cap_T;
-    const size_t e = esize(c.dtype);
-    P.xin_bytes = (int)std::max((size_t)2 * P.kmax * e, (size_t)(2 * HD + 4 * HD + 2 * 8 * 2 + 8 * 2 * HD) * 4);
+    P.xin_bytes = h->frame_xin;
     CK(cudaMemcpyAsync(h->p<FrameParams>(h->L.fparams), &P, sizeof P, cudaMemcpyHostToDevice, h->st));
     CK(cudaStreamSynchronize(h->st));
     return Q3_OK;
@@ -441,19 +448,32 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-        const int kmax = std::max(std::max(std::max(cfg->hidden, cfg->cp_hidden), std::max(cfg->ffn, cfg->cp_ffn)),
-                                  cfg->n_q_heads * HD);
+        const int H = cfg->hidden, Hc = cfg->cp_hidden, nqh = cfg->n_q_heads * HD;
+        const int kmax_cp = std::max(std::max(Hc, cfg->cp_ffn), std::max(nqh, H != Hc ? H : 0));
+        const int kmax_t = std::max(std::max(H, cfg->ffn), nqh);
+        h->frame_xin = (int)std::max((size_t)4 * std::max(2 * kmax_cp, kmax_t), frame_attn_scratch_bytes());
         const size_t e = esize(cfg->dtype);
-        const bool tiles_fit = (size_t)cfg->hidden * e * 2 <= 24 * 1024 && (size_t)cfg->cp_hidden * e * 2 <= 24 * 1024 &&
-                               (size_t)std::max(cfg->ffn, cfg->cp_ffn) * e <= 24 * 1024 &&
-                               (size_t)cfg->n_q_heads * HD * e <= 24 * 1024;
-        h->frame_smem = frame_smem_bytes(cfg->dtype, kmax);
+        const size_t tile = 24 * 1024;
+        const bool tiles_fit = (size_t)H * e * 2 <= tile && (size_t)Hc * e * 2 <= tile &&
+                               (size_t)std::max(cfg->ffn, cfg->cp_ffn) * e <= tile && (size_t)nqh * e <= tile;
+        h->frame_smem = frame_smem_bytes(cfg->dtype, h->frame_xin);
         const char* env = getenv("Q3TTS_FRAME_KERNEL");
         const bool want = !(env && env[0] == '0');
-        h->frame_ok = want && coop && sms > 0 && h->frame_smem > 0 && tiles_fit &&
-                      cfg->n_q_heads == 2 * cfg->n_kv_heads && cfg->n_kv_heads * L.fsplits <= sms * 4;
+        h->frame_ok = want && coop && sms >= cfg->n_kv_heads && h->frame_smem > 0 && tiles_fit &&
+                      cfg->n_q_heads == 2 * cfg->n_kv_heads;
         if (h->frame_ok && frame_setup(cfg->dtype, h->frame_smem) != cudaSuccess) { cudaGetLastError(); h->frame_ok = false; }
+        if (h->frame_ok) {
+            int blocks = 0;
+            if (frame_occupancy(cfg->dtype, h->frame_smem, &blocks) != cudaSuccess || blocks < 1) {
+                cudaGetLastError();
+                h->frame_ok = false;
+            }
+        }
         h->frame_grid = sms;
+        // talker attention splits: a split's cached K and V fit one ring slot
+        const int per_split = (int)(tile / (2 * HD * e));
+        h->frame_splits = std::max(1, std::min((cfg->max_ctx + per_split - 1) / per_split,
+                                               std::min(16, std::max(1, sms / cfg->n_kv_heads))));
         const char* ds = getenv("Q3TTS_DEBUG_SYNC");
         g_debug_sync = ds && ds[0] == '1';
         const char* tc = getenv("Q3TTS_TENSOR_CORES");
@@ -560,7 +580,7 @@ int q3tts_prefill(q3tts_t* h, int batch, const float* prompt, const int32_t* pro
     for (int r = 0; r < batch; ++r)
         for (int p = prompt_offsets[r]; p < prompt_offsets[r + 1]; ++p) { tok_row[p] = r; tok_pos[p] = p - prompt_offsets[r]; }
     float* x = h->p<float>(h->L.x);
-    void* headop = h->p<void>(h->L.headop);
+    float* headop = h->p<float>(h->L.headop);
     const int chunk = std::min(PREFILL_CHUNK, h->L.mmax);
     for (int t0 = 0; t0 < total; t0 += chunk) {
         const int M = std::min(chunk, total - t0);
@@ -576,14 +596,14 @@ int q3tts_prefill(q3tts_t* h, int batch, const float* prompt, const int32_t* pro
         CK(cudaMemcpyAsync(x, prompt + (size_t)t0 * H, (size_t)M * H * sizeof(float), cudaMemcpyDefault, h->st));
         int r = enqueue_layers(h, true, M, x, h->p<int>(h->L.t_row), h->p<int>(h->L.t_pos));
         if (r) return r;
-        CK(launch_rmsnorm(c.dtype, x, H, M, (const float*)h->w.talker.final_norm, H, c.rms_eps, headop, H,
+        CK(launch_rmsnorm(x, H, M, (const float*)h->w.talker.final_norm, H, c.rms_eps, headop, H,
                           h->p<float>(h->L.h), H, h->p<int>(h->L.last_row), h->st)); debug_wait(h->st, "launch_rmsnorm");
         // the host vectors are reused by the next chunk: let this chunk's copies finish
         CK(cudaStreamSynchronize(h->st));
     }
     float* logits = h->p<float>(h->L.logits);
     CK(launch_linear(c.dtype, h->w.codec_head, c.codec_vocab, H, headop, H, batch, logits, c.codec_vocab, nullptr, 0,
-                     h->err(), h->st)); debug_wait(h->st, "launch_linear");
+                     h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
     CK(launch_talker_sample(logits, c.codec_vocab, batch, h->rows(), h->p<q3tts_sampling>(h->L.params), c.eos_id,
                             c.suppress_lo, c.suppress_hi, 0, h->err(), h->cap_t, h->p<int>(h->L.cap_slot), h->cap_T,
                             h->st)); debug_wait(h->st, "launch_talker_sample");

@@ -370,9 +370,9 @@ def test_teacher_forcing_reproduces_free_run(tiny_weights):
     assert np.array_equal(forced.get("talker_logits"), free.get("talker_logits"))
 
 
-def test_bf16_mode_rounds_operands_and_cache(tiny_weights):
-    """bf16 weights through the oracle: the result differs from fp32 by about
-    bf16 rounding of activations, and not more."""
+def test_bf16_mode_rounds_the_cache(tiny_weights):
+    """The same (bf16-exact) weights in bf16 and fp32 mode differ only by the
+    bf16 rounding of the K/V cache: a small but nonzero difference."""
     wl32 = _tiny_wl(3, min_new_tokens=20)
     inp = synth.make_inputs(wl32)
     wbf = {k: ({kk: (synth.round_bf16(vv) if vv.ndim >= 2 and kk.startswith("w") else vv) for kk, vv in v.items()}
@@ -386,4 +386,4 @@ def test_bf16_mode_rounds_operands_and_cache(tiny_weights):
     t = oracle.teacher_from_codes(a.get("codes"), a.get("frames"), a.get("reason"), TINY.eos_id, 3)
     b = oracle.run(wlbf, wbf, inp, capture=True, teacher=t)
     d = np.abs(a.get("talker_logits") - b.get("talker_logits")).max()
-    assert 1e-5 < d < 0.1
+    assert 1e-6 < d < 0.02
