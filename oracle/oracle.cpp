@@ -362,31 +362,27 @@ int sample_one(const float* logits_in, int V, const SampleParams& sp, bool talke
     if (sp.temperature != 1.0f)
         for (int i = 0; i < V; ++i) l[i] = l[i] / sp.temperature;
 
-    // Decision margin of a draw, in units of processed logits: the score ratio
-    // ln(s1/s2) of the winner, and how close the top-k / top-p boundaries are
-    // (a kept-set change under small logit errors can change the winner).
-    double boundary = INFINITY;
+    // top-k: keep every logit >= the k-th largest (ties kept)
+    float vk = -INFINITY;
     if (sp.top_k > 0 && sp.top_k < V) {
         std::vector<float> sorted(l);
         std::sort(sorted.begin(), sorted.end(), [](float a, float b) { return a > b; });
-        float vk = sorted[sp.top_k - 1];
-        if (sorted[sp.top_k] != -INFINITY) boundary = (double)vk - (double)sorted[sp.top_k];
-        for (int i = 0; i < V; ++i)
-            if (l[i] < vk) l[i] = -INFINITY;
+        vk = sorted[sp.top_k - 1];
     }
-
     std::vector<int> kept;
     for (int i = 0; i < V; ++i)
-        if (l[i] != -INFINITY) kept.push_back(i);
+        if (l[i] != -INFINITY && l[i] >= vk) kept.push_back(i);
     if (kept.empty()) return ERR_NAN;
     std::sort(kept.begin(), kept.end(), [&](int a, int b) { return l[a] > l[b] || (l[a] == l[b] && a < b); });
     const float mx = l[kept[0]];
     std::vector<float> w(V, 0.0f);
-    for (int i : kept) w[i] = spec_expf(l[i] - mx);
+    for (int i = 0; i < V; ++i)
+        if (l[i] != -INFINITY) w[i] = spec_expf(l[i] - mx);
 
+    // top-p: fixed-point weights W_i = floor(w_i * 2^40), exact sums in the
+    // (l desc, id asc) order; keep j iff j == 0 or C_j < top_p * Z
+    std::vector<double> cum_ratio(V, 0.0);   // C_j / (top_p Z) of each kept id, for the margin
     if (sp.top_p < 1.0f) {
-        // Fixed-point weights W_i = floor(w_i * 2^40): sums are exact, so the
-        // kept set does not depend on summation order.
         std::vector<int64_t> W(V, 0);
         int64_t Z = 0;
         for (int i : kept) { W[i] = (int64_t)std::floor((double)w[i] * 1099511627776.0); Z += W[i]; }
@@ -394,30 +390,53 @@ int sample_one(const float* logits_in, int V, const SampleParams& sp, bool talke
         std::vector<int> nk;
         int64_t C = 0;
         for (size_t j = 0; j < kept.size(); ++j) {
+            cum_ratio[kept[j]] = limit > 0 ? (double)C / limit : 0.0;
             if (j == 0 || (double)C < limit) nk.push_back(kept[j]);
-            if (j > 0 && C > 0 && limit > 0) boundary = std::min(boundary, std::fabs(std::log((double)C / limit)));
             C += W[kept[j]];
         }
         kept.swap(nk);
     }
 
+    // draw: argmax of w_i / E_i over the kept ids, lowest id on ties
+    auto score = [&](int i) {
+        const float u = noise_uniform(seed, row, frame, step, (uint32_t)i);
+        return w[i] / -spec_logf(u);
+    };
     int best = -1;
-    float bs = 0.0f, second = 0.0f;
-    bool have2 = false;
-    std::sort(kept.begin(), kept.end());
-    for (int i : kept) {
-        float u = noise_uniform(seed, row, frame, step, (uint32_t)i);
-        float E = -spec_logf(u);
-        float sc = w[i] / E;
-        if (best < 0 || sc > bs) {
-            if (best >= 0) { second = bs; have2 = true; }
-            best = i; bs = sc;
-        } else if (!have2 || sc > second) {
-            second = sc; have2 = true;
-        }
+    float bs = 0.0f;
+    std::vector<int> by_id(kept);
+    std::sort(by_id.begin(), by_id.end());
+    for (int i : by_id) {
+        const float sc = score(i);
+        if (best < 0 || sc > bs) { best = i; bs = sc; }
     }
     *out_id = best;
-    *out_margin = std::min(have2 ? std::log((double)bs / (double)second) : INFINITY, boundary);
+
+    // Decision margin (in processed-logit units, ~ natural-log units of the
+    // score): the winner must beat, by the margin, every id that a small logit
+    // perturbation could keep -- the kept ids and the ids within the margin of
+    // the top-k or top-p boundary -- and must not itself sit near a boundary.
+    const double near = 0.05;
+    double margin = INFINITY;
+    auto near_top_p = [&](int i) {
+        return sp.top_p < 1.0f && cum_ratio[i] > 0.0 && std::fabs(std::log(cum_ratio[i])) < near;
+    };
+    for (int i = 0; i < V; ++i) {
+        if (i == best || l[i] == -INFINITY) continue;
+        const bool kept_i = std::binary_search(by_id.begin(), by_id.end(), i);
+        const bool cand = kept_i || (vk != -INFINITY && (double)l[i] >= (double)vk - near) || near_top_p(i);
+        if (!cand) continue;
+        margin = std::min(margin, std::log((double)bs / (double)score(i)));
+    }
+    if (vk != -INFINITY) {
+        // the winner drops out of top-k if the next value below it rises past it
+        float below = -INFINITY;
+        for (int i = 0; i < V; ++i)
+            if (l[i] < vk && l[i] > below) below = l[i];
+        if (below != -INFINITY) margin = std::min(margin, (double)l[best] - (double)below);
+    }
+    if (near_top_p(best)) margin = std::min(margin, std::fabs(std::log(cum_ratio[best])));
+    *out_margin = margin;
     return ERR_OK;
 }
 

@@ -59,16 +59,23 @@ def run_gpu(wl, dev_weights, inputs, cap_rows, chunks=None):
     return out
 
 
-def compare(wl, weights, inputs, g: GpuRun, tol=None, margin=MARGIN, report=None):
+def compare(wl, weights, inputs, g: GpuRun, tol=None, margin=MARGIN, report=None, upto=None):
     """Teacher-force the oracle on the GPU's codes for the captured rows and
     check frames, finish reasons, logits (<= tol) and decisions (where the
-    oracle's margin > margin).  Returns a summary dict."""
+    oracle's margin > margin).  upto: compare only frames [0, upto) (the
+    oracle then stops there).  Returns a summary dict."""
     tol = TOL[wl.dtype] if tol is None else tol
-    T = wl.frames
+    T = wl.frames if upto is None else min(upto, wl.frames)
     d = wl.dims
     rows = g.cap_rows
-    teacher = oracle.teacher_from_codes(g.codes[rows], g.frames[rows], g.reasons[rows], d.eos_id, T)
-    o = oracle.run(wl, weights, inputs, rows=rows, teacher=teacher, capture=True)
+    # the GPU run seen through a window of T frames
+    gf = np.minimum(g.frames, T)
+    gr = np.where((g.frames < T) | ((g.frames == T) & (g.reasons == oracle.REASON_EOS)), g.reasons,
+                  oracle.REASON_LENGTH)
+    wl_o = dataclasses.replace(wl, frames=T, rows=[dataclasses.replace(r, max_frames=min(r.max_frames, T))
+                                                   for r in wl.rows])
+    teacher = oracle.teacher_from_codes(g.codes[rows][:, :T], gf[rows], gr[rows], d.eos_id, T)
+    o = oracle.run(wl_o, weights, inputs, rows=rows, teacher=teacher, capture=True)
     of, orr = o.get("frames"), o.get("reason")
     otl, ocl = o.get("talker_logits"), o.get("cp_logits")
     own_sel, sel_m = o.get("own_sel"), o.get("sel_margin")
@@ -77,9 +84,9 @@ def compare(wl, weights, inputs, g: GpuRun, tol=None, margin=MARGIN, report=None
     n_dec = n_checked = n_mismatch = 0
     details = []
     for i, r in enumerate(rows):
-        nf = int(g.frames[r])
+        nf = int(gf[r])
         assert int(of[i]) == nf, (r, of[i], nf)
-        assert int(orr[i]) == int(g.reasons[r]), (r, orr[i], g.reasons[r])
+        assert int(orr[i]) == int(gr[r]), (r, orr[i], gr[r])
         forced = wl.rows[r].force_eos_at_frame
         # talker selections 0..nf
         for k in range(nf + 1):
@@ -89,7 +96,7 @@ def compare(wl, weights, inputs, g: GpuRun, tol=None, margin=MARGIN, report=None
             worst_t = max(worst_t, dt)
             if k < nf:
                 gsel = int(g.codes[r, k, 0])
-            elif int(g.reasons[r]) == oracle.REASON_EOS and k != forced:
+            elif int(gr[r]) == oracle.REASON_EOS and k != forced:
                 gsel = d.eos_id
             else:
                 continue
@@ -121,13 +128,13 @@ def compare(wl, weights, inputs, g: GpuRun, tol=None, margin=MARGIN, report=None
     # GPU's own captured logits give the GPU's ids, at every decision
     n_exact, exact_bad = 0, []
     for i, r in enumerate(rows):
-        nf = int(g.frames[r])
+        nf = int(gf[r])
         sp = wl.rows[r]
         seen = np.zeros(d.codec_vocab, np.uint8)
         for k in range(nf + 1):
             if k < nf:
                 gsel = int(g.codes[r, k, 0])
-            elif int(g.reasons[r]) == oracle.REASON_EOS:
+            elif int(gr[r]) == oracle.REASON_EOS:
                 gsel = d.eos_id
             else:
                 gsel = None
@@ -156,3 +163,23 @@ def compare(wl, weights, inputs, g: GpuRun, tol=None, margin=MARGIN, report=None
     assert not exact_bad, summary
     assert n_mismatch == 0, summary
     return summary
+
+
+def check_run_properties(wl, g: GpuRun):
+    """Properties of a whole batch that hold at any size: codes in range for
+    emitted frames and -1 after, finish reasons consistent with frame counts."""
+    d = wl.dims
+    assert np.all(g.reasons != 0), "every row must have finished"
+    assert not np.any(g.reasons == 3), "no row may end on NaN logits"
+    for r in range(wl.batch):
+        nf = int(g.frames[r])
+        sp = wl.rows[r]
+        c = g.codes[r]
+        assert np.all((c[:nf] >= 0) & (c[:nf] < d.cp_vocab)), r
+        assert np.all(c[nf:] == -1), r
+        if g.reasons[r] == oracle.REASON_LENGTH:
+            assert nf == sp.max_frames, r
+        else:
+            assert nf < sp.max_frames or nf == sp.force_eos_at_frame or nf == sp.max_frames, r
+            if sp.force_eos_at_frame >= 0:
+                assert nf <= sp.force_eos_at_frame, r

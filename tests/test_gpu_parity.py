@@ -8,7 +8,7 @@ import pytest
 import oracle
 import synth
 from synth import RowSampling, Workload, F32, BF16
-from parity import run_gpu, compare, TOL
+from parity import run_gpu, compare, check_run_properties, TOL
 
 pytestmark = pytest.mark.gpu
 
@@ -92,14 +92,21 @@ def test_rows_do_not_interact(q3):
     assert np.array_equal(full.codes[:2], part.codes)
 
 
-@pytest.mark.parametrize("idx", [1, 2])
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
 def test_full_size_workload(q3, idx):
+    """Every workload at its full size, in the launch configuration the
+    benchmark times.  Batches 1 and 32: the oracle follows sampled rows over
+    the whole run; batch 256 (1024 frames): the first and last rows over the
+    first 40 frames, and properties of all 256 rows over the whole run."""
     wl = synth.workload(idx)
     w = synth.make_weights(wl.dims, wl.dtype, wl.weight_seed)
     inp = synth.make_inputs(wl)
-    g = run_gpu(wl, q3.to_device_weights(w), inp, cap_rows=[0])
-    s = compare(wl, w, inp, g)
-    print(f"workload {idx}: frames {g.frames[0]} reason {g.reasons[0]} {s}")
+    rows = [0] if wl.batch == 1 else [0, wl.batch - 1]
+    g = run_gpu(wl, q3.to_device_weights(w), inp, cap_rows=rows)
+    check_run_properties(wl, g)
+    s = compare(wl, w, inp, g, upto=40 if wl.batch > 32 else None)
+    s.pop("details", None)
+    print(f"workload {idx}: frames {g.frames[rows].tolist()} reasons {g.reasons[rows].tolist()} {s}")
 
 
 def test_capacity_and_state_errors(q3):
