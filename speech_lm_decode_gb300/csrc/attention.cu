@@ -206,30 +206,27 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const float* __restrict
     }
 }
 
-// grid M, 128 threads: merge the splits of every head into the O-projection
-// operand; skipped tokens get zeros.
+// grid (M, nq), 128 threads (one head dimension each): merge the splits of
+// one head into the O-projection input; skipped tokens get zeros.
 __global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
                                                            const float* __restrict__ pacc, int n_splits, int nq,
                                                            const int* __restrict__ tok_pos, float* __restrict__ out,
                                                            int ldo) {
-    const int m = blockIdx.x, t = threadIdx.x;
-    const bool live = tok_pos[m] >= 0;
-    for (int h = 0; h < nq; ++h) {
-        float res = 0.f;
-        if (live) {
-            float ma = -INFINITY;
-            for (int s = 0; s < n_splits; ++s) ma = fmaxf(ma, pm[((size_t)m * n_splits + s) * nq + h]);
-            float den = 0.f, num = 0.f;
-            for (int s = 0; s < n_splits; ++s) {
-                const size_t pi = ((size_t)m * n_splits + s) * nq + h;
-                const float c = (pm[pi] == -INFINITY) ? 0.f : expf(pm[pi] - ma);
-                den += pl[pi] * c;
-                num += pacc[pi * HD + t] * c;
-            }
-            res = num / den;
+    const int m = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
+    float res = 0.f;
+    if (tok_pos[m] >= 0) {
+        float ma = -INFINITY;
+        for (int s = 0; s < n_splits; ++s) ma = fmaxf(ma, pm[((size_t)m * n_splits + s) * nq + h]);
+        float den = 0.f, num = 0.f;
+        for (int s = 0; s < n_splits; ++s) {
+            const size_t pi = ((size_t)m * n_splits + s) * nq + h;
+            const float c = (pm[pi] == -INFINITY) ? 0.f : expf(pm[pi] - ma);
+            den += pl[pi] * c;
+            num += pacc[pi * HD + t] * c;
         }
-        out[(size_t)m * ldo + (size_t)h * HD + t] = res;
+        res = num / den;
     }
+    out[(size_t)m * ldo + (size_t)h * HD + t] = res;
 }
 
 template <typename T>
@@ -246,7 +243,7 @@ static cudaError_t attention_impl(const float* qkv, int ldq, int M, int nq, int 
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    attn_combine_kernel<<<M, 128, 0, st>>>(pm, pl, pacc, n_splits, nq, tok_pos, out, ldo);
+    attn_combine_kernel<<<dim3(M, nq), 128, 0, st>>>(pm, pl, pacc, n_splits, nq, tok_pos, out, ldo);
     return cudaGetLastError();
 }
 
