@@ -24,6 +24,11 @@ struct PBlk {
     int cap, L, H, F;
 };
 
+// Activations exchanged between CTAs of one launch are 64-bit words: the fp32
+// value in the low half and the epoch of the phase that wrote it in the high
+// half, so a reader knows from the word itself that it is current.
+using Word = unsigned long long;
+
 struct FrameParams {
     PBlk t, c;
     const void* codec_emb;
@@ -32,48 +37,50 @@ struct FrameParams {
     const void* cp_heads;
     const void* cp_proj_w;
     const float* cp_proj_b;
-    int H, Hc, V, cpV, G, nq, nkv, eos, sup_lo, sup_hi, n_splits, kmax, max_batch;
+    int H, Hc, V, cpV, G, nq, nkv, eos, sup_lo, sup_hi, n_splits, max_batch;
     float eps;
     const float2* rope;
     int rope_rows;
     RowState* rows;
     const q3tts_sampling* P;
-    float* x;       // talker residual [H]
-    float* cx;      // predictor residual [2][Hc]
-    float* h;       // talker post-norm hidden [H]
-    float* qkv;     // [2][nqkv]
-    float* part;    // attention partials [2][nkv][S][GQ][HD+2]
-    float* o;       // attention output operand [2][nq*HD]
-    float* act;     // SiLU(g)*u operand [2][F]
-    float* logits;  // [V]
-    float* cpl;     // [cpV]
+    Word* x;        // talker residual [H]
+    Word* cx;       // predictor residual [2][Hc]
+    Word* qkv;      // [2][(nq + 2 nkv) * 128]
+    Word* o;        // attention output [2][nq * 128]
+    Word* act;      // SiLU(g) * u [2][F]
+    Word* logits;   // talker logits [V]
+    Word* cpl;      // predictor logits [cpV]
+    float* h;       // talker post-norm hidden [H] (read by the next launch)
+    float* part;    // attention partials
     int32_t* codes;
     int frames_cap;
     const float* text;
     const float* pad;
-    unsigned* bar;    // [0] grid barrier counter; [1] abort flag; [2..] per-head split counters
-                      // (zeroed before every launch)
+    unsigned* ctl;  // [0] abort flag (sticky until the next prefill clears it);
+                    // [8 + g] split counter of kv head g (talker attention)
     int* err;
     float* cap_t;
     float* cap_c;
     const int* cap_slot;
     int cap_T;
-    int xin_bytes;    // shared-memory bytes of the input-vector region
+    int xin_bytes;  // shared-memory bytes of the attention scratch region
 };
 
+constexpr int FRAME_CTL_WORDS = 64;
+constexpr int FRAME_MAX_ROWS = 128;   // residual rows one CTA updates in one phase
+constexpr int FRAME_TILE = 20 * 1024; // bytes of one weight ring slot
+constexpr int FRAME_MAX_PHASES = 1024;  // phases of one launch (epoch = selection * 1024 + phase)
+constexpr int FRAME_MAX_NORM = 2048;    // widest RMSNorm input (talker and predictor widths)
 
-constexpr int FRAME_BAR_WORDS = 64;
-
-// Shared memory the frame kernel needs with an input-vector region of
-// xin_bytes (0 if it does not fit one SM); the attention scratch that shares
-// that region needs frame_attn_scratch_bytes().
+// Shared memory the frame kernel needs with an attention scratch region of
+// xin_bytes (at least frame_attn_scratch_bytes()); 0 if it does not fit one SM.
 size_t frame_smem_bytes(int dtype, int xin_bytes);
 size_t frame_attn_scratch_bytes();
 // One-time attribute setup; returns cudaSuccess when the kernel can run.
 cudaError_t frame_setup(int dtype, size_t smem);
 // CTAs of the frame kernel that fit one SM with this shared memory.
 cudaError_t frame_occupancy(int dtype, size_t smem, int* blocks);
-// Launch one talker step (cooperative, one CTA per SM).
+// Launch one talker step (cooperative, `grid` CTAs).
 cudaError_t launch_frame(int dtype, const FrameParams* params_dev, int grid, size_t smem, cudaStream_t st);
 
 }  // namespace q3

@@ -4,19 +4,41 @@
 //
 // Why: at batch 1 every projection is a GEMV that streams its weights once;
 // the frame's ~3.3 GB (0.6B bf16) is bandwidth-trivial per phase (1-12 MB)
-// but the phases are a ~550-long dependent chain.  Weights do not depend on
-// activations, so each CTA's producer warp streams its slice of every
-// upcoming projection into a shared-memory ring with bulk async copies
-// (cp.async.bulk, completion on mbarriers) as far ahead as the ring allows,
-// across phase boundaries.  The eight consumer warps only wait for the grid
-// barrier that publishes the phase's input vector, then run the dot products
-// out of shared memory.  HBM streaming therefore continues while the chain
-// pays its barrier latencies.
+// but the phases form a ~560-long dependent chain.  Two things keep the chain
+// short:
 //
-// Layout of work: every GEMV phase splits its N output rows evenly over the
-// CTAs (no split-K, fixed reduction order, no atomics on values).  Attention
-// work items are (token, kv head, KV split); the last split of a head to
-// finish merges the partials (flash-decoding combine).  Draws run on CTA 0.
+// * Weights do not depend on activations, so each CTA's producer warp streams
+//   its slice of every upcoming projection into a shared-memory ring with bulk
+//   async copies (cp.async.bulk, completion on mbarriers) as far ahead as the
+//   ring allows, across phase boundaries.
+// * There is no grid-wide barrier.  Every activation that crosses CTAs is a
+//   64-bit word {fp32 value, epoch of the phase that wrote it}, stored with one
+//   relaxed 64-bit store; a reader polls exactly the words it needs until they
+//   carry the epoch it expects.  A phase therefore starts as soon as its own
+//   inputs exist, and the chain pays one L2 round trip per phase instead of a
+//   barrier.  Epochs are selection_index * 1024 + phase, unique per launch.
+//
+// Reuse of an exchange buffer is safe without a barrier because every GEMV
+// phase spreads its output rows over ALL CTAs (the grid is never larger than
+// the smallest output width) and every CTA reads the whole output of the
+// phase before it writes anything later: a CTA that overwrites a buffer has
+// transitively waited for every CTA to finish reading the previous contents.
+// Each link of that chain is a store that depends on a polled value (the poll
+// loop cannot exit before the load returned), so no store can become visible
+// before the read it waited for; no fence is needed on this path.  Plain data
+// that crosses CTAs inside a launch (attention partials) goes through the
+// usual fence + counter pattern.
+//
+// Layout of work: a GEMV phase splits its N output rows evenly over the CTAs
+// (no split-K, fixed reduction order, no atomics on values); inside a CTA each
+// warp takes groups of 1-4 rows of a ring tile and keeps the rows' dot
+// products in flight together.  Talker attention work items are (kv head, KV
+// split): the last split of a head to finish merges the partials
+// (flash-decoding combine).  Predictor attention (at most 17 positions) runs
+// one item per kv head on CTA g, for every token and step, so its cache
+// entries are written and read by the same CTA.  Predictor draws run on every
+// CTA (same logits, same deterministic draw, same id), which removes a
+// hand-off per codebook; the talker's draw runs on CTA 0.
 //
 // Every wait is bounded: an expired wait sets Q3's TIMEOUT error bit and the
 // abort flag, which makes every other wait return; the producer then waits
@@ -31,9 +53,10 @@ namespace q3 {
 
 constexpr int NCW = 8;                       // consumer warps
 constexpr int NTHREADS = (NCW + 1) * 32;     // + one producer warp
-constexpr int TILE = 24 * 1024;              // bytes per ring slot
+constexpr int TILE = FRAME_TILE;             // bytes per ring slot
 constexpr int NSLOT = 5;
 constexpr long long WAIT_LIMIT = 4000000000LL;  // cycles (~2 s) before a wait gives up
+constexpr int NORM_MAX = FRAME_MAX_NORM;     // widest vector an RMSNorm prologue normalizes
 
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -60,29 +83,109 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(b)) : "memory");
 }
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
+// barrier of the consumer threads that also ORs a predicate over them (same result in every thread)
+__device__ __forceinline__ bool consumer_sync_or(bool v) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.or.pred q, 2, 256, p;\n\t"
+        "selp.s32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((int)v)
+        : "memory");
+    return r != 0;
+}
 
-// activations written by other CTAs of this launch: read at L2, never from L1
+// exchange words: relaxed gpu-scope 64-bit accesses (single-copy atomic).  No
+// compiler memory clobber: what orders them is the data they carry (a store
+// writes values computed from polled words), and volatile keeps every poll a
+// fresh load.
+__device__ __forceinline__ Word ll_ld(const Word* p) {
+    Word w;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p));
+    return w;
+}
+__device__ __forceinline__ void ll_put(Word* p, float v, unsigned ep) {
+    const Word w = ((Word)ep << 32) | (Word)__float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w));
+}
+__device__ __forceinline__ unsigned ep_of(Word w) { return (unsigned)(w >> 32); }
+__device__ __forceinline__ float val_of(Word w) { return __uint_as_float((unsigned)w); }
+
+// data written by this CTA in an earlier phase (predictor cache) or by other
+// CTAs behind a fence (attention partials): read at L2, never from L1
 __device__ __forceinline__ float ldg(const float* p) { return __ldcg(p); }
-__device__ __forceinline__ int ldgi(const int* p) { return __ldcg(p); }
 __device__ __forceinline__ float ld_kv(const bf16* p) { return __bfloat162float(__ldcg(p)); }
 __device__ __forceinline__ float ld_kv(const float* p) { return __ldcg(p); }
 
+__device__ __forceinline__ bool aborted(const FrameParams& P) { return *(volatile unsigned*)&P.ctl[0] != 0u; }
+__device__ __forceinline__ void raise_abort(const FrameParams& P, int bits) {
+    if (bits) atomicOr(P.err, bits);
+    atomicExch(&P.ctl[0], 1u);
+}
+
 // Wait on an mbarrier phase; false if the wait expired or the launch aborted.
-__device__ bool mbar_wait(uint64_t* b, unsigned parity, const FrameParams& P) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, unsigned parity, const FrameParams& P) {
     if (mbar_try_wait(b, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(b, parity)) {
-        if (*(volatile unsigned*)&P.bar[1]) return false;
+        if (aborted(P)) return false;
         if (clock64() - t0 > WAIT_LIMIT) {
-            atomicOr(P.err, ERRB_TIMEOUT);
-            atomicExch(&P.bar[1], 1u);
+            raise_abort(P, ERRB_TIMEOUT);
             return false;
+        }
+    }
+    return true;
+}
+
+// Poll N exchange words at base[first + step j] (j < N; indexes >= limit are
+// skipped) until every one carries epoch e: all loads in flight together, and
+// each round re-loads only the words still missing.  False if the launch
+// aborted or the wait expired.  Inline on purpose: a call would make the
+// caller save its live registers to local memory around every wait.
+template <int N>
+__device__ __forceinline__ bool ll_poll(Word (&w)[N], const Word* base, int first, int step, int limit, unsigned e,
+                                        const FrameParams& P) {
+#pragma unroll
+    for (int j = 0; j < N; ++j) w[j] = first + step * j < limit ? ll_ld(base + first + step * j) : ((Word)e << 32);
+    long long t0 = 0;
+    for (unsigned it = 0;; ++it) {
+        bool pend = false;
+#pragma unroll
+        for (int j = 0; j < N; ++j) pend |= ep_of(w[j]) != e;
+        if (!pend) return true;
+        if (it == 0) t0 = clock64();
+        if ((it & 15u) == 15u) {
+            if (aborted(P)) return false;
+            if (clock64() - t0 > WAIT_LIMIT) {
+                raise_abort(P, ERRB_TIMEOUT);
+                return false;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < N; ++j)
+            if (ep_of(w[j]) != e) w[j] = ll_ld(base + first + step * j);
+    }
+}
+__device__ __forceinline__ bool ll_get(const Word* p, unsigned ep, float& v, const FrameParams& P) {
+    Word w[1];
+    const bool ok = ll_poll<1>(w, p, 0, 0, 1, ep, P);
+    v = val_of(w[0]);
+    return ok;
+}
+// dst[i] = src[i] (epoch ep) for this thread's i = tid, tid + 256, ... < n, four
+// loads in flight; *ss accumulates v * v in that order when given.
+__device__ bool ll_fetch(const Word* src, float* dst, int n, unsigned ep, float* ss, const FrameParams& P) {
+    for (int i = threadIdx.x; i < n; i += 4 * 256) {
+        Word w[4];
+        if (!ll_poll<4>(w, src, i, 256, n, ep, P)) return false;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int k = i + j * 256;
+            if (k >= n) break;
+            const float v = val_of(w[j]);
+            dst[k] = v;
+            if (ss) *ss = fmaf(v, v, *ss);
         }
     }
     return true;
@@ -94,33 +197,38 @@ struct FSmem {
     unsigned char ring[NSLOT][TILE];
     uint64_t full[NSLOT];
     uint64_t empty[NSLOT];
-    float red[64];
-    float resid[2][32];   // residual rows this CTA adds into (ADD epilogue), read in the prologue
+    float resid[2][2][FRAME_MAX_ROWS];  // residual entries a GEMV phase updates [phase parity][vector][row]
+    float pss[2][NCW][2];               // per-warp sums of squares of the RMSNorm inputs [phase parity]
+    int codes[MAX_GROUPS];              // this frame's codes as drawn so far
     int flag;
-    int aborted;
-    // then: input vectors of the current GEMV phase, fp32 [2][kmax] (also the
-    // attention phase's scratch); then the draw's scratch (CTA 0 only)
+    // then: two input-vector buffers (fp32 [M][K], one per GEMV phase parity;
+    // the attention phase's scratch shares the one the next GEMV phase fills);
+    // then the draw's scratch
 };
 
 __host__ __device__ constexpr size_t align128(size_t v) { return (v + 127) & ~(size_t)127; }
 template <typename T>
-__device__ __forceinline__ float* xin_ptr(FSmem<T>& s) {
-    return reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(&s) + align128(sizeof(FSmem<T>)));
+__device__ __forceinline__ float* xin_ptr(FSmem<T>& s, int buf, int xin_bytes) {
+    return reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(&s) + align128(sizeof(FSmem<T>)) +
+                                    (size_t)buf * align128((size_t)xin_bytes));
 }
 template <typename T>
 __device__ __forceinline__ SampSmem& samp_ptr(FSmem<T>& s, int xin_bytes) {
-    const size_t off = align128(sizeof(FSmem<T>)) + align128((size_t)xin_bytes);
+    const size_t off = align128(sizeof(FSmem<T>)) + 2 * align128((size_t)xin_bytes);
     return *reinterpret_cast<SampSmem*>(reinterpret_cast<unsigned char*>(&s) + off);
 }
 
 // ------------------------------------------------------------------ the frame schedule
-// Both roles walk the same schedule; the producer acts on GEMV phases only.
-// prologue: NORM = rmsnorm(vector) * w; LOAD = copy operand rows; RAW = operand of the raw vector
+// Both roles walk the same schedule; the producer acts on GEMV phases and on
+// the talker's attention phases only.
+// prologue: NORM = rmsnorm(vector) * w; LOAD = copy the input rows; RAW = the token itself
 enum class Pro { NORM, LOAD, RAW };
-// where the vector comes from: the residual rows (NONE) or an assembled token, whose
-// residual slice this CTA also writes
+// where the vector comes from: the input rows (NONE) or an assembled token, whose
+// residual slice this CTA also writes (NORM)
 enum class Tok { NONE, CP0, CPS, TALK };
 enum class Epi { STORE, ADD, BIAS, GATED };
+// exchange buffers (the epoch of each one's last write is tracked per CTA)
+enum Buf { BX, BCX, BQKV, BO, BACT, BLOG, BCPL, NBUF };
 
 struct Gemv {
     const void* W;
@@ -130,19 +238,20 @@ struct Gemv {
     Pro pro;
     Tok tok;
     Epi epi;
-    const float* pro_src;   // NORM: residual rows; LOAD: operand rows
-    int pro_ld;
+    Word* src;    // NORM / LOAD: input rows; NORM with a token: its residual rows
+    int src_ld, src_buf;
     const float* norm_w;
-    float* dst;
-    int ld_dst;
+    Word* dst;
+    int ld_dst, dst_buf;
     const float* bias;
-    float* hout;            // NORM: also write the fp32 normed vector (talker h)
-    int s_idx;              // TOK_CPS: predictor step
+    float* hout;  // NORM: also write the fp32 normed vector (talker h), this CTA's slice
+    int s_idx;    // CPS / RAW: predictor step
 };
 
 __device__ __forceinline__ void split_rows(int N, int& n0, int& n1) {
-    n0 = (int)(((long long)N * blockIdx.x) / gridDim.x);
-    n1 = (int)(((long long)N * (blockIdx.x + 1)) / gridDim.x);
+    // 32-bit: N * grid stays far below 2^32 for every width of the model
+    n0 = (int)(((unsigned)N * blockIdx.x) / gridDim.x);
+    n1 = (int)(((unsigned)N * (blockIdx.x + 1)) / gridDim.x);
 }
 
 template <typename T>
@@ -151,15 +260,12 @@ __device__ __forceinline__ int rows_per_tile(const Gemv& g) {
     return max(1, TILE / unit);
 }
 
-// Cached positions [j0, j1) of a talker attention item that the producer
+// Cached positions [j0, j1) of talker attention split sp that the producer
 // prefetches (all before the new token's position p0); false if none, or if
 // they do not fit one ring slot (then the consumer reads them directly).
 template <typename T>
-__device__ __forceinline__ bool kv_prefetch_range(const FrameParams& P, const PBlk& B, int M, int p0, int S, int item,
-                                                  int& j0, int& j1) {
-    const int m = item / (P.nkv * S);
-    const int sp = item % S;
-    const int n = p0 + m + 1;
+__device__ __forceinline__ bool kv_prefetch_range(int p0, int S, int sp, int& j0, int& j1) {
+    const int n = p0 + 1;
     const int chunk = (n + S - 1) / S;
     j0 = sp * chunk;
     j1 = min(min(n, j0 + chunk), p0);
@@ -173,6 +279,15 @@ struct Producer {
     const FrameParams& P;
     unsigned seq = 0;
     bool ok = true;
+    int pos = 0;
+
+    __device__ bool take_slot(int& slot) {
+        slot = seq % NSLOT;
+        const unsigned round = seq / NSLOT;
+        if (round > 0 && !mbar_wait(&s.empty[slot], (round - 1) & 1, P)) { ok = false; return false; }
+        ++seq;
+        return true;
+    }
 
     __device__ void gemv(const Gemv& g) {
         if (!ok) return;
@@ -182,45 +297,39 @@ struct Producer {
         const size_t row_bytes = (size_t)g.K * sizeof(T);
         for (int r0 = n0; r0 < n1; r0 += rt) {
             const int r = min(rt, n1 - r0);
-            const int slot = seq % NSLOT;
-            const unsigned round = seq / NSLOT;
-            if (round > 0 && !mbar_wait(&s.empty[slot], (round - 1) & 1, P)) { ok = false; return; }
+            int slot;
+            if (!take_slot(slot)) return;
             const unsigned bytes = (unsigned)(r * row_bytes * (g.gated ? 2 : 1));
             mbar_expect_tx(&s.full[slot], bytes);
-            const char* src = (const char*)g.W + (size_t)r0 * row_bytes;
-            bulk_g2s(s.ring[slot], src, (unsigned)(r * row_bytes), &s.full[slot]);
+            bulk_g2s(s.ring[slot], (const char*)g.W + (size_t)r0 * row_bytes, (unsigned)(r * row_bytes),
+                     &s.full[slot]);
             if (g.gated)
                 bulk_g2s(s.ring[slot] + r * row_bytes, (const char*)g.W + (size_t)(g.N + r0) * row_bytes,
                          (unsigned)(r * row_bytes), &s.full[slot]);
-            ++seq;
         }
     }
-    __device__ void barrier() {}
     // Talker attention: the cached K / V of positions before the new token do
     // not depend on this step; stream each of this CTA's splits into a slot.
     __device__ void attention(int l, const PBlk& B, int M, int p0, int S, bool talker) {
         if (!ok || !talker) return;
-        for (int item = blockIdx.x; item < M * P.nkv * S; item += gridDim.x) {
+        for (int item = blockIdx.x; item < P.nkv * S; item += gridDim.x) {
+            const int g = item / S, sp = item % S;
             int j0, j1;
-            if (!kv_prefetch_range<T>(P, B, M, p0, S, item, j0, j1)) continue;
-            const int g = (item / S) % P.nkv;
-            const int slot = seq % NSLOT;
-            const unsigned round = seq / NSLOT;
-            if (round > 0 && !mbar_wait(&s.empty[slot], (round - 1) & 1, P)) { ok = false; return; }
+            if (!kv_prefetch_range<T>(p0, S, sp, j0, j1)) continue;
+            int slot;
+            if (!take_slot(slot)) return;
             const size_t row_bytes = (size_t)HD * sizeof(T);
             const size_t base = (((size_t)l * P.max_batch + 0) * P.nkv + g) * B.cap + j0;
             const unsigned bytes = (unsigned)((j1 - j0) * row_bytes);
             mbar_expect_tx(&s.full[slot], 2 * bytes);
             bulk_g2s(s.ring[slot], (const char*)B.Kc + base * row_bytes, bytes, &s.full[slot]);
             bulk_g2s(s.ring[slot] + bytes, (const char*)B.Vc + base * row_bytes, bytes, &s.full[slot]);
-            ++seq;
         }
     }
-    __device__ void sample_cp(int) {}
-    __device__ void sample_talker() {}
+    __device__ void draw_cp(int) {}
+    __device__ void draw_talker() {}
     __device__ void prepare_talker() {}
     __device__ int talker_pos() const { return pos; }
-    int pos = 0;
     __device__ bool live() const { return ok; }
 
     // copies issued but not yet consumed must land before the CTA exits
@@ -233,301 +342,411 @@ struct Producer {
     }
 };
 
+// ------------------------------------------------------------------ GEMV helpers
+__device__ __forceinline__ void lds_f32x4(uint32_t a, float& x, float& y, float& z, float& w) {
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(x), "=f"(y), "=f"(z), "=f"(w) : "r"(a));
+}
+// 4 consecutive elements at shared address a as fp32
+__device__ __forceinline__ void lds4(uint32_t a, float (&v)[4], float) { lds_f32x4(a, v[0], v[1], v[2], v[3]); }
+__device__ __forceinline__ void lds4(uint32_t a, float4& v) { lds_f32x4(a, v.x, v.y, v.z, v.w); }
+__device__ __forceinline__ void lds4(uint32_t a, float (&v)[4], bf16) {
+    uint32_t x, y;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(x), "=r"(y) : "r"(a));
+    v[0] = __uint_as_float(x << 16); v[1] = __uint_as_float(x & 0xffff0000u);
+    v[2] = __uint_as_float(y << 16); v[3] = __uint_as_float(y & 0xffff0000u);
+}
+
+// Sums of V = 2^n values over the warp with V - 1 + (5 - n) shuffles: each
+// halving step keeps one half of the values in each half of the lanes.  Lane l
+// ends with the full sum of value j(l) = sum_s bit(l, 4 - s) * V / 2^(s + 1)
+// (s = 0 .. n-1); lanes that differ only in the low 5 - n bits hold the same value.
+template <int N, int OFF, int V>
+__device__ __forceinline__ void split_step(float (&v)[V], int lane) {
+    if constexpr (OFF >= 1) {
+        if constexpr (N > 1) {
+            const bool upper = (lane & OFF) != 0;
+#pragma unroll
+            for (int i = 0; i < N / 2; ++i) {
+                const float send = upper ? v[i] : v[i + N / 2];
+                const float keep = upper ? v[i + N / 2] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
+            }
+            split_step<N / 2, OFF / 2, V>(v, lane);
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], OFF);
+            split_step<1, OFF / 2, V>(v, lane);
+        }
+    }
+}
+template <int V>
+__device__ __forceinline__ float warp_sum_split(float (&v)[V], int lane) {
+    static_assert(V >= 1 && V <= 32 && (V & (V - 1)) == 0, "V must be a power of two");
+    split_step<V, 16, V>(v, lane);
+    return v[0];
+}
+// the value index lane l holds after warp_sum_split<V>
+template <int V>
+__device__ __forceinline__ int split_index(int lane) {
+    int j = 0, half = V / 2, bit = 16;
+#pragma unroll
+    for (int st = 0; st < 5; ++st) {
+        if (half >= 1) {
+            if (lane & bit) j += half;
+            half >>= 1;
+            bit >>= 1;
+        }
+    }
+    return j;
+}
+
 // ------------------------------------------------------------------ consumer
 template <typename T, int GQ>
 struct Consumer {
     FSmem<T>& s;
     const FrameParams& P;
-    unsigned seq = 0;
-    unsigned epoch = 0;
-    int frame = 0;      // frame completed by this step
-    int pos = 0;        // talker position of the new token
-    bool ok = true;
+    unsigned seq = 0;        // ring slots consumed
+    unsigned base = 0;       // epoch of this launch's phase 0
+    unsigned ph = 0;         // phases walked
+    unsigned gph = 0;        // GEMV phases walked (picks the partials buffer)
+    unsigned ep[NBUF] = {};  // epoch of the last write of each exchange buffer
+    int frame = 0;           // frame completed by this step
+    int pos = 0;             // talker position of the new token
+    bool ok = true;          // uniform over the CTA's consumer threads (changes in settle only)
+    bool failed = false;     // a wait of this thread failed (reported at the next settle)
 
-    __device__ float* xin() { return xin_ptr<T>(s); }
+    // input-vector buffer of the next GEMV phase (also the attention scratch)
+    __device__ float* xin_next() { return xin_ptr<T>(s, gph & 1, P.xin_bytes); }
+    __device__ unsigned next_phase() { return base + ph++; }
 
-    __device__ float block_sum(float v) {
-        v = warp_sum(v);
-        const int w = threadIdx.x >> 5;
-        consumer_sync();
-        if ((threadIdx.x & 31) == 0) s.red[w] = v;
-        consumer_sync();
-        float r = 0.f;
-#pragma unroll
-        for (int i = 0; i < NCW; ++i) r += s.red[i];
-        return r;
-    }
-
-    __device__ void abort_now() {
-        atomicExch(&P.bar[1], 1u);
-        ok = false;
-    }
-
-    // Grid-wide barrier: publish this CTA's writes of the phase, wait for all CTAs.
-    __device__ void barrier() {
-        consumer_sync();
-        ++epoch;
-        if (threadIdx.x == 0) {
-            int ab = 0;
-            if (ok) {
-                __threadfence();
-                atomicAdd(&P.bar[0], 1u);
-                const unsigned target = epoch * gridDim.x;
-                const long long t0 = clock64();
-                while (ld_acquire(&P.bar[0]) < target) {
-                    if (*(volatile unsigned*)&P.bar[1]) { ab = 1; break; }
-                    if (clock64() - t0 > WAIT_LIMIT) {
-                        atomicOr(P.err, ERRB_TIMEOUT);
-                        atomicExch(&P.bar[1], 1u);
-                        ab = 1;
-                        break;
-                    }
-                }
-            } else {
-                ab = 1;
-            }
-            s.aborted = ab;
-        }
-        consumer_sync();
-        if (s.aborted) ok = false;
+    // Every thread reports whether its waits succeeded (and any wait that failed
+    // earlier in this thread); all get the same answer: false if any failed.
+    __device__ bool settle(bool good) {
+        if (!good) failed = true;
+        if (consumer_sync_or(failed)) ok = false;
+        return ok;
     }
 
     __device__ bool live() const { return ok; }
 
-    // ---------------- token vectors (talker width H) for prologues
-    // Sources of the input vectors of a phase, resolved once per phase.
-    struct Src {
-        const float* f32;   // fp32 vector (residual rows, h) read at L2
-        const T* tab;       // embedding table row
-    };
-    __device__ Src source(const Gemv& g, int m) {
-        Src r{nullptr, nullptr};
+    // value i (talker width) of input vector m of an assembled-token phase
+    __device__ __forceinline__ float token_value(Tok tok, int s_idx, int m, int i) {
         const int H = P.H;
-        if (g.tok == Tok::NONE) {
-            r.f32 = g.pro_src + (size_t)m * g.pro_ld;
-        } else if (g.tok == Tok::CP0) {
-            if (m == 0) r.f32 = P.h;
-            else r.tab = (const T*)P.codec_emb + (size_t)P.rows[0].code0 * H;
-        } else if (g.tok == Tok::CPS) {
-            const int c = ldgi(P.codes + ((size_t)frame * MAX_GROUPS + g.s_idx));
-            if (c < 0 || c >= P.cpV) {
-                if (threadIdx.x == 0) atomicOr(P.err, ERRB_BOUNDS);
-                abort_now();
-                r.tab = (const T*)P.cp_emb;
-            } else {
-                r.tab = (const T*)P.cp_emb + ((size_t)(g.s_idx - 1) * P.cpV + c) * H;
-            }
+        if (tok == Tok::TALK) return talker_input(i);
+        if (tok == Tok::CP0) {
+            if (m == 0) return ldg(P.h + i);
+            return to_f(((const T*)P.codec_emb)[(size_t)s.codes[0] * H + i]);
         }
-        return r;
-    }
-    __device__ float value(const Gemv& g, const Src& src, int i) {
-        if (g.tok == Tok::TALK) return talker_input(i);
-        return src.f32 ? ldg(src.f32 + i) : to_f(src.tab[i]);
+        return to_f(((const T*)P.cp_emb)[((size_t)(s_idx - 1) * P.cpV + s.codes[s_idx]) * H + i]);
     }
 
-    // input vectors of a GEMV phase -> shared memory (fp32), one pass over
-    // global memory; ADD phases also fetch the residual rows they update
-    __device__ void prologue(const Gemv& g) {
-        float* xs = xin();
-        const int K = g.K;
-        const int tid = threadIdx.x;
-        if (g.epi == Epi::ADD) {
-            int n0, n1;
-            split_rows(g.N, n0, n1);
-            for (int i = tid; i < g.M * 32; i += 256) {
-                const int m = i / 32, r = i % 32;
-                if (n0 + r < n1) s.resid[m][r] = ldg(g.dst + (size_t)m * g.ld_dst + n0 + r);
-            }
-        }
-        if (g.pro == Pro::LOAD) {
-            for (int m = 0; m < g.M; ++m)
-                for (int i = tid; i < K; i += 256) xs[m * K + i] = ldg(g.pro_src + (size_t)m * g.pro_ld + i);
-            consumer_sync();
-            return;
-        }
-        if (g.pro == Pro::RAW) {   // predictor tokens into the width projection
-            for (int m = 0; m < g.M; ++m) {
-                const Src src = source(g, m);
-                for (int i = tid; i < K; i += 256) xs[m * K + i] = value(g, src, i);
-            }
-            consumer_sync();
-            return;
-        }
-        // NORM: (token -> this CTA's residual slice) -> rmsnorm * w
-        int r0, r1;
-        split_rows(K, r0, r1);
-        for (int m = 0; m < g.M; ++m) {
-            const Src src = source(g, m);
-            float* resid = const_cast<float*>(g.pro_src) + (size_t)m * g.pro_ld;
-            float ss = 0.f;
-            for (int i = tid; i < K; i += 256) {
-                const float v = value(g, src, i);
-                xs[m * K + i] = v;
-                ss = fmaf(v, v, ss);
-                if (g.tok != Tok::NONE && i >= r0 && i < r1) resid[i] = v;
-            }
-            const float tot = block_sum(ss);
-            const float r = 1.0f / sqrtf(tot / (float)K + P.eps);
-            for (int i = tid; i < K; i += 256) {
-                const float v = xs[m * K + i] * r * g.norm_w[i];
-                xs[m * K + i] = v;
-                if (g.hout && i >= r0 && i < r1) g.hout[i] = v;
-            }
-        }
-        consumer_sync();
-    }
-
-    // talker input (A1): codec_emb(code0) + sum_q table[q-1](code_q) + text row
-    int tk_ids[MAX_GROUPS];
+    // talker input: codec_emb(code0) + sum_q table[q-1](code_q) + text row
     const float* tk_text = nullptr;
     __device__ void prepare_talker() {
         if (!ok) return;
         const RowState& rs = P.rows[0];
-        bool good = true;
-        for (int q = 0; q < P.G; ++q) {
-            tk_ids[q] = ldgi(P.codes + ((size_t)frame * MAX_GROUPS + q));
-            good &= tk_ids[q] >= 0 && tk_ids[q] < (q == 0 ? P.V : P.cpV);
-        }
-        if (!good) {
-            if (threadIdx.x == 0) atomicOr(P.err, ERRB_BOUNDS);
-            abort_now();
-            for (int q = 0; q < P.G; ++q) tk_ids[q] = 0;
-        }
         tk_text = frame < rs.n_text ? P.text + (size_t)(rs.text_off + frame) * P.H : P.pad;
     }
     __device__ int talker_pos() const { return pos; }
     __device__ float talker_input(int i) {
         const int H = P.H;
-        float acc = to_f(((const T*)P.codec_emb)[(size_t)tk_ids[0] * H + i]);
-        for (int q = 1; q < P.G; ++q) acc += to_f(((const T*)P.cp_emb)[((size_t)(q - 1) * P.cpV + tk_ids[q]) * H + i]);
+        float acc = to_f(((const T*)P.codec_emb)[(size_t)s.codes[0] * H + i]);
+        for (int q = 1; q < P.G; ++q)
+            acc += to_f(((const T*)P.cp_emb)[((size_t)(q - 1) * P.cpV + s.codes[q]) * H + i]);
         return acc + tk_text[i];
     }
 
-    template <int M, bool GATED>
-    __device__ void gemv_tiles(const Gemv& g) {
+    // One GEMV phase.  Prologue: each thread fetches input elements i = tid,
+    // tid + 256, ... (polled exchange words or an assembled token), forms
+    // x (.) w for RMSNorm phases and stores it in this phase's shared buffer,
+    // and sums x^2; ADD phases also fetch the residual entries they update.  One
+    // barrier.  Then each warp takes groups of RG rows of the ring tiles,
+    // round-robin over the phase, keeps their dot products with the whole
+    // vector in flight, reduces them over the lanes together, and the lanes
+    // holding the sums write the outputs.  RMSNorm is applied as the scalar it
+    // is: W (x r (.) w) = r W (x (.) w), with r from the warps' sums of squares.
+    template <int RG, int M, bool GATED>
+    __device__ void gemv_run(const Gemv& g, unsigned cur) {
+        constexpr int H2 = GATED ? 2 : 1;
+        constexpr int V = RG * M * H2;
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+        const int K = g.K;
+        const bool norm = g.pro == Pro::NORM;
+        const bool tok = g.tok != Tok::NONE;
         int n0, n1;
         split_rows(g.N, n0, n1);
+        const int nrows = n1 - n0;
+        const int buf = gph & 1;
+        float* xs = xin_ptr<T>(s, buf, P.xin_bytes);
+        ++gph;
+        bool good = true;
+
+        // this thread's RMSNorm weights (K <= NORM_MAX), fetched before any wait
+        float nw[NORM_MAX / 256];
+        if (norm) {
+#pragma unroll
+            for (int j = 0; j < NORM_MAX / 256; ++j) nw[j] = tid + 256 * j < K ? g.norm_w[tid + 256 * j] : 0.f;
+        }
+        // residual entries this CTA updates
+        if (g.epi == Epi::ADD && tid < nrows * M) {
+            float v = 0.f;
+            good = ll_get(g.dst + (size_t)(tid % M) * g.ld_dst + n0 + tid / M, ep[g.dst_buf], v, P);
+            s.resid[buf][tid % M][tid / M] = v;
+        }
+        float ssq[2] = {0.f, 0.f};
+        constexpr int NJ = NORM_MAX / 256;
+        if (!tok && norm) {
+            // K <= NORM_MAX: all of this thread's words in flight at once
+            const unsigned e = ep[g.src_buf];
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                const Word* src = g.src + (size_t)m * g.src_ld;
+                Word w[NJ];
+                good = ll_poll<NJ>(w, src, tid, 256, K, e, P) && good;
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    const int i = tid + 256 * j;
+                    if (i < K) {
+                        const float v = val_of(w[j]);
+                        ssq[m] = fmaf(v, v, ssq[m]);
+                        xs[m * K + i] = v * nw[j];
+                    }
+                }
+            }
+        } else if (!tok) {
+            const unsigned e = ep[g.src_buf];
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                const Word* src = g.src + (size_t)m * g.src_ld;
+                for (int i0 = tid; i0 < K && good; i0 += 4 * 256) {
+                    Word w[4];
+                    good = ll_poll<4>(w, src, i0, 256, K, e, P);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (i0 + q * 256 < K) xs[m * K + i0 + q * 256] = val_of(w[q]);
+                }
+            }
+        } else {
+            // an assembled token (K = talker width <= NORM_MAX): every CTA builds
+            // the whole vector; with NORM it also publishes the CTA's slice of
+            // the residual rows
+            int r0 = 0, r1 = 0;
+            if (norm) split_rows(K, r0, r1);
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    const int i = tid + 256 * j;
+                    if (i < K) {
+                        float v = token_value(g.tok, g.s_idx, m, i);
+                        if (norm) {
+                            if (i >= r0 && i < r1) ll_put(g.src + (size_t)m * g.src_ld + i, v, cur);
+                            ssq[m] = fmaf(v, v, ssq[m]);
+                            v *= nw[j];
+                        }
+                        xs[m * K + i] = v;
+                    }
+                }
+            }
+        }
+        if (norm) {
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                const float q = warp_sum(ssq[m]);
+                if (lane == 0) s.pss[buf][warp][m] = q;
+            }
+        }
+        // the phase's one barrier (also makes a failed wait known to every thread)
+        if (!settle(good)) return;
+        float rm[2] = {1.f, 1.f};
+        if (norm) {
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                float q = 0.f;
+#pragma unroll
+                for (int w = 0; w < NCW; ++w) q += s.pss[buf][w][m];
+                rm[m] = 1.0f / sqrtf(q / (float)K + P.eps);
+            }
+        }
+        if (g.hout) {
+            // this CTA's slice of the normed vector (the talker's h, read by the next step)
+            int h0, h1;
+            split_rows(K, h0, h1);
+            for (int i = h0 + tid; i < h1; i += 256) g.hout[i] = xs[i] * rm[0];
+        }
+
+        // the rows, as they arrive.  A lane covers elements k + 4 l .. k + 4 l + 3
+        // and k + 128 + 4 l .. (l = lane) of every 256-element block k: its
+        // shared-memory reads of the vector and of a row are contiguous across
+        // the warp (no bank conflicts), and the vector is read once per group.
         const int rt = rows_per_tile<T>(g);
-        const int K = g.K;
-        const size_t row_bytes = (size_t)K * sizeof(T);
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        const float* xs = xin();
-        for (int r0 = n0; r0 < n1; r0 += rt) {
+        const int gpt = (rt + RG - 1) / RG;   // row groups of a full tile
+        const uint32_t row_bytes = (uint32_t)K * sizeof(T);
+        const uint32_t xs_a = smem_u32(xs);
+        const uint32_t ring_a = smem_u32(s.ring);
+        const int jv = split_index<V>(lane);
+        const int jr = jv / (M * H2), jm = (jv / H2) % M;
+        constexpr int NB = V == 16 ? 4 : (V == 8 ? 3 : (V == 4 ? 2 : (V == 2 ? 1 : 0)));
+        // the lane that writes value jv: lowest lane of its duplicates, gate half for gated
+        const bool writer = (lane & ((1 << (5 - NB)) - 1)) == 0 && (!GATED || (jv % H2) == 0);
+        int t = 0;
+        for (int r0 = n0; r0 < n1; r0 += rt, ++t) {
             const int r = min(rt, n1 - r0);
             const int slot = seq % NSLOT;
             const unsigned round = seq / NSLOT;
             ++seq;
-            if (!mbar_wait(&s.full[slot], round & 1, P)) { ok = false; return; }
-            const unsigned char* tile = s.ring[slot];
-            for (int i = warp; i < r; i += NCW) {
-                const T* wr = (const T*)(tile + i * row_bytes);
-                const T* ur = (const T*)(tile + (r + i) * row_bytes);
-                float acc[M], accu[M];
+            if (!mbar_wait(&s.full[slot], round & 1, P)) { failed = true; return; }
+            const uint32_t tile = ring_a + (uint32_t)slot * TILE;
+            const int ng = (r + RG - 1) / RG;
+            for (int q = (warp - (t * gpt) % NCW + NCW) % NCW; q < ng; q += NCW) {
+                const int i0 = q * RG;
+                const int nr = min(RG, r - i0);
+                uint32_t wrow[H2][RG];
 #pragma unroll
-                for (int m = 0; m < M; ++m) { acc[m] = 0.f; accu[m] = 0.f; }
-                for (int k = lane * 8; k < K; k += 256) {
-                    float w[8], u[8];
-                    load8(wr + k, w);
-                    if (GATED) load8(ur + k, u);
+                for (int h = 0; h < H2; ++h)
 #pragma unroll
-                    for (int m = 0; m < M; ++m) {
-                        float xv[8];
-                        load8(xs + m * K + k, xv);
+                    for (int rr = 0; rr < RG; ++rr)
+                        wrow[h][rr] = tile + (uint32_t)(h * r + i0 + min(rr, nr - 1)) * row_bytes;
+                float acc[2][H2][RG][M];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            acc[m] = fmaf(w[j], xv[j], acc[m]);
-                            if (GATED) accu[m] = fmaf(u[j], xv[j], accu[m]);
+                for (int a = 0; a < 2; ++a)
+#pragma unroll
+                    for (int h = 0; h < H2; ++h)
+#pragma unroll
+                        for (int rr = 0; rr < RG; ++rr)
+#pragma unroll
+                            for (int m = 0; m < M; ++m) acc[a][h][rr][m] = 0.f;
+                for (int kb = 0; kb < K; kb += 256) {
+#pragma unroll
+                    for (int a = 0; a < 2; ++a) {
+                        const int k = kb + a * 128 + lane * 4;
+                        if (k < K) {
+                            float4 xv[M];
+#pragma unroll
+                            for (int m = 0; m < M; ++m) lds4(xs_a + (uint32_t)(m * K + k) * 4u, xv[m]);
+#pragma unroll
+                            for (int h = 0; h < H2; ++h)
+#pragma unroll
+                                for (int rr = 0; rr < RG; ++rr) {
+                                    float wv[4];
+                                    lds4(wrow[h][rr] + (uint32_t)k * sizeof(T), wv, T());
+#pragma unroll
+                                    for (int m = 0; m < M; ++m) {
+                                        float& c = acc[a][h][rr][m];
+                                        c = fmaf(wv[0], xv[m].x, c);
+                                        c = fmaf(wv[1], xv[m].y, c);
+                                        c = fmaf(wv[2], xv[m].z, c);
+                                        c = fmaf(wv[3], xv[m].w, c);
+                                    }
+                                }
                         }
                     }
                 }
+                // value index (rr * M + m) * H2 + h
+                float v[V];
 #pragma unroll
-                for (int m = 0; m < M; ++m) {
-                    const float v = warp_sum(acc[m]);
-                    const float uu = GATED ? warp_sum(accu[m]) : 0.f;
-                    if (lane == 0) {
-                        const int n = r0 + i;
-                        float* d = g.dst + (size_t)m * g.ld_dst + n;
-                        if (GATED) {
-                            *d = v / (1.0f + expf(-v)) * uu;
-                        } else if (g.epi == Epi::ADD) {
-                            *d = s.resid[m][n - n0] + v;
-                        } else if (g.epi == Epi::BIAS) {
-                            *d = v + g.bias[n];
-                        } else {
-                            *d = v;
-                        }
+                for (int h = 0; h < H2; ++h)
+#pragma unroll
+                    for (int rr = 0; rr < RG; ++rr)
+#pragma unroll
+                        for (int m = 0; m < M; ++m) v[(rr * M + m) * H2 + h] = acc[0][h][rr][m] + acc[1][h][rr][m];
+                const float sum = warp_sum_split<V>(v, lane);
+                // gated: the up sum of the same output sits in the next value index
+                const float up = GATED ? __shfl_down_sync(0xffffffffu, sum, 1 << (5 - NB)) : 0.f;
+                if (writer && jr < nr) {
+                    const int n = r0 + i0 + jr;
+                    const float rr_m = jm == 0 ? rm[0] : rm[1];
+                    const float a = sum * rr_m;
+                    float o;
+                    if (GATED) {
+                        const float u = up * rr_m;
+                        o = a / (1.0f + expf(-a)) * u;
+                    } else if (g.epi == Epi::ADD) {
+                        o = s.resid[buf][jm][n - n0] + a;
+                    } else if (g.epi == Epi::BIAS) {
+                        o = a + g.bias[n];
+                    } else {
+                        o = a;
                     }
+                    ll_put(g.dst + (size_t)jm * g.ld_dst + n, o, cur);
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.empty[slot]);
         }
+        if (tok && norm) ep[g.src_buf] = cur;
     }
 
-    __device__ void gemv(const Gemv& g) {
-        if (!ok) return;
-        prologue(g);
-        if (!ok) return;
+    template <int RG>
+    __device__ void gemv_rg(const Gemv& g, unsigned cur) {
         if (g.gated) {
-            if (g.M == 1) gemv_tiles<1, true>(g); else gemv_tiles<2, true>(g);
+            if (g.M == 1) gemv_run<RG, 1, true>(g, cur); else gemv_run<RG, 2, true>(g, cur);
         } else {
-            if (g.M == 1) gemv_tiles<1, false>(g); else gemv_tiles<2, false>(g);
+            if (g.M == 1) gemv_run<RG, 1, false>(g, cur); else gemv_run<RG, 2, false>(g, cur);
         }
     }
 
-    // ---------------- attention (A4 + A5) for M new tokens at positions p0.. of a layer
-    // smem use: the xin region (not needed during this phase): q [GQ][HD], k/v of new tokens [2][HD] each.
+    __device__ void gemv(const Gemv& g) {
+        const unsigned cur = next_phase();
+        if (!ok) return;
+        int n0, n1;
+        split_rows(g.N, n0, n1);
+        const int nrows = n1 - n0, rt = rows_per_tile<T>(g);
+        int rg = nrows >= 3 * NCW ? 4 : (nrows >= 3 * NCW / 2 ? 2 : 1);
+        while (rg > rt) rg >>= 1;
+        if (rg == 4) gemv_rg<4>(g, cur);
+        else if (rg == 2) gemv_rg<2>(g, cur);
+        else gemv_rg<1>(g, cur);
+        ep[g.dst_buf] = cur;
+    }
+
+    // ---------------- attention for M new tokens at positions p0.. of a layer
+    // smem use (the scratch region): q [M][GQ][HD], new
+    // k / v [M][HD] each (rounded as cached), per-warp softmax state.
     __device__ void attention(int l, const PBlk& B, int M, int p0, int S, bool talker) {
+        const unsigned cur = next_phase();
         if (!ok) return;
         const int nq = P.nq, nkv = P.nkv;
         const int nqkv = (nq + 2 * nkv) * HD;
-        const int items = M * nkv * S;
+        const int items = talker ? nkv * S : nkv;
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        float* sq = reinterpret_cast<float*>(xin());       // [GQ][HD]
-        float* sk = sq + GQ * HD;                          // [2][HD] new keys (rounded as cached)
-        float* sv = sk + 2 * HD;                           // [2][HD] new values
-        float* sm_m = sv + 2 * HD;                         // [NCW][GQ]
-        float* sm_l = sm_m + NCW * GQ;                     // [NCW][GQ]
-        float* sacc = sm_l + NCW * GQ;                     // [NCW][GQ][HD]
+        float* sq = xin_next();               // [2][GQ][HD]
+        float* sk = sq + 2 * GQ * HD;         // [2][HD]
+        float* sv = sk + 2 * HD;              // [2][HD]
+        float* sm_m = sv + 2 * HD;            // [NCW][GQ]
+        float* sm_l = sm_m + NCW * GQ;        // [NCW][GQ]
+        float* sacc = sm_l + NCW * GQ;        // [NCW][GQ][HD]
+        const unsigned eq = ep[BQKV];
         for (int item = blockIdx.x; item < items; item += gridDim.x) {
-            const int m = item / (nkv * S);
-            const int g = (item / S) % nkv;
-            const int sp = item % S;
-            const int pos = p0 + m;
-            const int n = pos + 1;
-            const int chunk = (n + S - 1) / S;
-            const int j0 = sp * chunk, j1 = min(n, j0 + chunk);
-            // cache [L][max_batch][nkv][cap][HD], row 0
-            T* Kg = (T*)B.Kc + (((size_t)l * P.max_batch + 0) * nkv + g) * B.cap * HD;
-            T* Vg = (T*)B.Vc + (((size_t)l * P.max_batch + 0) * nkv + g) * B.cap * HD;
-            // q heads of this group (token m), k/v of the new tokens 0..m: QK-norm + RoPE
-            const int tasks = GQ + 2 * (m + 1);
-            for (int t = warp; t < tasks; t += NCW) {
-                const float* src;
+            const int g = talker ? item / S : item;
+            const int sp = talker ? item % S : 0;
+            // q heads of group g and the new k / v of tokens 0..M-1: QK-norm + RoPE
+            bool good = true;
+            constexpr int per = GQ + 2;
+            for (int t = warp; t < M * per; t += NCW) {
+                const int m = t / per, u = t % per;
+                const Word* src;
                 float* dst;
                 const float* wn = nullptr;
-                int tp;       // position for RoPE
-                bool rope = true;
-                if (t < GQ) {
-                    src = P.qkv + (size_t)m * nqkv + (size_t)(g * GQ + t) * HD;
-                    dst = sq + t * HD; wn = B.q_norm + (size_t)l * HD; tp = pos;
-                } else if (t < GQ + m + 1) {
-                    const int mm = t - GQ;
-                    src = P.qkv + (size_t)mm * nqkv + (size_t)(nq + g) * HD;
-                    dst = sk + mm * HD; wn = B.k_norm + (size_t)l * HD; tp = p0 + mm;
+                bool rope = true, kv = true;
+                if (u < GQ) {
+                    src = P.qkv + (size_t)m * nqkv + (size_t)(g * GQ + u) * HD;
+                    dst = sq + (m * GQ + u) * HD; wn = B.q_norm + (size_t)l * HD; kv = false;
+                } else if (u == GQ) {
+                    src = P.qkv + (size_t)m * nqkv + (size_t)(nq + g) * HD;
+                    dst = sk + m * HD; wn = B.k_norm + (size_t)l * HD;
                 } else {
-                    const int mm = t - GQ - (m + 1);
-                    src = P.qkv + (size_t)mm * nqkv + (size_t)(nq + nkv + g) * HD;
-                    dst = sv + mm * HD; rope = false; tp = 0;
+                    src = P.qkv + (size_t)m * nqkv + (size_t)(nq + nkv + g) * HD;
+                    dst = sv + m * HD; rope = false;
                 }
-                float e[4];
+                float e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) e[i] = ldg(src + lane + 32 * i);
+                for (int i = 0; i < 4; ++i) good = good && ll_get(src + lane + 32 * i, eq, e[i], P);
                 if (rope) {
                     const float ss = warp_sum(e[0] * e[0] + e[1] * e[1] + e[2] * e[2] + e[3] * e[3]);
                     const float r = 1.0f / sqrtf(ss / (float)HD + P.eps);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) e[i] = e[i] * r * wn[lane + 32 * i];
+                    const int tp = p0 + m;
                     const float2 c0 = P.rope[(size_t)tp * (HD / 2) + lane];
                     const float2 c1 = P.rope[(size_t)tp * (HD / 2) + lane + 32];
                     float a = e[0], b = e[2];
@@ -535,168 +754,210 @@ struct Consumer {
                     a = e[1]; b = e[3];
                     e[1] = a * c1.x - b * c1.y; e[3] = b * c1.x + a * c1.y;
                 }
-                const bool is_kv = t >= GQ;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = is_kv ? to_f(from_f<T>(e[i])) : e[i];
+                for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = kv ? to_f(from_f<T>(e[i])) : e[i];
             }
-            consumer_sync();
-            // the split holding this token's own position appends its k / v to the cache
-            if (pos >= j0 && pos < j1) {
-                for (int i = threadIdx.x; i < HD; i += 256) {
-                    Kg[(size_t)pos * HD + i] = from_f<T>(sk[m * HD + i]);
-                    Vg[(size_t)pos * HD + i] = from_f<T>(sv[m * HD + i]);
-                }
-            }
-            // cached positions of a talker split come from the ring (prefetched)
-            const T* kring = nullptr;
-            const T* vring = nullptr;
-            int pj0 = 0, pj1 = 0, slot = -1;
-            if (talker && kv_prefetch_range<T>(P, B, M, p0, S, item, pj0, pj1)) {
-                slot = seq % NSLOT;
-                const unsigned round = seq / NSLOT;
-                ++seq;
-                if (!mbar_wait(&s.full[slot], round & 1, P)) { ok = false; }
-                kring = (const T*)s.ring[slot];
-                vring = kring + (size_t)(pj1 - pj0) * HD;
-            }
-            // online softmax over positions j0..j1-1, one position per warp step
-            float mx[GQ], lsum[GQ], acc[GQ][4];
-#pragma unroll
-            for (int hh = 0; hh < GQ; ++hh) {
-                mx[hh] = -INFINITY; lsum[hh] = 0.f;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc[hh][i] = 0.f;
-            }
-            const float scale = 0.08838834764831845f;
-            for (int j = j0 + warp; j < j1; j += NCW) {
-                float kk[4], vv[4];
-                if (kring && j >= pj0 && j < pj1) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        kk[i] = to_f(kring[(size_t)(j - pj0) * HD + lane + 32 * i]);
-                        vv[i] = to_f(vring[(size_t)(j - pj0) * HD + lane + 32 * i]);
-                    }
-                } else if (j < p0) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        kk[i] = ld_kv(Kg + (size_t)j * HD + lane + 32 * i);
-                        vv[i] = ld_kv(Vg + (size_t)j * HD + lane + 32 * i);
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        kk[i] = sk[(j - p0) * HD + lane + 32 * i];
-                        vv[i] = sv[(j - p0) * HD + lane + 32 * i];
+            if (!settle(good)) return;
+            // cache [L][max_batch][nkv][cap][HD], row 0
+            T* Kg = (T*)B.Kc + (((size_t)l * P.max_batch + 0) * nkv + g) * B.cap * HD;
+            T* Vg = (T*)B.Vc + (((size_t)l * P.max_batch + 0) * nkv + g) * B.cap * HD;
+            for (int m = 0; m < M; ++m) {
+                const int pos = p0 + m;
+                const int n = pos + 1;
+                const int chunk = (n + S - 1) / S;
+                const int j0 = sp * chunk, j1 = min(n, j0 + chunk);
+                // the split holding the token's own position appends its k / v
+                if (pos >= j0 && pos < j1) {
+                    for (int i = threadIdx.x; i < HD; i += 256) {
+                        Kg[(size_t)pos * HD + i] = from_f<T>(sk[m * HD + i]);
+                        Vg[(size_t)pos * HD + i] = from_f<T>(sv[m * HD + i]);
                     }
                 }
+                // cached positions of a talker split come from the ring (prefetched)
+                const T* kring = nullptr;
+                const T* vring = nullptr;
+                int pj0 = 0, pj1 = 0, slot = -1;
+                bool ring_ok = true;
+                if (talker && kv_prefetch_range<T>(p0, S, sp, pj0, pj1)) {
+                    slot = seq % NSLOT;
+                    const unsigned round = seq / NSLOT;
+                    ++seq;
+                    ring_ok = mbar_wait(&s.full[slot], round & 1, P);
+                    kring = (const T*)s.ring[slot];
+                    vring = kring + (size_t)(pj1 - pj0) * HD;
+                }
+                // online softmax over positions j0..j1-1, one position per warp step
+                float mx[GQ], lsum[GQ], acc[GQ][4];
+                const float* q = sq + m * GQ * HD;
 #pragma unroll
                 for (int hh = 0; hh < GQ; ++hh) {
-                    float d = 0.f;
+                    mx[hh] = -INFINITY; lsum[hh] = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) d = fmaf(sq[hh * HD + lane + 32 * i], kk[i], d);
-                    d = warp_sum(d) * scale;
-                    const float mn = fmaxf(mx[hh], d);
-                    const float c = expf(mx[hh] - mn);
-                    const float p = expf(d - mn);
-                    lsum[hh] = lsum[hh] * c + p;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[hh][i] = fmaf(p, vv[i], acc[hh][i] * c);
-                    mx[hh] = mn;
+                    for (int i = 0; i < 4; ++i) acc[hh][i] = 0.f;
                 }
-            }
-            __syncwarp();
-            if (slot >= 0 && lane == 0) mbar_arrive(&s.empty[slot]);
+                const float scale = 0.08838834764831845f;
+                for (int j = j0 + warp; j < j1 && ring_ok; j += NCW) {
+                    float kk[4], vv[4];
+                    if (kring && j >= pj0 && j < pj1) {
 #pragma unroll
-            for (int hh = 0; hh < GQ; ++hh) {
-                if (lane == 0) { sm_m[warp * GQ + hh] = mx[hh]; sm_l[warp * GQ + hh] = lsum[hh]; }
+                        for (int i = 0; i < 4; ++i) {
+                            kk[i] = to_f(kring[(size_t)(j - pj0) * HD + lane + 32 * i]);
+                            vv[i] = to_f(vring[(size_t)(j - pj0) * HD + lane + 32 * i]);
+                        }
+                    } else if (j < p0) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) sacc[(warp * GQ + hh) * HD + lane + 32 * i] = acc[hh][i];
-            }
-            consumer_sync();
-            // merge the warps -> this split's partial
-            float* part = P.part + ((((size_t)m * nkv + g) * S + sp) * GQ) * (HD + 2);
-            for (int idx = threadIdx.x; idx < GQ * HD; idx += 256) {
-                const int hh = idx / HD, d = idx % HD;
-                float ma = -INFINITY;
-                for (int w = 0; w < NCW; ++w) ma = fmaxf(ma, sm_m[w * GQ + hh]);
-                float a = 0.f, ls = 0.f;
-                for (int w = 0; w < NCW; ++w) {
-                    const float c = (ma == -INFINITY) ? 0.f : expf(sm_m[w * GQ + hh] - ma);
-                    a += sacc[(w * GQ + hh) * HD + d] * c;
-                    ls += sm_l[w * GQ + hh] * c;
+                        for (int i = 0; i < 4; ++i) {
+                            kk[i] = ld_kv(Kg + (size_t)j * HD + lane + 32 * i);
+                            vv[i] = ld_kv(Vg + (size_t)j * HD + lane + 32 * i);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            kk[i] = sk[(j - p0) * HD + lane + 32 * i];
+                            vv[i] = sv[(j - p0) * HD + lane + 32 * i];
+                        }
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < GQ; ++hh) {
+                        float d = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) d = fmaf(q[hh * HD + lane + 32 * i], kk[i], d);
+                        d = warp_sum(d) * scale;
+                        const float mn = fmaxf(mx[hh], d);
+                        const float c = expf(mx[hh] - mn);
+                        const float p = expf(d - mn);
+                        lsum[hh] = lsum[hh] * c + p;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc[hh][i] = fmaf(p, vv[i], acc[hh][i] * c);
+                        mx[hh] = mn;
+                    }
                 }
-                part[hh * (HD + 2) + d] = a;
-                if (d == 0) { part[hh * (HD + 2) + HD] = ma; part[hh * (HD + 2) + HD + 1] = ls; }
-            }
-            // the last split of this (token, head group) to finish merges all splits
-            consumer_sync();
-            if (threadIdx.x == 0) {
-                __threadfence();
-                const unsigned old = atomicAdd(&P.bar[2 + m * nkv + g], 1u);
-                s.flag = (old == (unsigned)S - 1);
-            }
-            consumer_sync();
-            if (s.flag) {
-                __threadfence();
-                const float* pb = P.part + (((size_t)m * nkv + g) * S) * GQ * (HD + 2);
+                __syncwarp();
+                if (slot >= 0 && lane == 0) mbar_arrive(&s.empty[slot]);
+#pragma unroll
+                for (int hh = 0; hh < GQ; ++hh) {
+                    if (lane == 0) { sm_m[warp * GQ + hh] = mx[hh]; sm_l[warp * GQ + hh] = lsum[hh]; }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) sacc[(warp * GQ + hh) * HD + lane + 32 * i] = acc[hh][i];
+                }
+                if (!settle(ring_ok)) return;
+                Word* o = P.o + (size_t)m * nq * HD + (size_t)g * GQ * HD;
+                if (S == 1) {
+                    // one split: merge the warps straight into the output words
+                    for (int idx = threadIdx.x; idx < GQ * HD; idx += 256) {
+                        const int hh = idx / HD, d = idx % HD;
+                        float ma = -INFINITY;
+                        for (int w = 0; w < NCW; ++w) ma = fmaxf(ma, sm_m[w * GQ + hh]);
+                        float a = 0.f, ls = 0.f;
+                        for (int w = 0; w < NCW; ++w) {
+                            const float c = (ma == -INFINITY) ? 0.f : expf(sm_m[w * GQ + hh] - ma);
+                            a += sacc[(w * GQ + hh) * HD + d] * c;
+                            ls += sm_l[w * GQ + hh] * c;
+                        }
+                        ll_put(o + idx, a / ls, cur);
+                    }
+                    consumer_sync();
+                    continue;
+                }
+                // this split's partial
+                float* part = P.part + (((size_t)g * S + sp) * GQ) * (HD + 2);
                 for (int idx = threadIdx.x; idx < GQ * HD; idx += 256) {
                     const int hh = idx / HD, d = idx % HD;
                     float ma = -INFINITY;
-                    for (int q = 0; q < S; ++q) ma = fmaxf(ma, ldg(pb + ((size_t)q * GQ + hh) * (HD + 2) + HD));
-                    float num = 0.f, den = 0.f;
-                    for (int q = 0; q < S; ++q) {
-                        const float* pq = pb + ((size_t)q * GQ + hh) * (HD + 2);
-                        const float mq = ldg(pq + HD);
-                        const float c = (mq == -INFINITY) ? 0.f : expf(mq - ma);
-                        num += ldg(pq + d) * c;
-                        den += ldg(pq + HD + 1) * c;
+                    for (int w = 0; w < NCW; ++w) ma = fmaxf(ma, sm_m[w * GQ + hh]);
+                    float a = 0.f, ls = 0.f;
+                    for (int w = 0; w < NCW; ++w) {
+                        const float c = (ma == -INFINITY) ? 0.f : expf(sm_m[w * GQ + hh] - ma);
+                        a += sacc[(w * GQ + hh) * HD + d] * c;
+                        ls += sm_l[w * GQ + hh] * c;
                     }
-                    P.o[(size_t)m * nq * HD + (size_t)(g * GQ + hh) * HD + d] = num / den;
+                    part[hh * (HD + 2) + d] = a;
+                    if (d == 0) { part[hh * (HD + 2) + HD] = ma; part[hh * (HD + 2) + HD + 1] = ls; }
                 }
-                if (threadIdx.x == 0) P.bar[2 + m * nkv + g] = 0u;
+                // the last split of this head group to finish merges all splits
+                consumer_sync();
+                if (threadIdx.x == 0) {
+                    __threadfence();
+                    const unsigned old = atomicAdd(&P.ctl[8 + g], 1u);
+                    const int last = old == (unsigned)S - 1;
+                    if (last) atomicExch(&P.ctl[8 + g], 0u);
+                    s.flag = last;
+                }
+                consumer_sync();
+                if (s.flag) {
+                    __threadfence();
+                    const float* pb = P.part + ((size_t)g * S) * GQ * (HD + 2);
+                    for (int idx = threadIdx.x; idx < GQ * HD; idx += 256) {
+                        const int hh = idx / HD, d = idx % HD;
+                        float ma = -INFINITY;
+                        for (int qs = 0; qs < S; ++qs) ma = fmaxf(ma, ldg(pb + ((size_t)qs * GQ + hh) * (HD + 2) + HD));
+                        float num = 0.f, den = 0.f;
+                        for (int qs = 0; qs < S; ++qs) {
+                            const float* pq = pb + ((size_t)qs * GQ + hh) * (HD + 2);
+                            const float mq = ldg(pq + HD);
+                            const float c = (mq == -INFINITY) ? 0.f : expf(mq - ma);
+                            num += ldg(pq + d) * c;
+                            den += ldg(pq + HD + 1) * c;
+                        }
+                        ll_put(o + idx, num / den, cur);
+                    }
+                }
+                consumer_sync();
             }
-            consumer_sync();
         }
+        ep[BO] = cur;
     }
 
-    // ---------------- draws on CTA 0
-    __device__ void sample_cp(int sidx) {
-        if (!ok || blockIdx.x != 0) return;
+    // ---------------- draws
+    // Predictor draw s on every CTA: the same logits and the same deterministic
+    // draw give every CTA the same id; CTA 0 records it.
+    __device__ void draw_cp(int sidx) {
+        next_phase();
+        if (!ok) return;
         SampSmem& sm = samp_ptr<T>(s, P.xin_bytes);
+        if (!settle(ll_fetch(P.cpl, sm.l, P.cpV, ep[BCPL], nullptr, P))) return;
         const q3tts_sampling p = P.P[0];
-        if (P.cap_c && P.cap_slot[0] >= 0 && frame < P.cap_T) {
+        if (blockIdx.x == 0 && P.cap_c && P.cap_slot[0] >= 0 && frame < P.cap_T) {
             float* dst = P.cap_c + (((size_t)P.cap_slot[0] * P.cap_T + frame) * (P.G - 1) + sidx) * P.cpV;
-            for (int i = threadIdx.x; i < P.cpV; i += 256) dst[i] = ldg(P.cpl + i);
+            for (int i = threadIdx.x; i < P.cpV; i += 256) dst[i] = sm.l[i];
         }
         const DrawCfg d{p.cp_do_sample, p.cp_temperature, p.cp_top_k, p.cp_top_p};
-        const int id = sample_row(sm, P.cpl, P.cpV, d, false, 1.0f, nullptr, nullptr, 0, 0, -1, 0, 0, p.seed, 0u,
+        const int id = sample_row(sm, nullptr, P.cpV, d, false, 1.0f, nullptr, nullptr, 0, 0, -1, 0, 0, p.seed, 0u,
                                   (uint32_t)frame, (uint32_t)(sidx + 1));
-        if (threadIdx.x == 0) {
-            if (id < 0) {
-                atomicOr(P.err, ERRB_NAN);
-                RowState& rs = P.rows[0];
-                rs.finished = 1;
-                rs.reason = Q3_FINISHED_ERROR;
-                rs.frames = frame;
-                atomicExch(&P.bar[1], 1u);
-            } else {
-                P.codes[(size_t)frame * MAX_GROUPS + sidx + 1] = id;
+        if (id < 0) {
+            if (threadIdx.x == 0) {
+                if (blockIdx.x == 0) {
+                    RowState& rs = P.rows[0];
+                    rs.finished = 1;
+                    rs.reason = Q3_FINISHED_ERROR;
+                    rs.frames = frame;
+                }
+                raise_abort(P, ERRB_NAN);
             }
+            ok = false;
+            return;
         }
+        if (threadIdx.x == 0) {
+            s.codes[sidx + 1] = id;
+            if (blockIdx.x == 0) P.codes[(size_t)frame * MAX_GROUPS + sidx + 1] = id;
+        }
+        consumer_sync();
     }
 
-    __device__ void sample_talker() {
+    __device__ void draw_talker() {
+        next_phase();
         if (!ok || blockIdx.x != 0) return;
         SampSmem& sm = samp_ptr<T>(s, P.xin_bytes);
+        if (!settle(ll_fetch(P.logits, sm.l, P.V, ep[BLOG], nullptr, P))) return;
         RowState& rs = P.rows[0];
         const q3tts_sampling p = P.P[0];
         const int k = frame + 1;
         if (P.cap_t && P.cap_slot[0] >= 0 && k <= P.cap_T) {
             float* dst = P.cap_t + ((size_t)P.cap_slot[0] * (P.cap_T + 1) + k) * P.V;
-            for (int i = threadIdx.x; i < P.V; i += 256) dst[i] = ldg(P.logits + i);
+            for (int i = threadIdx.x; i < P.V; i += 256) dst[i] = sm.l[i];
         }
         const DrawCfg d{p.do_sample, p.temperature, p.top_k, p.top_p};
-        int id = sample_row(sm, P.logits, P.V, d, true, p.repetition_penalty, rs.seen, nullptr, k, p.min_new_tokens,
+        int id = sample_row(sm, nullptr, P.V, d, true, p.repetition_penalty, rs.seen, nullptr, k, p.min_new_tokens,
                             P.eos, P.sup_lo, P.sup_hi, p.seed, 0u, (uint32_t)k, 0u);
         if (threadIdx.x == 0) {
             rs.frames = k;
@@ -720,44 +981,37 @@ struct Consumer {
 
 // ------------------------------------------------------------------ schedule
 template <typename T, class R>
-__device__ void gemv_phase(R& r, const Gemv& g) {
-    r.gemv(g);
-    r.barrier();
-}
-
-template <typename T, class R>
-__device__ void layer(R& r, const FrameParams& P, const PBlk& B, int l, int M, int p0, int S, float* x, Tok tok,
-                      int s_idx, bool talker) {
+__device__ void layer(R& r, const FrameParams& P, const PBlk& B, int l, int M, int p0, int S, Word* x, int xb,
+                      Tok tok, int s_idx, bool talker) {
     const size_t e = sizeof(T);
     const int nq = P.nq, nkv = P.nkv, H = B.H, F = B.F;
     const int nqkv = (nq + 2 * nkv) * HD;
     Gemv g{};
-    // A2 + A3: (token assembly) + RMSNorm + q/k/v projection
+    // (token assembly) + RMSNorm + q/k/v projection
     g.W = (const char*)B.wqkv + (size_t)l * nqkv * H * e; g.N = nqkv; g.K = H; g.M = M;
-    g.pro = Pro::NORM; g.tok = tok; g.epi = Epi::STORE; g.pro_src = x; g.pro_ld = H;
-    g.norm_w = B.attn_norm + (size_t)l * H; g.dst = P.qkv; g.ld_dst = nqkv; g.s_idx = s_idx;
-    gemv_phase<T>(r, g);
-    // A4 + A5
+    g.pro = Pro::NORM; g.tok = tok; g.epi = Epi::STORE; g.src = x; g.src_ld = H; g.src_buf = xb;
+    g.norm_w = B.attn_norm + (size_t)l * H; g.dst = P.qkv; g.ld_dst = nqkv; g.dst_buf = BQKV; g.s_idx = s_idx;
+    r.gemv(g);
+    // QK-norm, RoPE, cache append, attention
     r.attention(l, B, M, p0, S, talker);
-    r.barrier();
-    // A6: O projection + residual
+    // O projection + residual
     g = Gemv{};
     g.W = (const char*)B.wo + (size_t)l * H * nq * HD * e; g.N = H; g.K = nq * HD; g.M = M;
-    g.pro = Pro::LOAD; g.tok = Tok::NONE; g.epi = Epi::ADD; g.pro_src = P.o; g.pro_ld = nq * HD;
-    g.dst = x; g.ld_dst = H;
-    gemv_phase<T>(r, g);
-    // A7: RMSNorm + gate/up + SiLU(g)*u
+    g.pro = Pro::LOAD; g.tok = Tok::NONE; g.epi = Epi::ADD; g.src = P.o; g.src_ld = nq * HD; g.src_buf = BO;
+    g.dst = x; g.ld_dst = H; g.dst_buf = xb;
+    r.gemv(g);
+    // RMSNorm + gate/up + SiLU(g)*u
     g = Gemv{};
     g.W = (const char*)B.wgu + (size_t)l * 2 * F * H * e; g.N = F; g.K = H; g.M = M; g.gated = true;
-    g.pro = Pro::NORM; g.tok = Tok::NONE; g.epi = Epi::GATED; g.pro_src = x; g.pro_ld = H;
-    g.norm_w = B.mlp_norm + (size_t)l * H; g.dst = P.act; g.ld_dst = F;
-    gemv_phase<T>(r, g);
-    // A8: down projection + residual
+    g.pro = Pro::NORM; g.tok = Tok::NONE; g.epi = Epi::GATED; g.src = x; g.src_ld = H; g.src_buf = xb;
+    g.norm_w = B.mlp_norm + (size_t)l * H; g.dst = P.act; g.ld_dst = F; g.dst_buf = BACT;
+    r.gemv(g);
+    // down projection + residual
     g = Gemv{};
     g.W = (const char*)B.wd + (size_t)l * H * F * e; g.N = H; g.K = F; g.M = M;
-    g.pro = Pro::LOAD; g.tok = Tok::NONE; g.epi = Epi::ADD; g.pro_src = P.act; g.pro_ld = F;
-    g.dst = x; g.ld_dst = H;
-    gemv_phase<T>(r, g);
+    g.pro = Pro::LOAD; g.tok = Tok::NONE; g.epi = Epi::ADD; g.src = P.act; g.src_ld = F; g.src_buf = BACT;
+    g.dst = x; g.ld_dst = H; g.dst_buf = xb;
+    r.gemv(g);
 }
 
 template <typename T, class R>
@@ -773,30 +1027,31 @@ __device__ void frame_schedule(R& r, const FrameParams& P) {
         if (proj) {
             Gemv g{};
             g.W = P.cp_proj_w; g.N = P.Hc; g.K = P.H; g.M = M; g.pro = Pro::RAW; g.tok = tok; g.epi = Epi::BIAS;
-            g.bias = P.cp_proj_b; g.dst = P.cx; g.ld_dst = P.Hc; g.s_idx = s;
-            gemv_phase<T>(r, g);
+            g.bias = P.cp_proj_b; g.dst = P.cx; g.ld_dst = P.Hc; g.dst_buf = BCX; g.s_idx = s;
+            r.gemv(g);
             layer_tok = Tok::NONE;
         }
         for (int l = 0; l < P.c.L && r.live(); ++l)
-            layer<T>(r, P, P.c, l, M, 0 + (s == 0 ? 0 : s + 1), 1, P.cx, l == 0 ? layer_tok : Tok::NONE, s, false);
+            layer<T>(r, P, P.c, l, M, s == 0 ? 0 : s + 1, 1, P.cx, BCX, l == 0 ? layer_tok : Tok::NONE, s, false);
         // final norm of the last token -> head[s]
         Gemv g{};
         g.W = (const char*)P.cp_heads + (size_t)s * P.cpV * P.Hc * e; g.N = P.cpV; g.K = P.Hc; g.M = 1;
-        g.pro = Pro::NORM; g.tok = Tok::NONE; g.epi = Epi::STORE; g.pro_src = P.cx + (size_t)(M - 1) * P.Hc;
-        g.pro_ld = P.Hc; g.norm_w = P.c.final_norm; g.dst = P.cpl; g.ld_dst = P.cpV;
-        gemv_phase<T>(r, g);
-        r.sample_cp(s);
-        r.barrier();
+        g.pro = Pro::NORM; g.tok = Tok::NONE; g.epi = Epi::STORE; g.src = P.cx + (size_t)(M - 1) * P.Hc;
+        g.src_ld = P.Hc; g.src_buf = BCX; g.norm_w = P.c.final_norm; g.dst = P.cpl; g.ld_dst = P.cpV;
+        g.dst_buf = BCPL;
+        r.gemv(g);
+        r.draw_cp(s);
     }
     // talker
     r.prepare_talker();
     for (int l = 0; l < P.t.L && r.live(); ++l)
-        layer<T>(r, P, P.t, l, 1, r.talker_pos(), P.n_splits, P.x, l == 0 ? Tok::TALK : Tok::NONE, 0, true);
+        layer<T>(r, P, P.t, l, 1, r.talker_pos(), P.n_splits, P.x, BX, l == 0 ? Tok::TALK : Tok::NONE, 0, true);
     Gemv g{};
     g.W = P.codec_head; g.N = P.V; g.K = P.H; g.M = 1; g.pro = Pro::NORM; g.tok = Tok::NONE; g.epi = Epi::STORE;
-    g.pro_src = P.x; g.pro_ld = P.H; g.norm_w = P.t.final_norm; g.dst = P.logits; g.ld_dst = P.V; g.hout = P.h;
-    gemv_phase<T>(r, g);
-    r.sample_talker();
+    g.src = P.x; g.src_ld = P.H; g.src_buf = BX; g.norm_w = P.t.final_norm; g.dst = P.logits; g.ld_dst = P.V;
+    g.dst_buf = BLOG; g.hout = P.h;
+    r.gemv(g);
+    r.draw_talker();
 }
 
 template <typename T, int GQ>
@@ -804,44 +1059,48 @@ __global__ void __launch_bounds__(NTHREADS, 1) frame_kernel(const FrameParams* _
     extern __shared__ __align__(128) unsigned char smraw[];
     FSmem<T>& s = *reinterpret_cast<FSmem<T>*>(smraw);
     const FrameParams& P = *Pp;
-    if (P.rows[0].finished) return;   // uniform over the grid
+    const RowState& rs = P.rows[0];
+    if (rs.finished || aborted(P)) return;   // uniform over the grid
+    const int frame = rs.sel - 1, pos = rs.pos, code0 = rs.code0;
+    // the same checks on every CTA: all leave, or none
+    if (frame < 0 || frame >= P.frames_cap || code0 < 0 || code0 >= P.V || rs.sel >= (1 << 22)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(P.err, ERRB_BOUNDS);
+        return;
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSLOT; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], NCW); }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        s.aborted = 0;
+        s.codes[0] = code0;
+        if (blockIdx.x == 0) P.codes[(size_t)frame * MAX_GROUPS] = code0;
     }
     __syncthreads();
     const int warp = threadIdx.x >> 5;
     if (warp == NCW) {
         if ((threadIdx.x & 31) == 0) {
             Producer<T> pr{s, P};
-            pr.pos = P.rows[0].pos;
+            pr.pos = pos;
             frame_schedule<T>(pr, P);
             pr.drain();
         }
         return;
     }
     Consumer<T, GQ> c{s, P};
-    c.frame = P.rows[0].sel - 1;
-    c.pos = P.rows[0].pos;
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        if (c.frame < 0 || c.frame >= P.frames_cap || P.rows[0].code0 < 0 || P.rows[0].code0 >= P.V) {
-            atomicOr(P.err, ERRB_BOUNDS);
-            atomicExch(&P.bar[1], 1u);
-        } else {
-            P.codes[(size_t)c.frame * MAX_GROUPS] = P.rows[0].code0;
-        }
-    }
+    c.frame = frame;
+    c.pos = pos;
+    c.base = (unsigned)rs.sel << 10;
     frame_schedule<T>(c, P);
 }
 
 // ------------------------------------------------------------------ host side
 template <typename T>
 static size_t smem_for(int xin_bytes) {
-    return align128(sizeof(FSmem<T>)) + align128((size_t)xin_bytes) + sizeof(SampSmem);
+    return align128(sizeof(FSmem<T>)) + 2 * align128((size_t)xin_bytes) + sizeof(SampSmem);
 }
 
-size_t frame_attn_scratch_bytes() { return (size_t)(2 * HD + 4 * HD + 2 * NCW * 2 + NCW * 2 * HD) * sizeof(float); }
+size_t frame_attn_scratch_bytes() {
+    constexpr int GQ = 2;
+    return (size_t)(2 * GQ * HD + 4 * HD + 2 * NCW * GQ + NCW * GQ * HD) * sizeof(float);
+}
 
 size_t frame_smem_bytes(int dtype, int xin_bytes) {
     const size_t b = dtype == Q3_BF16 ? smem_for<bf16>(xin_bytes) : smem_for<float>(xin_bytes);

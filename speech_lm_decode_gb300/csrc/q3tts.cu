@@ -10,6 +10,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "frame_params.h"
 #include "kernels.h"
@@ -26,9 +28,11 @@ constexpr int MIN_SAMPLE_SETS = 256; // staging for q3tts_sample_logits
 struct Layout {
     size_t kvK, kvV, ckvK, ckvV, rope, rows, params, h, x, cx, tok, opA, opB, headop, qkv, pm, pl, pacc, logits,
         cplogits, t_row, t_pos, c_row, c_pos, last_row, codes, codes_stage, text, pad, err, s_params, s_logits, s_sel, s_row, s_ids, s_seen, cap_slot,
-        fparams, fbar, fpart, fo, fact, tcs;
+        fparams, fctl, fpart, fll, tcs;
     size_t total;
     int mmax, kA, kB, rope_rows, frames_cap, n_sets, vmax, fsplits;
+    size_t fll_words;                   // exchange words of the frame kernel
+    size_t fw_x, fw_cx, fw_qkv, fw_o, fw_act, fw_log, fw_cpl;   // word offsets in fll
 };
 
 size_t esize(int dtype) { return dtype == Q3_BF16 ? 2 : 4; }
@@ -94,10 +98,21 @@ Layout make_layout(const q3tts_config& c) {
     // persistent frame kernel (batch 1)
     L.fsplits = 16;   // partial buffers sized for the largest split count
     L.fparams = take(sizeof(FrameParams));
-    L.fbar = take(FRAME_BAR_WORDS * sizeof(unsigned));
-    L.fpart = take((size_t)2 * c.n_kv_heads * L.fsplits * (c.n_q_heads / c.n_kv_heads) * (HD + 2) * sizeof(float));
-    L.fo = take((size_t)2 * c.n_q_heads * HD * sizeof(float));
-    L.fact = take((size_t)2 * std::max(c.ffn, c.cp_ffn) * sizeof(float));
+    L.fctl = take(FRAME_CTL_WORDS * sizeof(unsigned));
+    L.fpart = take((size_t)c.n_kv_heads * L.fsplits * (c.n_q_heads / c.n_kv_heads) * (HD + 2) * sizeof(float));
+    {
+        size_t w = 0;
+        auto words = [&](size_t n) { size_t o = w; w += (n + 31) / 32 * 32; return o; };
+        L.fw_x = words(c.hidden);
+        L.fw_cx = words(2 * (size_t)c.cp_hidden);
+        L.fw_qkv = words(2 * (size_t)nqkv);
+        L.fw_o = words(2 * (size_t)c.n_q_heads * HD);
+        L.fw_act = words(2 * (size_t)std::max(c.ffn, c.cp_ffn));
+        L.fw_log = words(c.codec_vocab);
+        L.fw_cpl = words(c.cp_vocab);
+        L.fll_words = w;
+        L.fll = take(w * sizeof(Word));
+    }
     // tensor-core path: bf16 high / low parts of an fp32 operand [mmax][kmax]
     L.tcs = c.dtype == Q3_BF16 ? take((size_t)L.mmax * std::max(L.kA, L.kB) * 4) : take(256);
     L.total = off;
@@ -206,6 +221,12 @@ void debug_wait(cudaStream_t st, const char* what) {
     }
 }
 
+// NVTX range for profilers (header-only NVTX3; no cost without a tool attached)
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
+
 void invalidate_graph(q3tts* h) {
     if (h->exec) cudaGraphExecDestroy(h->exec);
     if (h->graph) cudaGraphDestroy(h->graph);
@@ -268,7 +289,6 @@ int enqueue_cp_input(q3tts* h, int M) {
 // One talker step for the whole batch: complete frame k-1 through the code
 // predictor, assemble the next talker input, run the talker, select code0.
 int enqueue_frame(q3tts* h) {
-    CK(cudaMemsetAsync(h->p<unsigned>(h->L.fbar), 0, FRAME_BAR_WORDS * sizeof(unsigned), h->st));
     CK(launch_frame(h->c.dtype, h->p<FrameParams>(h->L.fparams), h->frame_grid, h->frame_smem, h->st)); debug_wait(h->st, "launch_frame");
     return Q3_OK;
 }
@@ -375,17 +395,17 @@ int upload_frame_params(q3tts* h) {
     P.H = c.hidden; P.Hc = c.cp_hidden; P.V = c.codec_vocab; P.cpV = c.cp_vocab; P.G = c.n_groups;
     P.nq = c.n_q_heads; P.nkv = c.n_kv_heads; P.eos = c.eos_id; P.sup_lo = c.suppress_lo; P.sup_hi = c.suppress_hi;
     P.n_splits = h->frame_splits;
-    P.kmax = std::max(std::max(std::max(c.hidden, c.cp_hidden), std::max(c.ffn, c.cp_ffn)), c.n_q_heads * HD);
     P.max_batch = c.max_batch;
     P.eps = c.rms_eps;
     P.rope = h->p<float2>(h->L.rope); P.rope_rows = h->L.rope_rows;
     P.rows = h->rows(); P.P = h->p<q3tts_sampling>(h->L.params);
-    P.x = h->p<float>(h->L.x); P.cx = h->p<float>(h->L.cx); P.h = h->p<float>(h->L.h);
-    P.qkv = h->p<float>(h->L.qkv); P.part = h->p<float>(h->L.fpart); P.o = h->p<float>(h->L.fo);
-    P.act = h->p<float>(h->L.fact); P.logits = h->p<float>(h->L.logits); P.cpl = h->p<float>(h->L.cplogits);
+    Word* ll = h->p<Word>(h->L.fll);
+    P.x = ll + h->L.fw_x; P.cx = ll + h->L.fw_cx; P.qkv = ll + h->L.fw_qkv; P.o = ll + h->L.fw_o;
+    P.act = ll + h->L.fw_act; P.logits = ll + h->L.fw_log; P.cpl = ll + h->L.fw_cpl;
+    P.h = h->p<float>(h->L.h); P.part = h->p<float>(h->L.fpart);
     P.codes = h->p<int32_t>(h->L.codes); P.frames_cap = h->L.frames_cap;
     P.text = h->p<float>(h->L.text); P.pad = h->p<float>(h->L.pad);
-    P.bar = h->p<unsigned>(h->L.fbar); P.err = h->err();
+    P.ctl = h->p<unsigned>(h->L.fctl); P.err = h->err();
     P.cap_t = h->cap_t; P.cap_c = h->cap_c; P.cap_slot = h->p<int>(h->L.cap_slot); P.cap_T = h->cap_T;
     P.xin_bytes = h->frame_xin;
     CK(cudaMemcpyAsync(h->p<FrameParams>(h->L.fparams), &P, sizeof P, cudaMemcpyHostToDevice, h->st));
@@ -449,11 +469,12 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
         const int H = cfg->hidden, Hc = cfg->cp_hidden, nqh = cfg->n_q_heads * HD;
-        const int kmax_cp = std::max(std::max(Hc, cfg->cp_ffn), std::max(nqh, H != Hc ? H : 0));
-        const int kmax_t = std::max(std::max(H, cfg->ffn), nqh);
-        h->frame_xin = (int)std::max((size_t)4 * std::max(2 * kmax_cp, kmax_t), frame_attn_scratch_bytes());
+        // input-vector buffers: the widest [M][K] fp32 of any GEMV phase
+        const int kx_t = std::max(std::max(H, cfg->ffn), nqh);
+        const int kx_c = std::max(std::max(Hc, cfg->cp_ffn), std::max(nqh, H != Hc ? H : 0));
+        h->frame_xin = (int)std::max((size_t)4 * std::max(kx_t, 2 * kx_c), frame_attn_scratch_bytes());
         const size_t e = esize(cfg->dtype);
-        const size_t tile = 24 * 1024;
+        const size_t tile = FRAME_TILE;
         const bool tiles_fit = (size_t)H * e * 2 <= tile && (size_t)Hc * e * 2 <= tile &&
                                (size_t)std::max(cfg->ffn, cfg->cp_ffn) * e <= tile && (size_t)nqh * e <= tile;
         h->frame_smem = frame_smem_bytes(cfg->dtype, h->frame_xin);
@@ -469,11 +490,23 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
                 h->frame_ok = false;
             }
         }
-        h->frame_grid = sms;
+        // grid: every GEMV phase must give each CTA at least one output row (the
+        // exchange words rely on it), so no more CTAs than the narrowest output
+        const int nqkv = (cfg->n_q_heads + 2 * cfg->n_kv_heads) * HD;
+        int grid = sms;
+        for (int n : {nqkv, H, cfg->ffn, Hc, cfg->cp_ffn, cfg->codec_vocab, cfg->cp_vocab}) grid = std::min(grid, n);
+        const int phases = (cfg->n_groups - 1) * ((H != Hc ? 1 : 0) + 5 * cfg->cp_layers + 2) + 5 * cfg->n_layers + 2;
+        // residual rows a CTA updates in one phase fit its buffer
+        auto rows = [&](int n) { return (n + grid - 1) / grid; };
+        const bool v_ok = rows(H) <= FRAME_MAX_ROWS && rows(Hc) <= FRAME_MAX_ROWS;
+        const bool grid_ok = grid >= cfg->n_kv_heads && v_ok && phases <= FRAME_MAX_PHASES &&
+                             cfg->n_kv_heads + 8 <= FRAME_CTL_WORDS && H <= FRAME_MAX_NORM && Hc <= FRAME_MAX_NORM;
+        h->frame_ok = h->frame_ok && grid_ok;
+        h->frame_grid = grid;
         // talker attention splits: a split's cached K and V fit one ring slot
         const int per_split = (int)(tile / (2 * HD * e));
         h->frame_splits = std::max(1, std::min((cfg->max_ctx + per_split - 1) / per_split,
-                                               std::min(16, std::max(1, sms / cfg->n_kv_heads))));
+                                               std::min(16, std::max(1, grid / cfg->n_kv_heads))));
         const char* ds = getenv("Q3TTS_DEBUG_SYNC");
         g_debug_sync = ds && ds[0] == '1';
         const char* tc = getenv("Q3TTS_TENSOR_CORES");
@@ -519,6 +552,7 @@ int q3tts_prefill(q3tts_t* h, int batch, const float* prompt, const int32_t* pro
                   const int32_t* text_offsets, const float* tts_pad, const q3tts_sampling* rows_in,
                   int32_t* code0_out) {
     if (!h) return Q3_ERR_ARG;
+    NvtxRange nvtx("q3tts_prefill");
     const q3tts_config& c = h->c;
     if (batch < 1 || batch > c.max_batch) return fail(h, Q3_ERR_CAPACITY, "batch %d outside 1..%d", batch, c.max_batch);
     if (!prompt || !prompt_offsets || !text_offsets || !tts_pad || !rows_in)
@@ -572,6 +606,12 @@ int q3tts_prefill(q3tts_t* h, int batch, const float* prompt, const int32_t* pro
     CK(cudaMemsetAsync(h->p<int32_t>(h->L.codes), 0xFF,
                        (size_t)c.max_batch * h->L.frames_cap * MAX_GROUPS * sizeof(int32_t), h->st));
     CK(cudaMemsetAsync(h->err(), 0, 4 * sizeof(int), h->st));
+    if (h->frame_ok) {
+        // exchange words start at epoch 0 (never a live epoch); abort flag and
+        // split counters start at 0
+        CK(cudaMemsetAsync(h->p<Word>(h->L.fll), 0, h->L.fll_words * sizeof(Word), h->st));
+        CK(cudaMemsetAsync(h->p<unsigned>(h->L.fctl), 0, FRAME_CTL_WORDS * sizeof(unsigned), h->st));
+    }
 
     // prompt through the talker, in chunks of whole tokens across rows
     const int total = prompt_offsets[batch];
@@ -623,6 +663,7 @@ int q3tts_prefill(q3tts_t* h, int batch, const float* prompt, const int32_t* pro
 int q3tts_step_frames(q3tts_t* h, int n_frames, int32_t* codes_out, int32_t* frames_emitted,
                       int32_t* finish_reason) {
     if (!h) return Q3_ERR_ARG;
+    NvtxRange nvtx("q3tts_step_frames");
     if (!h->prefilled) return fail(h, Q3_ERR_STATE, "q3tts_step_frames before q3tts_prefill");
     if (n_frames < 0) return fail(h, Q3_ERR_ARG, "negative n_frames");
     const q3tts_config& c = h->c;

@@ -214,6 +214,8 @@ struct DrawCfg {
 
 // One selection.  All 256 threads call it; returns the id (or -1 when the
 // logits hold NaN / +inf or no finite value) to every thread.
+//   lg: the raw logits in global memory, or nullptr when sm.l[0, V) holds them
+//       (each thread i of the block must have written the entries i, i + 256, ...).
 //   seen_bits / seen_bytes: ids drawn before (penalty); one of them or neither.
 static __device__ __noinline__ int sample_row(SampSmem& sm, const float* __restrict__ lg, int V, DrawCfg d, bool talker, float penalty,
                           const uint32_t* seen_bits, const uint8_t* seen_bytes, int sel, int min_new, int eos,
@@ -221,7 +223,9 @@ static __device__ __noinline__ int sample_row(SampSmem& sm, const float* __restr
     const int tid = threadIdx.x;
     int bad = 0;
     for (int i = tid; i < V; i += ST) {
-        float v = __ldcg(lg + i);   // logits may come from other CTAs of the same launch
+        // logits may come from other CTAs of the same launch (read at L2); with
+        // lg == nullptr the caller has already placed them in sm.l
+        float v = lg ? __ldcg(lg + i) : sm.l[i];
         bad |= (isnan(v) || v == INFINITY) ? 1 : 0;
         if (talker) {
             const bool seen = seen_bits ? ((seen_bits[i >> 5] >> (i & 31)) & 1u) : (seen_bytes ? seen_bytes[i] : 0);
