@@ -68,7 +68,8 @@ struct FrameParams {
 
 constexpr int FRAME_CTL_WORDS = 64;
 constexpr int FRAME_MAX_ROWS = 128;   // residual rows one CTA updates in one phase
-constexpr int FRAME_TILE = 20 * 1024; // bytes of one weight ring slot
+constexpr int FRAME_TILE = 24 * 1024; // bytes of one weight ring slot
+constexpr int FRAME_SLOTS = 6;        // ring slots
 constexpr int FRAME_MAX_PHASES = 1024;  // phases of one launch (epoch = selection * 1024 + phase)
 constexpr int FRAME_MAX_NORM = 2048;    // widest RMSNorm input (talker and predictor widths)
 

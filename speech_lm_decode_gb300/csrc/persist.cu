@@ -54,7 +54,7 @@ namespace q3 {
 constexpr int NCW = 8;                       // consumer warps
 constexpr int NTHREADS = (NCW + 1) * 32;     // + one producer warp
 constexpr int TILE = FRAME_TILE;             // bytes per ring slot
-constexpr int NSLOT = 5;
+constexpr int NSLOT = FRAME_SLOTS;
 constexpr long long WAIT_LIMIT = 4000000000LL;  // cycles (~2 s) before a wait gives up
 constexpr int NORM_MAX = FRAME_MAX_NORM;     // widest vector an RMSNorm prologue normalizes
 
@@ -201,9 +201,9 @@ struct FSmem {
     float pss[2][NCW][2];               // per-warp sums of squares of the RMSNorm inputs [phase parity]
     int codes[MAX_GROUPS];              // this frame's codes as drawn so far
     int flag;
-    // then: two input-vector buffers (fp32 [M][K], one per GEMV phase parity;
-    // the attention phase's scratch shares the one the next GEMV phase fills);
-    // then the draw's scratch
+    // then one region for: two input-vector buffers (fp32 [M][K], one per GEMV
+    // phase parity; the attention phase's scratch shares the one the next GEMV
+    // phase fills) or, during a draw (when no GEMV reads them), the draw's scratch
 };
 
 __host__ __device__ constexpr size_t align128(size_t v) { return (v + 127) & ~(size_t)127; }
@@ -213,9 +213,8 @@ __device__ __forceinline__ float* xin_ptr(FSmem<T>& s, int buf, int xin_bytes) {
                                     (size_t)buf * align128((size_t)xin_bytes));
 }
 template <typename T>
-__device__ __forceinline__ SampSmem& samp_ptr(FSmem<T>& s, int xin_bytes) {
-    const size_t off = align128(sizeof(FSmem<T>)) + 2 * align128((size_t)xin_bytes);
-    return *reinterpret_cast<SampSmem*>(reinterpret_cast<unsigned char*>(&s) + off);
+__device__ __forceinline__ SampSmem& samp_ptr(FSmem<T>& s) {
+    return *reinterpret_cast<SampSmem*>(reinterpret_cast<unsigned char*>(&s) + align128(sizeof(FSmem<T>)));
 }
 
 // ------------------------------------------------------------------ the frame schedule
@@ -345,6 +344,24 @@ struct Producer {
 // ------------------------------------------------------------------ GEMV helpers
 __device__ __forceinline__ void lds_f32x4(uint32_t a, float& x, float& y, float& z, float& w) {
     asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(x), "=f"(y), "=f"(z), "=f"(w) : "r"(a));
+}
+// pointer through an opaque register move: reads through the result cannot be
+// scheduled before the statement (a compiler barrier tied to the data)
+template <typename P>
+__device__ __forceinline__ P* launder(P* p) {
+    unsigned long long v = reinterpret_cast<unsigned long long>(p);
+    asm volatile("mov.b64 %0, %0;" : "+l"(v)::"memory");
+    return reinterpret_cast<P*>(v);
+}
+// 4 consecutive elements (index multiple of 4) as fp32
+__device__ __forceinline__ void load4(const bf16* p, float (&v)[4]) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    v[0] = __uint_as_float(u.x << 16); v[1] = __uint_as_float(u.x & 0xffff0000u);
+    v[2] = __uint_as_float(u.y << 16); v[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+__device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
+    const float4 f = *reinterpret_cast<const float4*>(p);
+    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
 }
 // 4 consecutive elements at shared address a as fp32
 __device__ __forceinline__ void lds4(uint32_t a, float (&v)[4], float) { lds_f32x4(a, v[0], v[1], v[2], v[3]); }
@@ -580,9 +597,7 @@ struct Consumer {
         // the warp (no bank conflicts), and the vector is read once per group.
         const int rt = rows_per_tile<T>(g);
         const int gpt = (rt + RG - 1) / RG;   // row groups of a full tile
-        const uint32_t row_bytes = (uint32_t)K * sizeof(T);
-        const uint32_t xs_a = smem_u32(xs);
-        const uint32_t ring_a = smem_u32(s.ring);
+        const size_t row_bytes = (size_t)K * sizeof(T);
         const int jv = split_index<V>(lane);
         const int jr = jv / (M * H2), jm = (jv / H2) % M;
         constexpr int NB = V == 16 ? 4 : (V == 8 ? 3 : (V == 4 ? 2 : (V == 2 ? 1 : 0)));
@@ -595,52 +610,58 @@ struct Consumer {
             const unsigned round = seq / NSLOT;
             ++seq;
             if (!mbar_wait(&s.full[slot], round & 1, P)) { failed = true; return; }
-            const uint32_t tile = ring_a + (uint32_t)slot * TILE;
+            // the tile's address passes through an opaque step after the wait, so
+            // no read of it can be scheduled before the data has landed
+            const unsigned char* tile = launder(s.ring[slot]);
             const int ng = (r + RG - 1) / RG;
             for (int q = (warp - (t * gpt) % NCW + NCW) % NCW; q < ng; q += NCW) {
                 const int i0 = q * RG;
                 const int nr = min(RG, r - i0);
-                uint32_t wrow[H2][RG];
+                const T* wrow[H2][RG];
 #pragma unroll
                 for (int h = 0; h < H2; ++h)
 #pragma unroll
                     for (int rr = 0; rr < RG; ++rr)
-                        wrow[h][rr] = tile + (uint32_t)(h * r + i0 + min(rr, nr - 1)) * row_bytes;
-                float acc[2][H2][RG][M];
+                        wrow[h][rr] = reinterpret_cast<const T*>(tile + (size_t)(h * r + i0 + min(rr, nr - 1)) * row_bytes);
+                // U accumulator sets (fewer for wide groups: 9 warps leave 168
+                // registers a thread): blocks of 128 elements, lane l on 4 l .. 4 l + 3
+                constexpr int U = H2 * RG * M <= 4 ? 4 : (H2 * RG * M <= 8 ? 2 : 1);
+                float acc[U][H2][RG][M];
 #pragma unroll
-                for (int a = 0; a < 2; ++a)
+                for (int a = 0; a < U; ++a)
 #pragma unroll
                     for (int h = 0; h < H2; ++h)
 #pragma unroll
                         for (int rr = 0; rr < RG; ++rr)
 #pragma unroll
                             for (int m = 0; m < M; ++m) acc[a][h][rr][m] = 0.f;
-                for (int kb = 0; kb < K; kb += 256) {
+                auto block = [&](int k, float (&A)[H2][RG][M]) {
+                    float4 xv[M];
 #pragma unroll
-                    for (int a = 0; a < 2; ++a) {
-                        const int k = kb + a * 128 + lane * 4;
-                        if (k < K) {
-                            float4 xv[M];
+                    for (int m = 0; m < M; ++m) xv[m] = *reinterpret_cast<const float4*>(xs + m * K + k);
 #pragma unroll
-                            for (int m = 0; m < M; ++m) lds4(xs_a + (uint32_t)(m * K + k) * 4u, xv[m]);
+                    for (int h = 0; h < H2; ++h)
 #pragma unroll
-                            for (int h = 0; h < H2; ++h)
+                        for (int rr = 0; rr < RG; ++rr) {
+                            float wv[4];
+                            load4(wrow[h][rr] + k, wv);
 #pragma unroll
-                                for (int rr = 0; rr < RG; ++rr) {
-                                    float wv[4];
-                                    lds4(wrow[h][rr] + (uint32_t)k * sizeof(T), wv, T());
-#pragma unroll
-                                    for (int m = 0; m < M; ++m) {
-                                        float& c = acc[a][h][rr][m];
-                                        c = fmaf(wv[0], xv[m].x, c);
-                                        c = fmaf(wv[1], xv[m].y, c);
-                                        c = fmaf(wv[2], xv[m].z, c);
-                                        c = fmaf(wv[3], xv[m].w, c);
-                                    }
-                                }
+                            for (int m = 0; m < M; ++m) {
+                                float& c = A[h][rr][m];
+                                c = fmaf(wv[0], xv[m].x, c);
+                                c = fmaf(wv[1], xv[m].y, c);
+                                c = fmaf(wv[2], xv[m].z, c);
+                                c = fmaf(wv[3], xv[m].w, c);
+                            }
                         }
-                    }
+                };
+                int kb = 0;
+                for (; kb + 128 * U <= K; kb += 128 * U) {
+#pragma unroll
+                    for (int a = 0; a < U; ++a) block(kb + 128 * a + lane * 4, acc[a]);
                 }
+                for (; kb < K; kb += 128)
+                    if (kb + lane * 4 < K) block(kb + lane * 4, acc[0]);
                 // value index (rr * M + m) * H2 + h
                 float v[V];
 #pragma unroll
@@ -648,7 +669,12 @@ struct Consumer {
 #pragma unroll
                     for (int rr = 0; rr < RG; ++rr)
 #pragma unroll
-                        for (int m = 0; m < M; ++m) v[(rr * M + m) * H2 + h] = acc[0][h][rr][m] + acc[1][h][rr][m];
+                        for (int m = 0; m < M; ++m) {
+                            float sacc = acc[0][h][rr][m];
+#pragma unroll
+                            for (int a = 1; a < U; ++a) sacc += acc[a][h][rr][m];
+                            v[(rr * M + m) * H2 + h] = sacc;
+                        }
                 const float sum = warp_sum_split<V>(v, lane);
                 // gated: the up sum of the same output sits in the next value index
                 const float up = GATED ? __shfl_down_sync(0xffffffffu, sum, 1 << (5 - NB)) : 0.f;
@@ -738,17 +764,26 @@ struct Consumer {
                     src = P.qkv + (size_t)m * nqkv + (size_t)(nq + nkv + g) * HD;
                     dst = sv + m * HD; rope = false;
                 }
-                float e[4] = {0.f, 0.f, 0.f, 0.f};
+                // norm weights and rotation first: they do not depend on the wait
+                float wnv[4] = {1.f, 1.f, 1.f, 1.f};
+                float2 c0 = make_float2(1.f, 0.f), c1 = make_float2(1.f, 0.f);
+                if (rope) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) good = good && ll_get(src + lane + 32 * i, eq, e[i], P);
+                    for (int i = 0; i < 4; ++i) wnv[i] = wn[lane + 32 * i];
+                    const int tp = p0 + m;
+                    c0 = P.rope[(size_t)tp * (HD / 2) + lane];
+                    c1 = P.rope[(size_t)tp * (HD / 2) + lane + 32];
+                }
+                Word wq[4];
+                good = ll_poll<4>(wq, src, lane, 32, HD, eq, P) && good;
+                float e[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) e[i] = val_of(wq[i]);
                 if (rope) {
                     const float ss = warp_sum(e[0] * e[0] + e[1] * e[1] + e[2] * e[2] + e[3] * e[3]);
                     const float r = 1.0f / sqrtf(ss / (float)HD + P.eps);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) e[i] = e[i] * r * wn[lane + 32 * i];
-                    const int tp = p0 + m;
-                    const float2 c0 = P.rope[(size_t)tp * (HD / 2) + lane];
-                    const float2 c1 = P.rope[(size_t)tp * (HD / 2) + lane + 32];
+                    for (int i = 0; i < 4; ++i) e[i] = e[i] * r * wnv[i];
                     float a = e[0], b = e[2];
                     e[0] = a * c0.x - b * c0.y; e[2] = b * c0.x + a * c0.y;
                     a = e[1]; b = e[3];
@@ -914,7 +949,10 @@ struct Consumer {
     __device__ void draw_cp(int sidx) {
         next_phase();
         if (!ok) return;
-        SampSmem& sm = samp_ptr<T>(s, P.xin_bytes);
+        // the draw's scratch overlays the input buffers: every warp must be done
+        // with the head's rows first
+        consumer_sync();
+        SampSmem& sm = samp_ptr<T>(s);
         if (!settle(ll_fetch(P.cpl, sm.l, P.cpV, ep[BCPL], nullptr, P))) return;
         const q3tts_sampling p = P.P[0];
         if (blockIdx.x == 0 && P.cap_c && P.cap_slot[0] >= 0 && frame < P.cap_T) {
@@ -947,7 +985,8 @@ struct Consumer {
     __device__ void draw_talker() {
         next_phase();
         if (!ok || blockIdx.x != 0) return;
-        SampSmem& sm = samp_ptr<T>(s, P.xin_bytes);
+        consumer_sync();   // the scratch overlays the input buffers (see draw_cp)
+        SampSmem& sm = samp_ptr<T>(s);
         if (!settle(ll_fetch(P.logits, sm.l, P.V, ep[BLOG], nullptr, P))) return;
         RowState& rs = P.rows[0];
         const q3tts_sampling p = P.P[0];
@@ -1094,7 +1133,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) frame_kernel(const FrameParams* _
 // ------------------------------------------------------------------ host side
 template <typename T>
 static size_t smem_for(int xin_bytes) {
-    return align128(sizeof(FSmem<T>)) + 2 * align128((size_t)xin_bytes) + sizeof(SampSmem);
+    return align128(sizeof(FSmem<T>)) + std::max(2 * align128((size_t)xin_bytes), sizeof(SampSmem));
 }
 
 size_t frame_attn_scratch_bytes() {
