@@ -7,13 +7,21 @@
 // tokens are its N dimension (NT tokens per tile), so D[n][m] = W_tile . X^T
 // lives in tensor memory as 128 lanes (weight rows) x NT fp32 columns.
 //   - TMA (cp.async.bulk.tensor, 128-byte swizzle) stages 64-wide K slices of
-//     both operands into a 4-deep shared-memory ring (mbarrier completion);
+//     both operands into a shared-memory ring as deep as ~192 KB allows
+//     (mbarrier completion);
 //   - one thread issues tcgen05.mma (kind::f16, M=128, N=NT, K=16 per
 //     instruction; W x hi, then W x lo into the same accumulator) and commits
 //     each stage back to the producer;
 //   - after the last stage, the four warps read their 32 TMEM lanes with
 //     tcgen05.ld and apply the epilogue (store / residual add / bias, or
 //     SiLU(g)*u for the stacked gate/up weights, which uses two accumulators).
+//   - when the output tiles alone cannot fill the GPU, K is split over the
+//     CTAs of a thread-block cluster (one output tile per cluster).  Once every
+//     CTA of the cluster has drained its operand ring (cluster barrier), each
+//     pushes its fp32 accumulator, column share by column share, into the ring
+//     of the CTA that owns those columns (distributed shared memory, vector
+//     stores); after a second barrier CTA z sums the z-th share over the splits
+//     in split order and applies the epilogue.
 // Every mbarrier wait is bounded; an expired wait sets the timeout error bit,
 // the CTA skips its remaining work, frees its TMEM and returns.
 #include <cuda.h>
@@ -30,8 +38,14 @@ namespace {
 
 constexpr int BM = 128;        // weight rows per tile (MMA M)
 constexpr int BK = 64;         // K per stage (one 128-byte swizzle row of bf16)
-constexpr int STAGES = 4;
+constexpr int RING_BYTES = 192 * 1024;
+// ring depth for a tile shape: stages of (BM (x2 gated) + 2 NT) x BK bf16
+constexpr int stages_for(int nt, bool gated) {
+    const int st = RING_BYTES / ((BM * (gated ? 2 : 1) + 2 * nt) * BK * 2);
+    return st > 8 ? 8 : st;
+}
 constexpr long long TC_WAIT_LIMIT = 2000000000LL;
+constexpr int kSMs = 148;      // CTAs for about one wave (one 192 KB CTA per SM)
 
 __device__ __forceinline__ uint32_t s_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -92,6 +106,20 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(s_u32(bar))
                  : "memory");
 }
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// address of shared location a in cluster CTA `rank`
+__device__ __forceinline__ uint32_t map_peer(uint32_t a, int rank) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    return ra;
+}
+// four fp32 to a peer's shared memory (address from map_peer)
+__device__ __forceinline__ void st_dsmem4(uint32_t ra, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(ra), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -107,7 +135,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <int NT, bool GATED>
+template <int NT, bool GATED, int STAGES>
 struct TcSmem {
     alignas(1024) bf16 a[STAGES][BM * BK];
     alignas(1024) bf16 a2[GATED ? STAGES : 1][GATED ? BM * BK : 8];
@@ -125,22 +153,28 @@ constexpr uint32_t tmem_cols(bool gated) {
     return need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
 }
 
-template <int NT, bool GATED>
+template <int NT, bool GATED, int STAGES>
 __global__ void __launch_bounds__(128, 1) umma_linear_kernel(const __grid_constant__ CUtensorMap tmW,
                                                              const __grid_constant__ CUtensorMap tmX,
                                                              const __grid_constant__ CUtensorMap tmX2, int N, int K,
                                                              int M, float* __restrict__ Y, int ldy,
                                                              const float* __restrict__ bias, int accumulate, int F,
-                                                             float* __restrict__ Gout, int ldg, int* err) {
+                                                             float* __restrict__ Gout, int ldg, int kbs, int* err) {
     extern __shared__ __align__(1024) unsigned char raw[];
     // 1024-byte alignment of the swizzled tiles
     unsigned char* base = (unsigned char*)(((uintptr_t)raw + 1023) & ~(uintptr_t)1023);
-    TcSmem<NT, GATED>& s = *reinterpret_cast<TcSmem<NT, GATED>*>(base);
+    TcSmem<NT, GATED, STAGES>& s = *reinterpret_cast<TcSmem<NT, GATED, STAGES>*>(base);
     constexpr uint32_t COLS = tmem_cols<NT>(GATED);
     constexpr uint32_t IDESC = make_idesc(BM, NT);
+    constexpr int H2 = GATED ? 2 : 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * BM, m0 = blockIdx.y * NT;
-    const int nk = (K + BK - 1) / BK;
+    // grid (ks, weight-row tiles, token tiles); cluster (ks, 1, 1): rank = K split
+    const int n0 = blockIdx.y * BM, m0 = blockIdx.z * NT;
+    const int ks = gridDim.x, kz = blockIdx.x;
+    // this CTA's K blocks [kb0, kb0 + nk)
+    const int nk_all = (K + BK - 1) / BK;
+    const int kb0 = kz * kbs;
+    const int nk = min(kbs, nk_all - kb0);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) { mb_init(&s.full[i], 1); mb_init(&s.empty[i], 1); }
@@ -166,10 +200,11 @@ __global__ void __launch_bounds__(128, 1) umma_linear_kernel(const __grid_consta
             const unsigned round = kb / STAGES;
             if (round > 0 && !mb_wait(&s.empty[st], (round - 1) & 1, err)) { ok = false; break; }
             mb_expect_tx(&s.full[st], bytes);
-            tma_2d(s.a[st], &tmW, kb * BK, n0, &s.full[st]);
-            if (GATED) tma_2d(s.a2[st], &tmW, kb * BK, F + n0, &s.full[st]);
-            tma_2d(s.b[st], &tmX, kb * BK, m0, &s.full[st]);
-            tma_2d(s.b2[st], &tmX2, kb * BK, m0, &s.full[st]);
+            const int kx = (kb0 + kb) * BK;
+            tma_2d(s.a[st], &tmW, kx, n0, &s.full[st]);
+            if (GATED) tma_2d(s.a2[st], &tmW, kx, F + n0, &s.full[st]);
+            tma_2d(s.b[st], &tmX, kx, m0, &s.full[st]);
+            tma_2d(s.b2[st], &tmX2, kx, m0, &s.full[st]);
         }
     } else if (warp == 1 && lane == 0) {
         // MMA issuer
@@ -199,34 +234,86 @@ __global__ void __launch_bounds__(128, 1) umma_linear_kernel(const __grid_consta
     // epilogue: warp w owns TMEM lanes 32w..32w+31 (weight rows n0+32w..)
     const bool have = __all_sync(0xffffffffu, mb_wait(&s.done, 0, err));
     tc_fence_after();
-    if (have) {
-        const int n = n0 + warp * 32 + lane;
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-#pragma unroll 1
-        for (int c0 = 0; c0 < NT; c0 += 16) {
-            float v[16];
-            tmem_ld16(lane_base + c0, v);
-            if (GATED) {
-                float u[16];
-                tmem_ld16(lane_base + NT + c0, u);
-                if (n < F) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int m = m0 + c0 + j;
-                        if (m < M) Gout[(size_t)m * ldg + n] = v[j] / (1.0f + expf(-v[j])) * u[j];
-                    }
-                }
-            } else if (n < N) {
-                const float bn = bias ? bias[n] : 0.f;
+    const int row = warp * 32 + lane;
+    const int n = n0 + row;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    // final values of this thread's row for tokens m0 + c0 .. c0 + 15
+    auto finish = [&](int c0, const float (&v)[16], const float (&u)[16]) {
+        if (GATED) {
+            if (n < F) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int m = m0 + c0 + j;
-                    if (m < M) {
-                        float* y = Y + (size_t)m * ldy + n;
-                        *y = accumulate ? *y + v[j] + bn : v[j] + bn;
+                    if (m < M) Gout[(size_t)m * ldg + n] = v[j] / (1.0f + expf(-v[j])) * u[j];
+                }
+            }
+        } else if (n < N) {
+            const float bn = bias ? bias[n] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int m = m0 + c0 + j;
+                if (m < M) {
+                    float* y = Y + (size_t)m * ldy + n;
+                    *y = accumulate ? *y + v[j] + bn : v[j] + bn;
+                }
+            }
+        }
+    };
+    if (ks == 1) {
+        if (have) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < NT; c0 += 16) {
+                float v[16], u[16];
+                tmem_ld16(lane_base + c0, v);
+                if (GATED) tmem_ld16(lane_base + NT + c0, u);
+                finish(c0, v, u);
+            }
+        }
+    } else {
+        // owner z of token columns [z per, z per + per) keeps an inbox in its
+        // drained ring: [split][H2][row][per + 4] fp32 (padded rows)
+        const int per = (NT / 16 + ks - 1) / ks * 16;
+        const int rs = per + 4;
+        const uint32_t inbox = s_u32(s.a);
+        cluster_sync();   // every ring of the cluster is drained
+        if (have) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < NT; c0 += 16) {
+                const int o = c0 / per, cl = c0 - o * per;
+                float v[16], u[16];
+                tmem_ld16(lane_base + c0, v);
+                if (GATED) tmem_ld16(lane_base + NT + c0, u);
+#pragma unroll
+                for (int h = 0; h < H2; ++h) {
+                    const float* src = h ? u : v;
+                    const uint32_t dst =
+                        map_peer(inbox + (uint32_t)((((kz * H2 + h) * BM + row) * rs + cl) * 4), o);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        st_dsmem4(dst + 16u * q, src[4 * q], src[4 * q + 1], src[4 * q + 2], src[4 * q + 3]);
+                }
+            }
+        }
+        cluster_sync();   // every push has landed
+        const float* box = reinterpret_cast<const float*>(s.a);
+#pragma unroll 1
+        for (int cl = 0; cl < per && kz * per + cl < NT; cl += 16) {
+            float v[16], u[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) { v[j] = 0.f; u[j] = 0.f; }
+            for (int z = 0; z < ks; ++z) {
+#pragma unroll
+                for (int h = 0; h < H2; ++h) {
+                    const float4* q = reinterpret_cast<const float4*>(box + ((z * H2 + h) * BM + row) * rs + cl);
+                    float* d = h ? u : v;
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const float4 f = q[k4];
+                        d[4 * k4] += f.x; d[4 * k4 + 1] += f.y; d[4 * k4 + 2] += f.z; d[4 * k4 + 3] += f.w;
                     }
                 }
             }
+            finish(kz * per + cl, v, u);
         }
     }
     tc_fence_before();
@@ -260,72 +347,171 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int ld, int 
 }
 
 // x -> (hi, lo): hi = bf16(x), lo = bf16(x - hi); [M][K] each, row stride K.
+// Grid (ceil(K / 1024), M): each thread converts 4 consecutive elements
+// (K and ldx are multiples of 8, so the float4 reads are aligned).
 __global__ void split_kernel(const float* __restrict__ X, int ldx, int M, int K, bf16* __restrict__ hi,
                              bf16* __restrict__ lo) {
-    const long total = (long)M * K;
-    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
-        const int m = (int)(i / K), k = (int)(i % K);
-        const float x = X[(size_t)m * ldx + k];
-        const bf16 h = __float2bfloat16_rn(x);
-        hi[i] = h;
-        lo[i] = __float2bfloat16_rn(x - __bfloat162float(h));
+    const int m = blockIdx.y;
+    const int k = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (m >= M || k >= K) return;
+    const float4 x = *reinterpret_cast<const float4*>(X + (size_t)m * ldx + k);
+    const float xs[4] = {x.x, x.y, x.z, x.w};
+    __align__(8) bf16 h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        h[i] = __float2bfloat16_rn(xs[i]);
+        l[i] = __float2bfloat16_rn(xs[i] - __bfloat162float(h[i]));
     }
+    *reinterpret_cast<uint2*>(hi + (size_t)m * K + k) = *reinterpret_cast<const uint2*>(h);
+    *reinterpret_cast<uint2*>(lo + (size_t)m * K + k) = *reinterpret_cast<const uint2*>(l);
+}
+
+// Clusters of `ks` CTAs of this kernel that can be resident at once (cached).
+template <int NT, bool GATED>
+int cluster_capacity(int ks) {
+    constexpr int STAGES = stages_for(NT, GATED);
+    static int cap[9] = {0};
+    if (ks < 1 || ks > 8) return 0;
+    if (cap[ks] == 0) {
+        const size_t smem = sizeof(TcSmem<NT, GATED, STAGES>) + 1024;
+        if (cudaFuncSetAttribute(umma_linear_kernel<NT, GATED, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(ks, 1, 1);
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = ks;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, (void*)umma_linear_kernel<NT, GATED, STAGES>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = ks == 1 ? kSMs : 0;
+        }
+        cap[ks] = n > 0 ? n : -1;
+    }
+    return cap[ks] > 0 ? cap[ks] : 0;
+}
+
+// Resident CTAs of this kernel at once (1 CTA per SM: ~192 KB of shared memory).
+template <int NT, bool GATED>
+int resident_ctas(int ks) {
+    return ks == 1 ? kSMs : cluster_capacity<NT, GATED>(ks) * ks;
+}
+
+// Cost of an NT-wide tile shape split ks ways: each CTA streams its operand
+// bytes at a rate limited by its in-flight ring, so the time goes with the
+// waves times the K blocks (stage bytes) of one CTA.  Returns the best ks and
+// its cost.
+template <int NT, bool GATED>
+double best_split(int nrows, int M, int K, int* ks_out) {
+    constexpr int H2 = GATED ? 2 : 1;
+    constexpr size_t stage = (size_t)(BM * H2 + 2 * NT) * BK * sizeof(bf16);
+    constexpr size_t ring = (size_t)stages_for(NT, GATED) * stage;
+    const int tiles = ((nrows + BM - 1) / BM) * ((M + NT - 1) / NT);
+    const int nk = (K + BK - 1) / BK;
+    double best = 1e300;
+    *ks_out = 1;
+    for (int ks : {1, 2, 4, 8}) {
+        if (ks > 1 && ks > nk / 2) continue;
+        const int per = (NT / 16 + ks - 1) / ks * 16;
+        if (ks > 1 && (size_t)ks * H2 * BM * (per + 4) * sizeof(float) > ring) continue;   // inbox must fit
+        const int res = resident_ctas<NT, GATED>(ks);
+        if (res <= 0) continue;
+        const int kbs = (nk + ks - 1) / ks;
+        const int waves = (tiles * ks + res - 1) / res;
+        // a split adds its reduction: about one more stage of traffic
+        const double cost = (double)waves * (kbs + (ks > 1 ? 1 : 0)) * (double)stage;
+        if (cost < best) { best = cost; *ks_out = ks; }
+    }
+    return best;
 }
 
 template <int NT, bool GATED>
 cudaError_t launch_tc(const void* W, int N, int K, const float* X, int ldx, int M, float* Y, int ldy,
-                      const float* bias, int accumulate, int F, float* G, int ldg, const TcScratch& tc, int* err,
-                      cudaStream_t st) {
+                      const float* bias, int accumulate, int F, float* G, int ldg, int ks, const TcScratch& tc,
+                      int* err, cudaStream_t st) {
+    constexpr int STAGES = stages_for(NT, GATED);
     bf16* hi = (bf16*)tc.base;
     bf16* lo = hi + (size_t)M * K;
-    const long total = (long)M * K;
-    split_kernel<<<(int)std::min<long>((total + 255) / 256, 2048), 256, 0, st>>>(X, ldx, M, K, hi, lo);
+    split_kernel<<<dim3((K + 1023) / 1024, M), 256, 0, st>>>(X, ldx, M, K, hi, lo);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap mw, mx, mx2;
     const int wrows = GATED ? 2 * F : N;
     if (!make_map(&mw, W, wrows, K, K, BM) || !make_map(&mx, hi, M, K, K, NT) || !make_map(&mx2, lo, M, K, K, NT))
         return cudaErrorInvalidValue;
-    const size_t smem = sizeof(TcSmem<NT, GATED>) + 1024;
+    const size_t smem = sizeof(TcSmem<NT, GATED, STAGES>) + 1024;
     static bool attr_set = false;
     if (!attr_set) {
-        e = cudaFuncSetAttribute(umma_linear_kernel<NT, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(umma_linear_kernel<NT, GATED, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    dim3 grid((N + BM - 1) / BM, (M + NT - 1) / NT);
-    umma_linear_kernel<NT, GATED><<<grid, 128, smem, st>>>(mw, mx, mx2, N, K, M, Y, ldy, bias, accumulate, F, G, ldg,
-                                                            err);
-    return cudaGetLastError();
+    const int nrows = GATED ? F : N;
+    const int nk = (K + BK - 1) / BK;
+    const int kbs = (nk + ks - 1) / ks;
+    ks = (nk + kbs - 1) / kbs;   // every split gets at least one K block
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ks, (nrows + BM - 1) / BM, (M + NT - 1) / NT);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, umma_linear_kernel<NT, GATED, STAGES>, mw, mx, mx2, N, K, M, Y, ldy, bias,
+                              accumulate, F, G, ldg, kbs, err);
+}
+
+// Tile width and K split of least cost among the widths the tokens allow.
+template <bool GATED>
+void pick_shape(int nrows, int M, int K, int* nt, int* ks) {
+    double best = 1e300;
+    for (int w : {128, 64, 32}) {
+        if (w > 32 && w > ((M + 31) / 32) * 32) continue;
+        int k = 1;
+        const double c = w == 128 ? best_split<128, GATED>(nrows, M, K, &k)
+                       : w == 64 ? best_split<64, GATED>(nrows, M, K, &k) : best_split<32, GATED>(nrows, M, K, &k);
+        if (c < best) { best = c; *nt = w; *ks = k; }
+    }
 }
 
 }  // namespace
 
 bool tc_available() { return encode_fn() != nullptr; }
 
-// Tokens per tile: the largest of 32/64/128 that still gives >= ~150 tiles.
-static int pick_nt(int N, int M) {
-    const int nt_rows = (N + BM - 1) / BM;
-    for (int nt : {128, 64})
-        if (nt <= ((M + 31) / 32) * 32 && nt_rows * ((M + nt - 1) / nt) >= 150) return nt;
-    return 32;
-}
-
 cudaError_t launch_linear_tc(const void* W, int N, int K, const float* X, int ldx, int M, float* Y, int ldy,
                              const float* bias, int accumulate, const TcScratch& tc, int* err, cudaStream_t st) {
-    switch (pick_nt(N, M)) {
-        case 128: return launch_tc<128, false>(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, tc, err, st);
-        case 64: return launch_tc<64, false>(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, tc, err, st);
-        default: return launch_tc<32, false>(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, tc, err, st);
+    int nt = 32, ks = 1;
+    pick_shape<false>(N, M, K, &nt, &ks);
+    switch (nt) {
+        case 128: return launch_tc<128, false>(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, ks, tc, err, st);
+        case 64: return launch_tc<64, false>(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, ks, tc, err, st);
+        default: return launch_tc<32, false>(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, ks, tc, err, st);
     }
 }
 
 cudaError_t launch_linear_gated_tc(const void* W, int F, int K, const float* X, int ldx, int M, float* out, int ldo,
                                    const TcScratch& tc, int* err, cudaStream_t st) {
-    // gate + up accumulators and two input parts: keep the tile at <= 64 tokens
-    switch (std::min(pick_nt(F, M), 64)) {
-        case 64: return launch_tc<64, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, tc, err, st);
-        default: return launch_tc<32, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, tc, err, st);
+    int nt = 32, ks = 1;
+    pick_shape<true>(F, M, K, &nt, &ks);
+    switch (nt) {
+        case 128: return launch_tc<128, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, ks, tc, err, st);
+        case 64: return launch_tc<64, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, ks, tc, err, st);
+        default: return launch_tc<32, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, ks, tc, err, st);
     }
 }
 
