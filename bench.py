@@ -46,6 +46,34 @@ def parse():
 
 
 # ---------------------------------------------------------------- byte model
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
+
+
+def measured_traffic(workload: int):
+    """DRAM bytes per launch of the step's dominant kernel from the committed ncu
+    capture, or None when there is none for this workload or the kernel's
+    sources changed since it was taken."""
+    import hashlib
+    try:
+        lines = open(TRAFFIC_FILE).read().splitlines()
+    except OSError:
+        return None, None
+    for ln in lines:
+        if ln.startswith("#") or not ln.strip():
+            continue
+        kv = dict(tok.split("=", 1) for tok in ln.split())
+        if int(kv.get("workload", -1)) != workload:
+            continue
+        h = hashlib.sha256()
+        for f in kv["sources"].split(","):
+            with open(os.path.join(ROOT, "speech_lm_decode_gb300", "csrc", f), "rb") as fh:
+                h.update(fh.read())
+        if h.hexdigest()[:16] != kv["sha"]:
+            return None, kv["kernel"]
+        return float(kv["bytes"]), kv["kernel"]
+    return None, None
+
+
 def step_bytes(wl, live_pos):
     """Algorithmic bytes of one step: every weight streamed once per use plus
     the KV cache read (and written) by attention.  live_pos: talker position of
@@ -304,15 +332,19 @@ def main():
     value = res["frames"] / sec
     bytes_total = res["wbytes"] + res["kvbytes"]
     achieved = bytes_total / (res["local_ms"] / 1000.0) / 1e9
+    # at batch 1 one launch of the frame kernel is the whole step
+    traffic, tk = measured_traffic(args.workload) if wl.batch == 1 else (None, None)
+    kernel_name = ("frame_kernel (one launch = the whole step; traffic from ncu, bytes per launch)"
+                   if wl.batch == 1 else "frame step (all kernels of one talker step)")
     line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": res["steps"],
             "warmup": args.warmup, "ms_per_step": res["ms"] / max(res["steps"], 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == synth.BF16 else "f32",
             "data": "synthetic (seeded random-init weights, N(0,1) prompts)", "config": config,
             "us_per_frame": 1e6 * sec / max(res["frames"], 1),
-            "roofline": {"bound": "hbm", "kernel": "frame step (all kernels of one talker step)",
+            "roofline": {"bound": "hbm", "kernel": kernel_name,
                          "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / pk["hbm_gbs"], "peak_kind": pk_kind,
-                         "traffic": None, "algorithmic_bytes_per_step": bytes_total / max(res["steps"], 1)},
+                         "traffic": traffic, "algorithmic_bytes_per_step": bytes_total / max(res["steps"], 1)},
             "gpu_launches": res["kernels_per_step"] * res["steps"],
             "clocks": res["clocks"]}
     if "e2e" in res:
