@@ -68,6 +68,7 @@ struct FrameParams {
 
 constexpr int FRAME_CTL_WORDS = 64;
 constexpr int FRAME_MAX_ROWS = 128;   // residual rows one CTA updates in one phase
+constexpr int FRAME_MAX_PART = 1024;  // partial sums of one phase on one CTA (rows x 2 x 2 x 8 splits)
 constexpr int FRAME_TILE = 24 * 1024; // bytes of one weight ring slot
 constexpr int FRAME_SLOTS = 6;        // ring slots
 constexpr int FRAME_MAX_PHASES = 1024;  // phases of one launch (epoch = selection * 1024 + phase)
@@ -75,13 +76,15 @@ constexpr int FRAME_MAX_NORM = 2048;    // widest RMSNorm input (talker and pred
 
 // Shared memory the frame kernel needs with an attention scratch region of
 // xin_bytes (at least frame_attn_scratch_bytes()); 0 if it does not fit one SM.
-size_t frame_smem_bytes(int dtype, int xin_bytes);
+// tc_rows: bf16 GEMV rows on the tensor cores (else FMA rows)
+size_t frame_smem_bytes(int dtype, int xin_bytes, bool tc_rows);
 size_t frame_attn_scratch_bytes();
 // One-time attribute setup; returns cudaSuccess when the kernel can run.
-cudaError_t frame_setup(int dtype, size_t smem);
+cudaError_t frame_setup(int dtype, size_t smem, bool tc_rows);
 // CTAs of the frame kernel that fit one SM with this shared memory.
-cudaError_t frame_occupancy(int dtype, size_t smem, int* blocks);
+cudaError_t frame_occupancy(int dtype, size_t smem, bool tc_rows, int* blocks);
 // Launch one talker step (cooperative, `grid` CTAs).
-cudaError_t launch_frame(int dtype, const FrameParams* params_dev, int grid, size_t smem, cudaStream_t st);
+cudaError_t launch_frame(int dtype, bool tc_rows, const FrameParams* params_dev, int grid, size_t smem,
+                         cudaStream_t st);
 
 }  // namespace q3

@@ -48,6 +48,7 @@
 #include "frame_params.h"
 
 #include <algorithm>
+#include <type_traits>
 
 namespace q3 {
 
@@ -57,6 +58,9 @@ constexpr int TILE = FRAME_TILE;             // bytes per ring slot
 constexpr int NSLOT = FRAME_SLOTS;
 constexpr long long WAIT_LIMIT = 4000000000LL;  // cycles (~2 s) before a wait gives up
 constexpr int NORM_MAX = FRAME_MAX_NORM;     // widest vector an RMSNorm prologue normalizes
+constexpr int ROW_PAD = 32;                  // bytes after each bf16 weight row in the ring
+constexpr int KSMAX = 8;                     // K splits of one GEMV phase (tensor-core rows)
+constexpr int WT = 3;                        // ring tiles per window of tensor-core rows
 
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -192,13 +196,15 @@ __device__ bool ll_fetch(const Word* src, float* dst, int n, unsigned ep, float*
 }
 
 // ------------------------------------------------------------------ shared memory
-template <typename T>
+template <typename T, bool TCR>
 struct FSmem {
     unsigned char ring[NSLOT][TILE];
     uint64_t full[NSLOT];
     uint64_t empty[NSLOT];
     float resid[2][2][FRAME_MAX_ROWS];  // residual entries a GEMV phase updates [phase parity][vector][row]
     float pss[2][NCW][2];               // per-warp sums of squares of the RMSNorm inputs [phase parity]
+    // tensor-core rows: per-split partial sums [row][gate/up][vector][split]
+    float part[TCR ? FRAME_MAX_PART : 1];
     int codes[MAX_GROUPS];              // this frame's codes as drawn so far
     int flag;
     // then one region for: two input-vector buffers (fp32 [M][K], one per GEMV
@@ -207,14 +213,14 @@ struct FSmem {
 };
 
 __host__ __device__ constexpr size_t align128(size_t v) { return (v + 127) & ~(size_t)127; }
-template <typename T>
-__device__ __forceinline__ float* xin_ptr(FSmem<T>& s, int buf, int xin_bytes) {
-    return reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(&s) + align128(sizeof(FSmem<T>)) +
+template <class S>
+__device__ __forceinline__ float* xin_ptr(S& s, int buf, int xin_bytes) {
+    return reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(&s) + align128(sizeof(S)) +
                                     (size_t)buf * align128((size_t)xin_bytes));
 }
-template <typename T>
-__device__ __forceinline__ SampSmem& samp_ptr(FSmem<T>& s) {
-    return *reinterpret_cast<SampSmem*>(reinterpret_cast<unsigned char*>(&s) + align128(sizeof(FSmem<T>)));
+template <class S>
+__device__ __forceinline__ SampSmem& samp_ptr(S& s) {
+    return *reinterpret_cast<SampSmem*>(reinterpret_cast<unsigned char*>(&s) + align128(sizeof(S)));
 }
 
 // ------------------------------------------------------------------ the frame schedule
@@ -253,9 +259,16 @@ __device__ __forceinline__ void split_rows(int N, int& n0, int& n1) {
     n1 = (int)(((unsigned)N * (blockIdx.x + 1)) / gridDim.x);
 }
 
-template <typename T>
+// Rows of a ring tile: for the tensor-core rows (TCR, bf16) rows are stored
+// padded (row stride 2K + ROW_PAD bytes) so that the fragment loads of 8 rows
+// hit distinct banks; otherwise rows are contiguous.
+template <typename T, bool TCR>
+__device__ __forceinline__ int row_stride(int K) {
+    return TCR ? K * 2 + ROW_PAD : K * (int)sizeof(T);
+}
+template <typename T, bool TCR>
 __device__ __forceinline__ int rows_per_tile(const Gemv& g) {
-    const int unit = g.K * (int)sizeof(T) * (g.gated ? 2 : 1);
+    const int unit = row_stride<T, TCR>(g.K) * (g.gated ? 2 : 1);
     return max(1, TILE / unit);
 }
 
@@ -272,9 +285,9 @@ __device__ __forceinline__ bool kv_prefetch_range(int p0, int S, int sp, int& j0
 }
 
 // ------------------------------------------------------------------ producer
-template <typename T>
+template <typename T, bool TCR>
 struct Producer {
-    FSmem<T>& s;
+    FSmem<T, TCR>& s;
     const FrameParams& P;
     unsigned seq = 0;
     bool ok = true;
@@ -292,7 +305,7 @@ struct Producer {
         if (!ok) return;
         int n0, n1;
         split_rows(g.N, n0, n1);
-        const int rt = rows_per_tile<T>(g);
+        const int rt = rows_per_tile<T, TCR>(g);
         const size_t row_bytes = (size_t)g.K * sizeof(T);
         for (int r0 = n0; r0 < n1; r0 += rt) {
             const int r = min(rt, n1 - r0);
@@ -300,11 +313,23 @@ struct Producer {
             if (!take_slot(slot)) return;
             const unsigned bytes = (unsigned)(r * row_bytes * (g.gated ? 2 : 1));
             mbar_expect_tx(&s.full[slot], bytes);
-            bulk_g2s(s.ring[slot], (const char*)g.W + (size_t)r0 * row_bytes, (unsigned)(r * row_bytes),
-                     &s.full[slot]);
-            if (g.gated)
-                bulk_g2s(s.ring[slot] + r * row_bytes, (const char*)g.W + (size_t)(g.N + r0) * row_bytes,
-                         (unsigned)(r * row_bytes), &s.full[slot]);
+            if (TCR) {
+                // one copy per row into the padded layout (gate rows, then up rows)
+                const size_t rs = (size_t)row_stride<T, TCR>(g.K);
+                for (int i = 0; i < r; ++i)
+                    bulk_g2s(s.ring[slot] + i * rs, (const char*)g.W + (size_t)(r0 + i) * row_bytes,
+                             (unsigned)row_bytes, &s.full[slot]);
+                if (g.gated)
+                    for (int i = 0; i < r; ++i)
+                        bulk_g2s(s.ring[slot] + (r + i) * rs, (const char*)g.W + (size_t)(g.N + r0 + i) * row_bytes,
+                                 (unsigned)row_bytes, &s.full[slot]);
+            } else {
+                bulk_g2s(s.ring[slot], (const char*)g.W + (size_t)r0 * row_bytes, (unsigned)(r * row_bytes),
+                         &s.full[slot]);
+                if (g.gated)
+                    bulk_g2s(s.ring[slot] + r * row_bytes, (const char*)g.W + (size_t)(g.N + r0) * row_bytes,
+                             (unsigned)(r * row_bytes), &s.full[slot]);
+            }
         }
     }
     // Talker attention: the cached K / V of positions before the new token do
@@ -352,6 +377,12 @@ __device__ __forceinline__ P* launder(P* p) {
     unsigned long long v = reinterpret_cast<unsigned long long>(p);
     asm volatile("mov.b64 %0, %0;" : "+l"(v)::"memory");
     return reinterpret_cast<P*>(v);
+}
+// D += A B for mma.m16n8k16 (bf16 in, fp32 accumulate); A rows 8..15 are zero
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
 }
 // 4 consecutive elements (index multiple of 4) as fp32
 __device__ __forceinline__ void load4(const bf16* p, float (&v)[4]) {
@@ -417,9 +448,9 @@ __device__ __forceinline__ int split_index(int lane) {
 }
 
 // ------------------------------------------------------------------ consumer
-template <typename T, int GQ>
+template <typename T, int GQ, bool TCR>
 struct Consumer {
-    FSmem<T>& s;
+    FSmem<T, TCR>& s;
     const FrameParams& P;
     unsigned seq = 0;        // ring slots consumed
     unsigned base = 0;       // epoch of this launch's phase 0
@@ -432,7 +463,7 @@ struct Consumer {
     bool failed = false;     // a wait of this thread failed (reported at the next settle)
 
     // input-vector buffer of the next GEMV phase (also the attention scratch)
-    __device__ float* xin_next() { return xin_ptr<T>(s, gph & 1, P.xin_bytes); }
+    __device__ float* xin_next() { return xin_ptr(s, gph & 1, P.xin_bytes); }
     __device__ unsigned next_phase() { return base + ph++; }
 
     // Every thread reports whether its waits succeeded (and any wait that failed
@@ -472,6 +503,121 @@ struct Consumer {
         return acc + tk_text[i];
     }
 
+    // The rows of a GEMV phase on the tensor cores (bf16 weights).  Each
+    // mma.m16n8k16 multiplies the input vectors (A: rows 0..M-1 of 16, bf16 high
+    // part, then low part into the same accumulator) with 8 weight rows (B)
+    // over 16 elements of K.  The K order inside a 16-element step is permuted
+    // so that a lane's A and B fragments are 4 consecutive elements (one 8-byte
+    // load): MMA k pairs (2q, 2q+1) and (2q+8, 2q+9) are elements 4q..4q+3.
+    // The phase's tiles are taken WT at a time (all resident); a window's rows
+    // form 8-row blocks (across tiles), and (block, K split) units are dealt to
+    // the warps; their partial sums meet in shared memory, and after the
+    // phase's second barrier one thread per output adds the splits in order.
+    template <int M, bool GATED>
+    __device__ void rows_tc(const Gemv& g, unsigned cur, int buf, const float (&rm)[2], int n0, int nrows) {
+        constexpr int H2 = GATED ? 2 : 1;
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const int K = g.K, nks = K >> 4;
+        const int rt = rows_per_tile<T, TCR>(g);
+        const size_t rs = (size_t)row_stride<T, TCR>(K);
+        const int ntiles = (nrows + rt - 1) / rt;
+        const int nbw = (min(WT * rt, nrows) + 7) >> 3;   // blocks of a full window
+        const int ks = max(1, min(KSMAX, NCW / nbw));
+        const int gq = lane >> 2, q = lane & 3;
+        const bool xrow = gq < M;
+        const unsigned char* xb = reinterpret_cast<const unsigned char*>(xin_ptr(s, buf, P.xin_bytes));
+        const unsigned char* xh = xb + (size_t)min(gq, M - 1) * K * 2 + q * 8;
+        const unsigned char* xl = xh + (size_t)M * K * 2;
+        float* part = s.part;
+        bool good = true;
+        for (int w0 = 0; w0 < ntiles; w0 += WT) {
+            const int wt = min(WT, ntiles - w0);
+            const unsigned seqw = seq;
+            for (int t = 0; t < wt; ++t) {
+                const unsigned sq = seqw + t;
+                good = good && mbar_wait(&s.full[sq % NSLOT], (sq / NSLOT) & 1, P);
+            }
+            seq += wt;
+            const int row_w0 = w0 * rt;
+            const int rw = min(wt * rt, nrows - row_w0);
+            const int nb = (rw + 7) >> 3;
+            for (int u = warp; good && u < nb * ks; u += NCW) {
+                const int b = u / ks, kq = u - b * ks;
+                const int k0 = nks * kq / ks, k1 = nks * (kq + 1) / ks;
+                const int j = min(b * 8 + gq, rw - 1);   // this lane's weight row in the window
+                const int t = j / rt, i = j - t * rt;
+                const int rtile = min(rt, nrows - row_w0 - t * rt);
+                const unsigned char* tb = s.ring[(seqw + t) % NSLOT];
+                const unsigned char* wa = tb + (size_t)i * rs + q * 8;
+                const unsigned char* ua = tb + (size_t)(rtile + i) * rs + q * 8;
+                float d[4][H2][4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int h = 0; h < H2; ++h)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) d[c][h][e] = 0.f;
+                for (int kk = k0; kk < k1; kk += 4) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int k = kk + c;
+                        if (k < k1) {
+                            const uint2 bw = *reinterpret_cast<const uint2*>(wa + (size_t)k * 32);
+                            uint2 ah = make_uint2(0u, 0u), al = make_uint2(0u, 0u);
+                            if (xrow) {
+                                ah = *reinterpret_cast<const uint2*>(xh + (size_t)k * 32);
+                                al = *reinterpret_cast<const uint2*>(xl + (size_t)k * 32);
+                            }
+                            mma_bf16(d[c][0], ah.x, ah.y, bw.x, bw.y);
+                            mma_bf16(d[c][0], al.x, al.y, bw.x, bw.y);
+                            if (GATED) {
+                                const uint2 bu = *reinterpret_cast<const uint2*>(ua + (size_t)k * 32);
+                                mma_bf16(d[c][H2 - 1], ah.x, ah.y, bu.x, bu.y);
+                                mma_bf16(d[c][H2 - 1], al.x, al.y, bu.x, bu.y);
+                            }
+                        }
+                    }
+                }
+                // lane 4m + q holds vector m's sums for rows 2q and 2q + 1 of the block
+                if (xrow) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int jr = b * 8 + 2 * q + e;
+                        if (jr < rw) {
+                            const int prow = row_w0 + jr;
+#pragma unroll
+                            for (int h = 0; h < H2; ++h)
+                                part[((prow * H2 + h) * M + gq) * KSMAX + kq] =
+                                    (d[0][h][e] + d[1][h][e]) + (d[2][h][e] + d[3][h][e]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                for (int t = 0; t < wt; ++t) mbar_arrive(&s.empty[(seqw + t) % NSLOT]);
+        }
+        if (!good) failed = true;
+        // every partial is in place (and a failed wait is known to every warp)
+        if (!settle(good)) return;
+        for (int o = threadIdx.x; o < nrows * M; o += 256) {
+            const int row = o / M, m = o - row * M, n = n0 + row;
+            float a = 0.f, up = 0.f;
+            for (int kq = 0; kq < ks; ++kq) {
+                a += part[((row * H2) * M + m) * KSMAX + kq];
+                if (GATED) up += part[((row * H2 + 1) * M + m) * KSMAX + kq];
+            }
+            const float r_m = m == 0 ? rm[0] : rm[1];
+            a *= r_m;
+            float out;
+            if (GATED) out = a / (1.0f + expf(-a)) * (up * r_m);
+            else if (g.epi == Epi::ADD) out = s.resid[buf][m][row] + a;
+            else if (g.epi == Epi::BIAS) out = a + g.bias[n];
+            else out = a;
+            ll_put(g.dst + (size_t)m * g.ld_dst + n, out, cur);
+        }
+    }
+
     // One GEMV phase.  Prologue: each thread fetches input elements i = tid,
     // tid + 256, ... (polled exchange words or an assembled token), forms
     // x (.) w for RMSNorm phases and stores it in this phase's shared buffer,
@@ -493,9 +639,21 @@ struct Consumer {
         split_rows(g.N, n0, n1);
         const int nrows = n1 - n0;
         const int buf = gph & 1;
-        float* xs = xin_ptr<T>(s, buf, P.xin_bytes);
+        float* xs = xin_ptr(s, buf, P.xin_bytes);
         ++gph;
         bool good = true;
+        // the input vectors in this phase's buffer: fp32 [M][K] for the FMA rows,
+        // bf16 high and low parts [M][K] each for the tensor-core rows
+        auto put_x = [&](int m, int i, float v) {
+            if constexpr (TCR) {
+                bf16* xh = reinterpret_cast<bf16*>(xs);
+                const bf16 h = __float2bfloat16_rn(v);
+                xh[m * K + i] = h;
+                xh[(M + m) * K + i] = __float2bfloat16_rn(v - __bfloat162float(h));
+            } else {
+                xs[m * K + i] = v;
+            }
+        };
 
         // this thread's RMSNorm weights (K <= NORM_MAX), fetched before any wait
         float nw[NORM_MAX / 256];
@@ -525,7 +683,7 @@ struct Consumer {
                     if (i < K) {
                         const float v = val_of(w[j]);
                         ssq[m] = fmaf(v, v, ssq[m]);
-                        xs[m * K + i] = v * nw[j];
+                        put_x(m, i, v * nw[j]);
                     }
                 }
             }
@@ -539,7 +697,7 @@ struct Consumer {
                     good = ll_poll<4>(w, src, i0, 256, K, e, P);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        if (i0 + q * 256 < K) xs[m * K + i0 + q * 256] = val_of(w[q]);
+                        if (i0 + q * 256 < K) put_x(m, i0 + q * 256, val_of(w[q]));
                 }
             }
         } else {
@@ -560,7 +718,7 @@ struct Consumer {
                             ssq[m] = fmaf(v, v, ssq[m]);
                             v *= nw[j];
                         }
-                        xs[m * K + i] = v;
+                        put_x(m, i, v);
                     }
                 }
             }
@@ -588,14 +746,28 @@ struct Consumer {
             // this CTA's slice of the normed vector (the talker's h, read by the next step)
             int h0, h1;
             split_rows(K, h0, h1);
-            for (int i = h0 + tid; i < h1; i += 256) g.hout[i] = xs[i] * rm[0];
+            for (int i = h0 + tid; i < h1; i += 256) {
+                float xv;
+                if constexpr (TCR) {
+                    const bf16* xh = reinterpret_cast<const bf16*>(xs);
+                    xv = __bfloat162float(xh[i]) + __bfloat162float(xh[M * K + i]);
+                } else {
+                    xv = xs[i];
+                }
+                g.hout[i] = xv * rm[0];
+            }
+        }
+        if constexpr (TCR) {
+            rows_tc<M, GATED>(g, cur, buf, rm, n0, nrows);
+            if (tok && norm) ep[g.src_buf] = cur;
+            return;
         }
 
         // the rows, as they arrive.  A lane covers elements k + 4 l .. k + 4 l + 3
         // and k + 128 + 4 l .. (l = lane) of every 256-element block k: its
         // shared-memory reads of the vector and of a row are contiguous across
         // the warp (no bank conflicts), and the vector is read once per group.
-        const int rt = rows_per_tile<T>(g);
+        const int rt = rows_per_tile<T, TCR>(g);
         const int gpt = (rt + RG - 1) / RG;   // row groups of a full tile
         const size_t row_bytes = (size_t)K * sizeof(T);
         const int jv = split_index<V>(lane);
@@ -716,10 +888,11 @@ struct Consumer {
         if (!ok) return;
         int n0, n1;
         split_rows(g.N, n0, n1);
-        const int nrows = n1 - n0, rt = rows_per_tile<T>(g);
+        const int nrows = n1 - n0, rt = rows_per_tile<T, TCR>(g);
         int rg = nrows >= 3 * NCW ? 4 : (nrows >= 3 * NCW / 2 ? 2 : 1);
         while (rg > rt) rg >>= 1;
-        if (rg == 4) gemv_rg<4>(g, cur);
+        if (TCR) gemv_rg<1>(g, cur);   // tensor-core rows; no row groups
+        else if (rg == 4) gemv_rg<4>(g, cur);
         else if (rg == 2) gemv_rg<2>(g, cur);
         else gemv_rg<1>(g, cur);
         ep[g.dst_buf] = cur;
@@ -952,7 +1125,7 @@ struct Consumer {
         // the draw's scratch overlays the input buffers: every warp must be done
         // with the head's rows first
         consumer_sync();
-        SampSmem& sm = samp_ptr<T>(s);
+        SampSmem& sm = samp_ptr(s);
         if (!settle(ll_fetch(P.cpl, sm.l, P.cpV, ep[BCPL], nullptr, P))) return;
         const q3tts_sampling p = P.P[0];
         if (blockIdx.x == 0 && P.cap_c && P.cap_slot[0] >= 0 && frame < P.cap_T) {
@@ -986,7 +1159,7 @@ struct Consumer {
         next_phase();
         if (!ok || blockIdx.x != 0) return;
         consumer_sync();   // the scratch overlays the input buffers (see draw_cp)
-        SampSmem& sm = samp_ptr<T>(s);
+        SampSmem& sm = samp_ptr(s);
         if (!settle(ll_fetch(P.logits, sm.l, P.V, ep[BLOG], nullptr, P))) return;
         RowState& rs = P.rows[0];
         const q3tts_sampling p = P.P[0];
@@ -1093,10 +1266,10 @@ __device__ void frame_schedule(R& r, const FrameParams& P) {
     r.draw_talker();
 }
 
-template <typename T, int GQ>
+template <typename T, int GQ, bool TCR>
 __global__ void __launch_bounds__(NTHREADS, 1) frame_kernel(const FrameParams* __restrict__ Pp) {
     extern __shared__ __align__(128) unsigned char smraw[];
-    FSmem<T>& s = *reinterpret_cast<FSmem<T>*>(smraw);
+    FSmem<T, TCR>& s = *reinterpret_cast<FSmem<T, TCR>*>(smraw);
     const FrameParams& P = *Pp;
     const RowState& rs = P.rows[0];
     if (rs.finished || aborted(P)) return;   // uniform over the grid
@@ -1116,14 +1289,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) frame_kernel(const FrameParams* _
     const int warp = threadIdx.x >> 5;
     if (warp == NCW) {
         if ((threadIdx.x & 31) == 0) {
-            Producer<T> pr{s, P};
+            Producer<T, TCR> pr{s, P};
             pr.pos = pos;
             frame_schedule<T>(pr, P);
             pr.drain();
         }
         return;
     }
-    Consumer<T, GQ> c{s, P};
+    Consumer<T, GQ, TCR> c{s, P};
     c.frame = frame;
     c.pos = pos;
     c.base = (unsigned)rs.sel << 10;
@@ -1131,9 +1304,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) frame_kernel(const FrameParams* _
 }
 
 // ------------------------------------------------------------------ host side
-template <typename T>
+template <typename T, bool TCR>
 static size_t smem_for(int xin_bytes) {
-    return align128(sizeof(FSmem<T>)) + std::max(2 * align128((size_t)xin_bytes), sizeof(SampSmem));
+    return align128(sizeof(FSmem<T, TCR>)) + std::max(2 * align128((size_t)xin_bytes), sizeof(SampSmem));
 }
 
 size_t frame_attn_scratch_bytes() {
@@ -1141,24 +1314,28 @@ size_t frame_attn_scratch_bytes() {
     return (size_t)(2 * GQ * HD + 4 * HD + 2 * NCW * GQ + NCW * GQ * HD) * sizeof(float);
 }
 
-size_t frame_smem_bytes(int dtype, int xin_bytes) {
-    const size_t b = dtype == Q3_BF16 ? smem_for<bf16>(xin_bytes) : smem_for<float>(xin_bytes);
+// the kernel variant: fp32 weights (FMA rows), bf16 with FMA rows, bf16 with tensor-core rows
+static const void* variant(int dtype, bool tc_rows) {
+    if (dtype != Q3_BF16) return (const void*)frame_kernel<float, 2, false>;
+    return tc_rows ? (const void*)frame_kernel<bf16, 2, true> : (const void*)frame_kernel<bf16, 2, false>;
+}
+
+size_t frame_smem_bytes(int dtype, int xin_bytes, bool tc_rows) {
+    const size_t b = dtype != Q3_BF16 ? smem_for<float, false>(xin_bytes)
+                   : tc_rows ? smem_for<bf16, true>(xin_bytes) : smem_for<bf16, false>(xin_bytes);
     return b <= 227 * 1024 ? b : 0;
 }
 
-cudaError_t frame_setup(int dtype, size_t smem) {
-    if (dtype == Q3_BF16)
-        return cudaFuncSetAttribute(frame_kernel<bf16, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    return cudaFuncSetAttribute(frame_kernel<float, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+cudaError_t frame_setup(int dtype, size_t smem, bool tc_rows) {
+    return cudaFuncSetAttribute(variant(dtype, tc_rows), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
-cudaError_t frame_occupancy(int dtype, size_t smem, int* blocks) {
-    if (dtype == Q3_BF16)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, frame_kernel<bf16, 2>, NTHREADS, smem);
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, frame_kernel<float, 2>, NTHREADS, smem);
+cudaError_t frame_occupancy(int dtype, size_t smem, bool tc_rows, int* blocks) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, variant(dtype, tc_rows), NTHREADS, smem);
 }
 
-cudaError_t launch_frame(int dtype, const FrameParams* params_dev, int grid, size_t smem, cudaStream_t st) {
+cudaError_t launch_frame(int dtype, bool tc_rows, const FrameParams* params_dev, int grid, size_t smem,
+                         cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(NTHREADS);
@@ -1169,8 +1346,9 @@ cudaError_t launch_frame(int dtype, const FrameParams* params_dev, int grid, siz
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (dtype == Q3_BF16) return cudaLaunchKernelEx(&cfg, frame_kernel<bf16, 2>, params_dev);
-    return cudaLaunchKernelEx(&cfg, frame_kernel<float, 2>, params_dev);
+    if (dtype != Q3_BF16) return cudaLaunchKernelEx(&cfg, frame_kernel<float, 2, false>, params_dev);
+    if (tc_rows) return cudaLaunchKernelEx(&cfg, frame_kernel<bf16, 2, true>, params_dev);
+    return cudaLaunchKernelEx(&cfg, frame_kernel<bf16, 2, false>, params_dev);
 }
 
 }  // namespace q3

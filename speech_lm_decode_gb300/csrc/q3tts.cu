@@ -167,6 +167,7 @@ struct q3tts {
     bool capturing = false;
     int splits_t = 1;
     bool frame_ok = false;      // the persistent frame kernel can serve batch 1
+    bool frame_tc = false;      // ... with its GEMV rows on the tensor cores
     size_t frame_smem = 0;
     int frame_grid = 0;
     int frame_xin = 0;
@@ -289,7 +290,7 @@ int enqueue_cp_input(q3tts* h, int M) {
 // One talker step for the whole batch: complete frame k-1 through the code
 // predictor, assemble the next talker input, run the talker, select code0.
 int enqueue_frame(q3tts* h) {
-    CK(launch_frame(h->c.dtype, h->p<FrameParams>(h->L.fparams), h->frame_grid, h->frame_smem, h->st)); debug_wait(h->st, "launch_frame");
+    CK(launch_frame(h->c.dtype, h->frame_tc, h->p<FrameParams>(h->L.fparams), h->frame_grid, h->frame_smem, h->st)); debug_wait(h->st, "launch_frame");
     return Q3_OK;
 }
 
@@ -477,15 +478,22 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
         const size_t tile = FRAME_TILE;
         const bool tiles_fit = (size_t)H * e * 2 <= tile && (size_t)Hc * e * 2 <= tile &&
                                (size_t)std::max(cfg->ffn, cfg->cp_ffn) * e <= tile && (size_t)nqh * e <= tile;
-        h->frame_smem = frame_smem_bytes(cfg->dtype, h->frame_xin);
+        // tensor-core rows where the phases are short (hidden <= 1024: the chain's
+        // latency dominates); FMA rows for wider models, whose phases stream
+        // long weight slices and are bandwidth-bound
+        h->frame_tc = cfg->dtype == Q3_BF16 && H <= 1024 && Hc <= 1024;
+        h->frame_smem = frame_smem_bytes(cfg->dtype, h->frame_xin, h->frame_tc);
         const char* env = getenv("Q3TTS_FRAME_KERNEL");
         const bool want = !(env && env[0] == '0');
         h->frame_ok = want && coop && sms >= cfg->n_kv_heads && h->frame_smem > 0 && tiles_fit &&
                       cfg->n_q_heads == 2 * cfg->n_kv_heads;
-        if (h->frame_ok && frame_setup(cfg->dtype, h->frame_smem) != cudaSuccess) { cudaGetLastError(); h->frame_ok = false; }
+        if (h->frame_ok && frame_setup(cfg->dtype, h->frame_smem, h->frame_tc) != cudaSuccess) {
+            cudaGetLastError();
+            h->frame_ok = false;
+        }
         if (h->frame_ok) {
             int blocks = 0;
-            if (frame_occupancy(cfg->dtype, h->frame_smem, &blocks) != cudaSuccess || blocks < 1) {
+            if (frame_occupancy(cfg->dtype, h->frame_smem, h->frame_tc, &blocks) != cudaSuccess || blocks < 1) {
                 cudaGetLastError();
                 h->frame_ok = false;
             }
@@ -498,7 +506,16 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
         const int phases = (cfg->n_groups - 1) * ((H != Hc ? 1 : 0) + 5 * cfg->cp_layers + 2) + 5 * cfg->n_layers + 2;
         // residual rows a CTA updates in one phase fit its buffer
         auto rows = [&](int n) { return (n + grid - 1) / grid; };
-        const bool v_ok = rows(H) <= FRAME_MAX_ROWS && rows(Hc) <= FRAME_MAX_ROWS;
+        bool v_ok = rows(H) <= FRAME_MAX_ROWS && rows(Hc) <= FRAME_MAX_ROWS;
+        if (cfg->dtype == Q3_BF16 && cfg->hidden <= 1024 && cfg->cp_hidden <= 1024) {
+            // tensor-core rows: K in steps of 16, and a phase's partial sums (rows x
+            // gate/up x vectors x 8 splits) fit the CTA's buffer
+            for (int k : {H, cfg->ffn, Hc, cfg->cp_ffn, nqh}) v_ok = v_ok && k % 16 == 0;
+            const int pmax = FRAME_MAX_PART / 8;
+            v_ok = v_ok && rows(nqkv) * 2 <= pmax && rows(cfg->ffn) * 2 <= pmax && rows(cfg->cp_ffn) * 4 <= pmax &&
+                   rows(H) * 2 <= pmax && rows(Hc) * 2 <= pmax && rows(cfg->codec_vocab) <= pmax &&
+                   rows(cfg->cp_vocab) <= pmax;
+        }
         const bool grid_ok = grid >= cfg->n_kv_heads && v_ok && phases <= FRAME_MAX_PHASES &&
                              cfg->n_kv_heads + 8 <= FRAME_CTL_WORDS && H <= FRAME_MAX_NORM && Hc <= FRAME_MAX_NORM;
         h->frame_ok = h->frame_ok && grid_ok;
