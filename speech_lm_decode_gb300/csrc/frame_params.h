@@ -69,8 +69,6 @@ struct FrameParams {
 constexpr int FRAME_CTL_WORDS = 64;
 constexpr int FRAME_MAX_ROWS = 128;   // residual rows one CTA updates in one phase
 constexpr int FRAME_MAX_PART = 1024;  // partial sums of one phase on one CTA (rows x 2 x 2 x 8 splits)
-constexpr int FRAME_TILE = 24 * 1024; // bytes of one weight ring slot
-constexpr int FRAME_SLOTS = 6;        // ring slots
 constexpr int FRAME_MAX_PHASES = 1024;  // phases of one launch (epoch = selection * 1024 + phase)
 constexpr int FRAME_MAX_NORM = 2048;    // widest RMSNorm input (talker and predictor widths)
 
@@ -79,6 +77,9 @@ constexpr int FRAME_MAX_NORM = 2048;    // widest RMSNorm input (talker and pred
 // tc_rows: bf16 GEMV rows on the tensor cores (else FMA rows)
 size_t frame_smem_bytes(int dtype, int xin_bytes, bool tc_rows);
 size_t frame_attn_scratch_bytes();
+// bytes of one weight ring slot of a kernel variant
+size_t frame_tile_bytes(bool tc_rows);
+constexpr int FRAME_CP_VMAX = 2048;   // largest predictor vocabulary the frame kernel draws over
 // One-time attribute setup; returns cudaSuccess when the kernel can run.
 cudaError_t frame_setup(int dtype, size_t smem, bool tc_rows);
 // CTAs of the frame kernel that fit one SM with this shared memory.

@@ -54,8 +54,16 @@ namespace q3 {
 
 constexpr int NCW = 8;                       // consumer warps
 constexpr int NTHREADS = (NCW + 1) * 32;     // + one producer warp
-constexpr int TILE = FRAME_TILE;             // bytes per ring slot
-constexpr int NSLOT = FRAME_SLOTS;
+// Weight ring of a kernel variant (24 KB slots): six for the tensor-core rows
+// (whose row buffer of partial sums takes the room of a seventh), seven for
+// the FMA rows.  Measured on config 2, more slots or wider windows of the
+// tensor-core rows do not help.
+template <bool TCR>
+struct Ring {
+    static constexpr int SLOTS = TCR ? 6 : 7;
+    static constexpr int TILE = 24576;
+};
+constexpr int CP_VMAX = 2048;                // predictor vocabulary bound of the frame kernel
 constexpr long long WAIT_LIMIT = 4000000000LL;  // cycles (~2 s) before a wait gives up
 constexpr int NORM_MAX = FRAME_MAX_NORM;     // widest vector an RMSNorm prologue normalizes
 constexpr int ROW_PAD = 32;                  // bytes after each bf16 weight row in the ring
@@ -198,6 +206,7 @@ __device__ bool ll_fetch(const Word* src, float* dst, int n, unsigned ep, float*
 // ------------------------------------------------------------------ shared memory
 template <typename T, bool TCR>
 struct FSmem {
+    static constexpr int NSLOT = Ring<TCR>::SLOTS, TILE = Ring<TCR>::TILE;
     unsigned char ring[NSLOT][TILE];
     uint64_t full[NSLOT];
     uint64_t empty[NSLOT];
@@ -207,9 +216,11 @@ struct FSmem {
     float part[TCR ? FRAME_MAX_PART : 1];
     int codes[MAX_GROUPS];              // this frame's codes as drawn so far
     int flag;
-    // then one region for: two input-vector buffers (fp32 [M][K], one per GEMV
-    // phase parity; the attention phase's scratch shares the one the next GEMV
-    // phase fills) or, during a draw (when no GEMV reads them), the draw's scratch
+    // then one region for: two input-vector buffers (one per GEMV phase
+    // parity; the attention phase's scratch shares the one the next GEMV
+    // phase fills) or, during a predictor draw (when no GEMV reads them), the
+    // draw's scratch.  The talker's draw, the launch's last step, runs on CTA 0
+    // in the drained weight ring.
 };
 
 __host__ __device__ constexpr size_t align128(size_t v) { return (v + 127) & ~(size_t)127; }
@@ -219,8 +230,8 @@ __device__ __forceinline__ float* xin_ptr(S& s, int buf, int xin_bytes) {
                                     (size_t)buf * align128((size_t)xin_bytes));
 }
 template <class S>
-__device__ __forceinline__ SampSmem& samp_ptr(S& s) {
-    return *reinterpret_cast<SampSmem*>(reinterpret_cast<unsigned char*>(&s) + align128(sizeof(S)));
+__device__ __forceinline__ SampSmemT<CP_VMAX>& samp_ptr(S& s) {
+    return *reinterpret_cast<SampSmemT<CP_VMAX>*>(reinterpret_cast<unsigned char*>(&s) + align128(sizeof(S)));
 }
 
 // ------------------------------------------------------------------ the frame schedule
@@ -269,24 +280,25 @@ __device__ __forceinline__ int row_stride(int K) {
 template <typename T, bool TCR>
 __device__ __forceinline__ int rows_per_tile(const Gemv& g) {
     const int unit = row_stride<T, TCR>(g.K) * (g.gated ? 2 : 1);
-    return max(1, TILE / unit);
+    return max(1, Ring<TCR>::TILE / unit);
 }
 
 // Cached positions [j0, j1) of talker attention split sp that the producer
 // prefetches (all before the new token's position p0); false if none, or if
 // they do not fit one ring slot (then the consumer reads them directly).
-template <typename T>
+template <typename T, bool TCR>
 __device__ __forceinline__ bool kv_prefetch_range(int p0, int S, int sp, int& j0, int& j1) {
     const int n = p0 + 1;
     const int chunk = (n + S - 1) / S;
     j0 = sp * chunk;
     j1 = min(min(n, j0 + chunk), p0);
-    return j1 > j0 && (size_t)(j1 - j0) * HD * sizeof(T) * 2 <= (size_t)TILE;
+    return j1 > j0 && (size_t)(j1 - j0) * HD * sizeof(T) * 2 <= (size_t)Ring<TCR>::TILE;
 }
 
 // ------------------------------------------------------------------ producer
 template <typename T, bool TCR>
 struct Producer {
+    static constexpr int NSLOT = Ring<TCR>::SLOTS;
     FSmem<T, TCR>& s;
     const FrameParams& P;
     unsigned seq = 0;
@@ -339,7 +351,7 @@ struct Producer {
         for (int item = blockIdx.x; item < P.nkv * S; item += gridDim.x) {
             const int g = item / S, sp = item % S;
             int j0, j1;
-            if (!kv_prefetch_range<T>(p0, S, sp, j0, j1)) continue;
+            if (!kv_prefetch_range<T, TCR>(p0, S, sp, j0, j1)) continue;
             int slot;
             if (!take_slot(slot)) return;
             const size_t row_bytes = (size_t)HD * sizeof(T);
@@ -450,6 +462,7 @@ __device__ __forceinline__ int split_index(int lane) {
 // ------------------------------------------------------------------ consumer
 template <typename T, int GQ, bool TCR>
 struct Consumer {
+    static constexpr int NSLOT = Ring<TCR>::SLOTS, TILE = Ring<TCR>::TILE;
     FSmem<T, TCR>& s;
     const FrameParams& P;
     unsigned seq = 0;        // ring slots consumed
@@ -463,7 +476,7 @@ struct Consumer {
     bool failed = false;     // a wait of this thread failed (reported at the next settle)
 
     // input-vector buffer of the next GEMV phase (also the attention scratch)
-    __device__ float* xin_next() { return xin_ptr(s, gph & 1, P.xin_bytes); }
+    __device__ float* xin_next() { return xin_ptr(s, (int)(gph & 1), P.xin_bytes); }
     __device__ unsigned next_phase() { return base + ph++; }
 
     // Every thread reports whether its waits succeeded (and any wait that failed
@@ -986,7 +999,7 @@ struct Consumer {
                 const T* vring = nullptr;
                 int pj0 = 0, pj1 = 0, slot = -1;
                 bool ring_ok = true;
-                if (talker && kv_prefetch_range<T>(p0, S, sp, pj0, pj1)) {
+                if (talker && kv_prefetch_range<T, TCR>(p0, S, sp, pj0, pj1)) {
                     slot = seq % NSLOT;
                     const unsigned round = seq / NSLOT;
                     ++seq;
@@ -1125,7 +1138,7 @@ struct Consumer {
         // the draw's scratch overlays the input buffers: every warp must be done
         // with the head's rows first
         consumer_sync();
-        SampSmem& sm = samp_ptr(s);
+        auto& sm = samp_ptr(s);
         if (!settle(ll_fetch(P.cpl, sm.l, P.cpV, ep[BCPL], nullptr, P))) return;
         const q3tts_sampling p = P.P[0];
         if (blockIdx.x == 0 && P.cap_c && P.cap_slot[0] >= 0 && frame < P.cap_T) {
@@ -1158,8 +1171,11 @@ struct Consumer {
     __device__ void draw_talker() {
         next_phase();
         if (!ok || blockIdx.x != 0) return;
-        consumer_sync();   // the scratch overlays the input buffers (see draw_cp)
-        SampSmem& sm = samp_ptr(s);
+        // the launch's last step: every weight tile has been consumed, so the
+        // draw's scratch (the full vocabulary) can live in the drained ring
+        static_assert(sizeof(SampSmem) <= sizeof(s.ring), "talker draw scratch must fit the ring");
+        consumer_sync();
+        SampSmem& sm = *reinterpret_cast<SampSmem*>(&s.ring[0][0]);
         if (!settle(ll_fetch(P.logits, sm.l, P.V, ep[BLOG], nullptr, P))) return;
         RowState& rs = P.rows[0];
         const q3tts_sampling p = P.P[0];
@@ -1280,7 +1296,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) frame_kernel(const FrameParams* _
         return;
     }
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NSLOT; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], NCW); }
+        for (int i = 0; i < Ring<TCR>::SLOTS; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], NCW); }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s.codes[0] = code0;
         if (blockIdx.x == 0) P.codes[(size_t)frame * MAX_GROUPS] = code0;
@@ -1306,8 +1322,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) frame_kernel(const FrameParams* _
 // ------------------------------------------------------------------ host side
 template <typename T, bool TCR>
 static size_t smem_for(int xin_bytes) {
-    return align128(sizeof(FSmem<T, TCR>)) + std::max(2 * align128((size_t)xin_bytes), sizeof(SampSmem));
+    return align128(sizeof(FSmem<T, TCR>)) +
+           std::max(2 * align128((size_t)xin_bytes), sizeof(SampSmemT<CP_VMAX>));
 }
+
+size_t frame_tile_bytes(bool tc_rows) { return tc_rows ? Ring<true>::TILE : Ring<false>::TILE; }
 
 size_t frame_attn_scratch_bytes() {
     constexpr int GQ = 2;

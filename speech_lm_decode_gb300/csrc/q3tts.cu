@@ -475,17 +475,19 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
         const int kx_c = std::max(std::max(Hc, cfg->cp_ffn), std::max(nqh, H != Hc ? H : 0));
         h->frame_xin = (int)std::max((size_t)4 * std::max(kx_t, 2 * kx_c), frame_attn_scratch_bytes());
         const size_t e = esize(cfg->dtype);
-        const size_t tile = FRAME_TILE;
+        const bool tc_shape = cfg->dtype == Q3_BF16 && H <= 1024 && Hc <= 1024;
+        const size_t tile = frame_tile_bytes(tc_shape);
         const bool tiles_fit = (size_t)H * e * 2 <= tile && (size_t)Hc * e * 2 <= tile &&
                                (size_t)std::max(cfg->ffn, cfg->cp_ffn) * e <= tile && (size_t)nqh * e <= tile;
         // tensor-core rows where the phases are short (hidden <= 1024: the chain's
         // latency dominates); FMA rows for wider models, whose phases stream
         // long weight slices and are bandwidth-bound
-        h->frame_tc = cfg->dtype == Q3_BF16 && H <= 1024 && Hc <= 1024;
+        h->frame_tc = tc_shape;
         h->frame_smem = frame_smem_bytes(cfg->dtype, h->frame_xin, h->frame_tc);
         const char* env = getenv("Q3TTS_FRAME_KERNEL");
         const bool want = !(env && env[0] == '0');
         h->frame_ok = want && coop && sms >= cfg->n_kv_heads && h->frame_smem > 0 && tiles_fit &&
+                      cfg->cp_vocab <= FRAME_CP_VMAX &&
                       cfg->n_q_heads == 2 * cfg->n_kv_heads;
         if (h->frame_ok && frame_setup(cfg->dtype, h->frame_smem, h->frame_tc) != cudaSuccess) {
             cudaGetLastError();

@@ -103,11 +103,13 @@ __device__ __forceinline__ int samp_sync_or(int v) {
     return r;
 }
 
-struct SampSmem {
-    float l[MAX_VOCAB];
-    unsigned long long key[MAX_VOCAB];
-    int kept[MAX_VOCAB];
-    unsigned char keep_flag[MAX_VOCAB];
+// Scratch of one draw over at most VMAX logits.
+template <int VMAX>
+struct SampSmemT {
+    float l[VMAX];
+    unsigned long long key[VMAX];
+    int kept[VMAX];
+    unsigned char keep_flag[VMAX];
     int hist[256];
     long long scan[ST];
     float red_f[ST / 32];
@@ -116,12 +118,15 @@ struct SampSmem {
     float mx;
     long long Z;
 };
+using SampSmem = SampSmemT<MAX_VOCAB>;
+
 
 
 __device__ __forceinline__ bool better(float a, int ia, float b, int ib) { return a > b || (a == b && ia < ib); }
 
 // Argmax over (value desc, index asc); the result index is returned to all threads.
-__device__ __forceinline__ int block_argmax(SampSmem& sm, float v, int i) {
+template <class S>
+__device__ __forceinline__ int block_argmax(S& sm, float v, int i) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
         const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
@@ -143,7 +148,8 @@ __device__ __forceinline__ int block_argmax(SampSmem& sm, float v, int i) {
     return sm.result;
 }
 
-__device__ __forceinline__ float block_max(SampSmem& sm, float v) {
+template <class S>
+__device__ __forceinline__ float block_max(S& sm, float v) {
     v = warp_max(v);
     samp_sync();
     if ((threadIdx.x & 31) == 0) sm.red_f[threadIdx.x >> 5] = v;
@@ -155,7 +161,8 @@ __device__ __forceinline__ float block_max(SampSmem& sm, float v) {
 }
 
 // Inclusive scan of one int64 per thread (thread order); also returns the total.
-__device__ __forceinline__ long long block_scan_ll(SampSmem& sm, long long v, long long* total) {
+template <class S>
+__device__ __forceinline__ long long block_scan_ll(S& sm, long long v, long long* total) {
     sm.scan[threadIdx.x] = v;
     samp_sync();
     for (int o = 1; o < ST; o <<= 1) {
@@ -180,7 +187,8 @@ __device__ __forceinline__ float order_key_inv(uint32_t k) {
 
 // k-th largest of l[0..V) counting multiplicity (1 <= k <= V): MSB-first radix
 // select over the order-preserving 32-bit keys, 8 bits per pass.
-__device__ __forceinline__ float kth_largest(SampSmem& sm, int V, int k) {
+template <class S>
+__device__ __forceinline__ float kth_largest(S& sm, int V, int k) {
     uint32_t prefix = 0, pmask = 0;
     int kk = k;
     for (int shift = 24; shift >= 0; shift -= 8) {
@@ -217,7 +225,9 @@ struct DrawCfg {
 //   lg: the raw logits in global memory, or nullptr when sm.l[0, V) holds them
 //       (each thread i of the block must have written the entries i, i + 256, ...).
 //   seen_bits / seen_bytes: ids drawn before (penalty); one of them or neither.
-static __device__ __noinline__ int sample_row(SampSmem& sm, const float* __restrict__ lg, int V, DrawCfg d, bool talker, float penalty,
+//   S: a SampSmemT<VMAX> with V <= VMAX.
+template <class S>
+static __device__ __noinline__ int sample_row(S& sm, const float* __restrict__ lg, int V, DrawCfg d, bool talker, float penalty,
                           const uint32_t* seen_bits, const uint8_t* seen_bytes, int sel, int min_new, int eos,
                           int sup_lo, int sup_hi, uint64_t seed, uint32_t row, uint32_t frame, uint32_t step) {
     const int tid = threadIdx.x;
