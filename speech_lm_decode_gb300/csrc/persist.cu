@@ -390,11 +390,13 @@ __device__ __forceinline__ P* launder(P* p) {
     asm volatile("mov.b64 %0, %0;" : "+l"(v)::"memory");
     return reinterpret_cast<P*>(v);
 }
-// D += A B for mma.m16n8k16 (bf16 in, fp32 accumulate); A rows 8..15 are zero
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+// D += A B for mma.m16n8k16 (bf16 in, fp32 accumulate).  a0 / a2: this lane's
+// A row (lane / 4), low / high k pair; a1 / a3: the same for A row lane / 4 + 8.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 // 4 consecutive elements (index multiple of 4) as fp32
 __device__ __forceinline__ void load4(const bf16* p, float (&v)[4]) {
@@ -517,13 +519,14 @@ struct Consumer {
     }
 
     // The rows of a GEMV phase on the tensor cores (bf16 weights).  Each
-    // mma.m16n8k16 multiplies the input vectors (A: rows 0..M-1 of 16, bf16 high
-    // part, then low part into the same accumulator) with 8 weight rows (B)
-    // over 16 elements of K.  The K order inside a 16-element step is permuted
-    // so that a lane's A and B fragments are 4 consecutive elements (one 8-byte
-    // load): MMA k pairs (2q, 2q+1) and (2q+8, 2q+9) are elements 4q..4q+3.
+    // mma.m16n8k16 multiplies 16 weight rows (A) with the input vectors (B:
+    // column 2m is vector m's bf16 high part, column 2m + 1 its low part) over
+    // 16 elements of K, so one instruction gives both parts of 16 dot products.
+    // The K order inside a 16-element step is permuted so that a lane's A and B
+    // fragments are 4 consecutive elements (one 8-byte load each): MMA k pairs
+    // (2q, 2q+1) and (2q+8, 2q+9) are elements 4q..4q+3.
     // The phase's tiles are taken WT at a time (all resident); a window's rows
-    // form 8-row blocks (across tiles), and (block, K split) units are dealt to
+    // form 16-row blocks (across tiles), and (block, K split) units are dealt to
     // the warps; their partial sums meet in shared memory, and after the
     // phase's second barrier one thread per output adds the splits in order.
     template <int M, bool GATED>
@@ -534,13 +537,14 @@ struct Consumer {
         const int rt = rows_per_tile<T, TCR>(g);
         const size_t rs = (size_t)row_stride<T, TCR>(K);
         const int ntiles = (nrows + rt - 1) / rt;
-        const int nbw = (min(WT * rt, nrows) + 7) >> 3;   // blocks of a full window
+        const int nbw = (min(WT * rt, nrows) + 15) >> 4;   // blocks of a full window
         const int ks = max(1, min(KSMAX, NCW / nbw));
         const int gq = lane >> 2, q = lane & 3;
-        const bool xrow = gq < M;
+        // B fragment: this lane supplies column gq (vector gq / 2, high part if
+        // gq is even); columns from 2M on are zero
+        const bool xcol = gq < 2 * M;
         const unsigned char* xb = reinterpret_cast<const unsigned char*>(xin_ptr(s, buf, P.xin_bytes));
-        const unsigned char* xh = xb + (size_t)min(gq, M - 1) * K * 2 + q * 8;
-        const unsigned char* xl = xh + (size_t)M * K * 2;
+        const unsigned char* xa = xb + ((size_t)(gq & 1) * M + min(gq >> 1, M - 1)) * K * 2 + q * 8;
         float* part = s.part;
         bool good = true;
         for (int w0 = 0; w0 < ntiles; w0 += WT) {
@@ -553,16 +557,22 @@ struct Consumer {
             seq += wt;
             const int row_w0 = w0 * rt;
             const int rw = min(wt * rt, nrows - row_w0);
-            const int nb = (rw + 7) >> 3;
+            const int nb = (rw + 15) >> 4;
             for (int u = warp; good && u < nb * ks; u += NCW) {
                 const int b = u / ks, kq = u - b * ks;
                 const int k0 = nks * kq / ks, k1 = nks * (kq + 1) / ks;
-                const int j = min(b * 8 + gq, rw - 1);   // this lane's weight row in the window
-                const int t = j / rt, i = j - t * rt;
-                const int rtile = min(rt, nrows - row_w0 - t * rt);
-                const unsigned char* tb = s.ring[(seqw + t) % NSLOT];
-                const unsigned char* wa = tb + (size_t)i * rs + q * 8;
-                const unsigned char* ua = tb + (size_t)(rtile + i) * rs + q * 8;
+                // this lane's A rows of the block: gq and gq + 8 (clamped into the window)
+                const unsigned char* wa[2];
+                const unsigned char* ua[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int j = min(b * 16 + gq + 8 * h, rw - 1);
+                    const int t = j / rt, i = j - t * rt;
+                    const int rtile = min(rt, nrows - row_w0 - t * rt);
+                    const unsigned char* tb = s.ring[(seqw + t) % NSLOT];
+                    wa[h] = tb + (size_t)i * rs + q * 8;
+                    ua[h] = tb + (size_t)(rtile + i) * rs + q * 8;
+                }
                 float d[4][H2][4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
@@ -575,33 +585,32 @@ struct Consumer {
                     for (int c = 0; c < 4; ++c) {
                         const int k = kk + c;
                         if (k < k1) {
-                            const uint2 bw = *reinterpret_cast<const uint2*>(wa + (size_t)k * 32);
-                            uint2 ah = make_uint2(0u, 0u), al = make_uint2(0u, 0u);
-                            if (xrow) {
-                                ah = *reinterpret_cast<const uint2*>(xh + (size_t)k * 32);
-                                al = *reinterpret_cast<const uint2*>(xl + (size_t)k * 32);
-                            }
-                            mma_bf16(d[c][0], ah.x, ah.y, bw.x, bw.y);
-                            mma_bf16(d[c][0], al.x, al.y, bw.x, bw.y);
+                            uint2 xv = make_uint2(0u, 0u);
+                            if (xcol) xv = *reinterpret_cast<const uint2*>(xa + (size_t)k * 32);
+                            const uint2 w0 = *reinterpret_cast<const uint2*>(wa[0] + (size_t)k * 32);
+                            const uint2 w1 = *reinterpret_cast<const uint2*>(wa[1] + (size_t)k * 32);
+                            mma_bf16(d[c][0], w0.x, w1.x, w0.y, w1.y, xv.x, xv.y);
                             if (GATED) {
-                                const uint2 bu = *reinterpret_cast<const uint2*>(ua + (size_t)k * 32);
-                                mma_bf16(d[c][H2 - 1], ah.x, ah.y, bu.x, bu.y);
-                                mma_bf16(d[c][H2 - 1], al.x, al.y, bu.x, bu.y);
+                                const uint2 u0 = *reinterpret_cast<const uint2*>(ua[0] + (size_t)k * 32);
+                                const uint2 u1 = *reinterpret_cast<const uint2*>(ua[1] + (size_t)k * 32);
+                                mma_bf16(d[c][H2 - 1], u0.x, u1.x, u0.y, u1.y, xv.x, xv.y);
                             }
                         }
                     }
                 }
-                // lane 4m + q holds vector m's sums for rows 2q and 2q + 1 of the block
-                if (xrow) {
+                // lane 4 r + q (q < M) holds vector q's high and low sums of
+                // rows r (d[0], d[1]) and r + 8 (d[2], d[3]) of the block
+                if (q < M) {
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int jr = b * 8 + 2 * q + e;
+                        const int jr = b * 16 + gq + 8 * e;
                         if (jr < rw) {
                             const int prow = row_w0 + jr;
 #pragma unroll
                             for (int h = 0; h < H2; ++h)
-                                part[((prow * H2 + h) * M + gq) * KSMAX + kq] =
-                                    (d[0][h][e] + d[1][h][e]) + (d[2][h][e] + d[3][h][e]);
+                                part[((prow * H2 + h) * M + q) * KSMAX + kq] =
+                                    ((d[0][h][2 * e] + d[0][h][2 * e + 1]) + (d[1][h][2 * e] + d[1][h][2 * e + 1])) +
+                                    ((d[2][h][2 * e] + d[2][h][2 * e + 1]) + (d[3][h][2 * e] + d[3][h][2 * e + 1]));
                         }
                     }
                 }
