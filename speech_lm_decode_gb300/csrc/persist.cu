@@ -390,6 +390,18 @@ __device__ __forceinline__ P* launder(P* p) {
     asm volatile("mov.b64 %0, %0;" : "+l"(v)::"memory");
     return reinterpret_cast<P*>(v);
 }
+// a shared-memory address through an opaque register move: loads from it
+// cannot be scheduled before the statement
+__device__ __forceinline__ uint32_t launder_u32(uint32_t v) {
+    asm volatile("mov.b32 %0, %0;" : "+r"(v)::"memory");
+    return v;
+}
+// 8-byte shared-memory load (not volatile: the compiler may batch them)
+__device__ __forceinline__ uint2 lds_v2(uint32_t a) {
+    uint2 r;
+    asm("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(a));
+    return r;
+}
 // D += A B for mma.m16n8k16 (bf16 in, fp32 accumulate).  a0 / a2: this lane's
 // A row (lane / 4), low / high k pair; a1 / a3: the same for A row lane / 4 + 8.
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -543,8 +555,9 @@ struct Consumer {
         // B fragment: this lane supplies column gq (vector gq / 2, high part if
         // gq is even); columns from 2M on are zero
         const bool xcol = gq < 2 * M;
-        const unsigned char* xb = reinterpret_cast<const unsigned char*>(xin_ptr(s, buf, P.xin_bytes));
-        const unsigned char* xa = xb + ((size_t)(gq & 1) * M + min(gq >> 1, M - 1)) * K * 2 + q * 8;
+        // the vector was stored before the phase's barrier; its address is taken after it
+        const uint32_t xa = launder_u32(smem_u32(xin_ptr(s, buf, P.xin_bytes))) +
+                            (uint32_t)(((gq & 1) * M + min(gq >> 1, M - 1)) * K * 2 + q * 8);
         float* part = s.part;
         bool good = true;
         for (int w0 = 0; w0 < ntiles; w0 += WT) {
@@ -555,6 +568,8 @@ struct Consumer {
                 good = good && mbar_wait(&s.full[sq % NSLOT], (sq / NSLOT) & 1, P);
             }
             seq += wt;
+            // ring addresses taken after the waits
+            const uint32_t ring = launder_u32(smem_u32(&s.ring[0][0]));
             const int row_w0 = w0 * rt;
             const int rw = min(wt * rt, nrows - row_w0);
             const int nb = (rw + 15) >> 4;
@@ -562,16 +577,15 @@ struct Consumer {
                 const int b = u / ks, kq = u - b * ks;
                 const int k0 = nks * kq / ks, k1 = nks * (kq + 1) / ks;
                 // this lane's A rows of the block: gq and gq + 8 (clamped into the window)
-                const unsigned char* wa[2];
-                const unsigned char* ua[2];
+                uint32_t wa[2], ua[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int j = min(b * 16 + gq + 8 * h, rw - 1);
                     const int t = j / rt, i = j - t * rt;
                     const int rtile = min(rt, nrows - row_w0 - t * rt);
-                    const unsigned char* tb = s.ring[(seqw + t) % NSLOT];
-                    wa[h] = tb + (size_t)i * rs + q * 8;
-                    ua[h] = tb + (size_t)(rtile + i) * rs + q * 8;
+                    const uint32_t tb = ring + (uint32_t)(((seqw + t) % NSLOT) * TILE);
+                    wa[h] = tb + (uint32_t)(i * rs + q * 8);
+                    ua[h] = tb + (uint32_t)((rtile + i) * rs + q * 8);
                 }
                 float d[4][H2][4];
 #pragma unroll
@@ -580,22 +594,38 @@ struct Consumer {
                     for (int h = 0; h < H2; ++h)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) d[c][h][e] = 0.f;
-                for (int kk = k0; kk < k1; kk += 4) {
+                // four K steps at a time, every load of the four issued before their MMAs
+                int k = k0;
+                for (; k + 4 <= k1; k += 4) {
+                    uint2 xv[4], w0[4], w1[4], u0[GATED ? 4 : 1], u1[GATED ? 4 : 1];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const int k = kk + c;
-                        if (k < k1) {
-                            uint2 xv = make_uint2(0u, 0u);
-                            if (xcol) xv = *reinterpret_cast<const uint2*>(xa + (size_t)k * 32);
-                            const uint2 w0 = *reinterpret_cast<const uint2*>(wa[0] + (size_t)k * 32);
-                            const uint2 w1 = *reinterpret_cast<const uint2*>(wa[1] + (size_t)k * 32);
-                            mma_bf16(d[c][0], w0.x, w1.x, w0.y, w1.y, xv.x, xv.y);
-                            if (GATED) {
-                                const uint2 u0 = *reinterpret_cast<const uint2*>(ua[0] + (size_t)k * 32);
-                                const uint2 u1 = *reinterpret_cast<const uint2*>(ua[1] + (size_t)k * 32);
-                                mma_bf16(d[c][H2 - 1], u0.x, u1.x, u0.y, u1.y, xv.x, xv.y);
-                            }
+                        const uint32_t o = (uint32_t)(k + c) * 32u;
+                        xv[c] = make_uint2(0u, 0u);
+                        if (xcol) xv[c] = lds_v2(xa + o);
+                        w0[c] = lds_v2(wa[0] + o);
+                        w1[c] = lds_v2(wa[1] + o);
+                        if constexpr (GATED) {
+                            u0[c] = lds_v2(ua[0] + o);
+                            u1[c] = lds_v2(ua[1] + o);
                         }
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        mma_bf16(d[c][0], w0[c].x, w1[c].x, w0[c].y, w1[c].y, xv[c].x, xv[c].y);
+                        if constexpr (GATED)
+                            mma_bf16(d[c][H2 - 1], u0[c].x, u1[c].x, u0[c].y, u1[c].y, xv[c].x, xv[c].y);
+                    }
+                }
+                for (; k < k1; ++k) {
+                    const uint32_t o = (uint32_t)k * 32u;
+                    uint2 xv = make_uint2(0u, 0u);
+                    if (xcol) xv = lds_v2(xa + o);
+                    const uint2 a0 = lds_v2(wa[0] + o), a1 = lds_v2(wa[1] + o);
+                    mma_bf16(d[0][0], a0.x, a1.x, a0.y, a1.y, xv.x, xv.y);
+                    if constexpr (GATED) {
+                        const uint2 g0 = lds_v2(ua[0] + o), g1 = lds_v2(ua[1] + o);
+                        mma_bf16(d[0][H2 - 1], g0.x, g1.x, g0.y, g1.y, xv.x, xv.y);
                     }
                 }
                 // lane 4 r + q (q < M) holds vector q's high and low sums of
@@ -1217,78 +1247,170 @@ struct Consumer {
 
 
 // ------------------------------------------------------------------ schedule
-template <typename T, class R>
-__device__ void layer(R& r, const FrameParams& P, const PBlk& B, int l, int M, int p0, int S, Word* x, int xb,
-                      Tok tok, int s_idx, bool talker) {
+// The step is a flat list of phases walked by one loop, so that each kind of
+// phase has exactly one call site: one copy of its code, which stays in the
+// instruction cache from one use to the next (a call site per layer phase
+// would inline a separate copy of the same GEMV code for each).
+enum class Ph { PROJ, QKV, ATTN, O, GU, DOWN, HEAD, DRAW_CP, PREP_T, DRAW_T };
+
+struct PhaseAt {
+    Ph kind;
+    int s;         // predictor pass (codebook s + 1 is drawn at its end)
+    int l;         // layer
+    bool talker;
+};
+
+// phase i of the step: predictor passes s = 0..G-2 ([projection], 5 phases per
+// layer, head, draw), then the talker (prepare, 5 phases per layer, head, draw)
+__device__ __forceinline__ PhaseAt phase_at(int i, const FrameParams& P) {
+    const int proj = P.H != P.Hc ? 1 : 0;
+    const int per_pass = proj + 5 * P.c.L + 2;
+    const int n_pred = (P.G - 1) * per_pass;
+    PhaseAt a{Ph::PREP_T, 0, 0, false};
+    int j;
+    int L;
+    if (i < n_pred) {
+        a.s = i / per_pass;
+        j = i - a.s * per_pass;
+        if (proj && j == 0) { a.kind = Ph::PROJ; return a; }
+        j -= proj;
+        L = P.c.L;
+    } else {
+        a.talker = true;
+        j = i - n_pred;
+        if (j == 0) return a;   // PREP_T
+        j -= 1;
+        L = P.t.L;
+    }
+    if (j < 5 * L) {
+        a.l = j / 5;
+        a.kind = (Ph)((int)Ph::QKV + j % 5);
+    } else {
+        a.kind = j == 5 * L ? Ph::HEAD : (a.talker ? Ph::DRAW_T : Ph::DRAW_CP);
+    }
+    return a;
+}
+
+__device__ __forceinline__ int phase_count(const FrameParams& P) {
+    const int proj = P.H != P.Hc ? 1 : 0;
+    return (P.G - 1) * (proj + 5 * P.c.L + 2) + 1 + 5 * P.t.L + 2;
+}
+
+// the GEMV of a projection, layer or head phase
+template <typename T>
+__device__ __forceinline__ Gemv phase_gemv(const PhaseAt& a, const FrameParams& P) {
     const size_t e = sizeof(T);
-    const int nq = P.nq, nkv = P.nkv, H = B.H, F = B.F;
+    const PBlk& B = a.talker ? P.t : P.c;
+    const int nq = P.nq, nkv = P.nkv, H = B.H, F = B.F, l = a.l;
     const int nqkv = (nq + 2 * nkv) * HD;
+    const int M = (!a.talker && a.s == 0) ? 2 : 1;
+    Word* x = a.talker ? P.x : P.cx;
+    const int xb = a.talker ? BX : BCX;
+    // the token a pass starts from: assembled by the first GEMV that reads it
+    const Tok first_tok = a.talker ? Tok::TALK : (a.s == 0 ? Tok::CP0 : Tok::CPS);
+    const bool proj = P.H != P.Hc;
     Gemv g{};
-    // (token assembly) + RMSNorm + q/k/v projection
-    g.W = (const char*)B.wqkv + (size_t)l * nqkv * H * e; g.N = nqkv; g.K = H; g.M = M;
-    g.pro = Pro::NORM; g.tok = tok; g.epi = Epi::STORE; g.src = x; g.src_ld = H; g.src_buf = xb;
-    g.norm_w = B.attn_norm + (size_t)l * H; g.dst = P.qkv; g.ld_dst = nqkv; g.dst_buf = BQKV; g.s_idx = s_idx;
-    r.gemv(g);
-    // QK-norm, RoPE, cache append, attention
-    r.attention(l, B, M, p0, S, talker);
-    // O projection + residual
-    g = Gemv{};
-    g.W = (const char*)B.wo + (size_t)l * H * nq * HD * e; g.N = H; g.K = nq * HD; g.M = M;
-    g.pro = Pro::LOAD; g.tok = Tok::NONE; g.epi = Epi::ADD; g.src = P.o; g.src_ld = nq * HD; g.src_buf = BO;
-    g.dst = x; g.ld_dst = H; g.dst_buf = xb;
-    r.gemv(g);
-    // RMSNorm + gate/up + SiLU(g)*u
-    g = Gemv{};
-    g.W = (const char*)B.wgu + (size_t)l * 2 * F * H * e; g.N = F; g.K = H; g.M = M; g.gated = true;
-    g.pro = Pro::NORM; g.tok = Tok::NONE; g.epi = Epi::GATED; g.src = x; g.src_ld = H; g.src_buf = xb;
-    g.norm_w = B.mlp_norm + (size_t)l * H; g.dst = P.act; g.ld_dst = F; g.dst_buf = BACT;
-    r.gemv(g);
-    // down projection + residual
-    g = Gemv{};
-    g.W = (const char*)B.wd + (size_t)l * H * F * e; g.N = H; g.K = F; g.M = M;
-    g.pro = Pro::LOAD; g.tok = Tok::NONE; g.epi = Epi::ADD; g.src = P.act; g.src_ld = F; g.src_buf = BACT;
-    g.dst = x; g.ld_dst = H; g.dst_buf = xb;
-    r.gemv(g);
+    g.M = M;
+    g.s_idx = a.talker ? 0 : a.s;
+    switch (a.kind) {
+        case Ph::PROJ:
+            g.W = P.cp_proj_w; g.N = P.Hc; g.K = P.H; g.pro = Pro::RAW; g.tok = first_tok; g.epi = Epi::BIAS;
+            g.bias = P.cp_proj_b; g.dst = P.cx; g.ld_dst = P.Hc; g.dst_buf = BCX;
+            break;
+        case Ph::QKV:
+            // (token assembly) + RMSNorm + q/k/v projection
+            g.W = (const char*)B.wqkv + (size_t)l * nqkv * H * e; g.N = nqkv; g.K = H;
+            g.pro = Pro::NORM; g.tok = (l == 0 && (a.talker || !proj)) ? first_tok : Tok::NONE; g.epi = Epi::STORE;
+            g.src = x; g.src_ld = H; g.src_buf = xb;
+            g.norm_w = B.attn_norm + (size_t)l * H; g.dst = P.qkv; g.ld_dst = nqkv; g.dst_buf = BQKV;
+            break;
+        case Ph::O:
+            // O projection + residual
+            g.W = (const char*)B.wo + (size_t)l * H * nq * HD * e; g.N = H; g.K = nq * HD;
+            g.pro = Pro::LOAD; g.tok = Tok::NONE; g.epi = Epi::ADD; g.src = P.o; g.src_ld = nq * HD; g.src_buf = BO;
+            g.dst = x; g.ld_dst = H; g.dst_buf = xb;
+            break;
+        case Ph::GU:
+            // RMSNorm + gate/up + SiLU(g)*u
+            g.W = (const char*)B.wgu + (size_t)l * 2 * F * H * e; g.N = F; g.K = H; g.gated = true;
+            g.pro = Pro::NORM; g.tok = Tok::NONE; g.epi = Epi::GATED; g.src = x; g.src_ld = H; g.src_buf = xb;
+            g.norm_w = B.mlp_norm + (size_t)l * H; g.dst = P.act; g.ld_dst = F; g.dst_buf = BACT;
+            break;
+        case Ph::DOWN:
+            // down projection + residual
+            g.W = (const char*)B.wd + (size_t)l * H * F * e; g.N = H; g.K = F;
+            g.pro = Pro::LOAD; g.tok = Tok::NONE; g.epi = Epi::ADD; g.src = P.act; g.src_ld = F; g.src_buf = BACT;
+            g.dst = x; g.ld_dst = H; g.dst_buf = xb;
+            break;
+        default:   // HEAD: final norm of the last token -> predictor head[s] / codec head
+            g.M = 1; g.pro = Pro::NORM; g.tok = Tok::NONE; g.epi = Epi::STORE;
+            g.norm_w = B.final_norm; g.src_ld = H;
+            if (a.talker) {
+                g.W = P.codec_head; g.N = P.V; g.K = P.H; g.src = P.x; g.src_buf = BX;
+                g.dst = P.logits; g.ld_dst = P.V; g.dst_buf = BLOG; g.hout = P.h;
+            } else {
+                g.W = (const char*)P.cp_heads + (size_t)a.s * P.cpV * P.Hc * e; g.N = P.cpV; g.K = P.Hc;
+                g.src = P.cx + (size_t)(M - 1) * P.Hc; g.src_buf = BCX;
+                g.dst = P.cpl; g.ld_dst = P.cpV; g.dst_buf = BCPL;
+            }
+            break;
+    }
+    return g;
 }
 
 template <typename T, class R>
-__device__ void frame_schedule(R& r, const FrameParams& P) {
-    const size_t e = sizeof(T);
-    const int G1 = P.G - 1;
-    const bool proj = P.H != P.Hc;
-    // code predictor: tokens [h, codec_emb(code0)] at 0,1, then table[s-1](code_s) at s+1
-    for (int s = 0; s < G1 && r.live(); ++s) {
-        const int M = s == 0 ? 2 : 1;
-        const Tok tok = s == 0 ? Tok::CP0 : Tok::CPS;
-        Tok layer_tok = tok;
-        if (proj) {
-            Gemv g{};
-            g.W = P.cp_proj_w; g.N = P.Hc; g.K = P.H; g.M = M; g.pro = Pro::RAW; g.tok = tok; g.epi = Epi::BIAS;
-            g.bias = P.cp_proj_b; g.dst = P.cx; g.ld_dst = P.Hc; g.dst_buf = BCX; g.s_idx = s;
-            r.gemv(g);
-            layer_tok = Tok::NONE;
+__device__ __forceinline__ void run_phase(R& r, const FrameParams& P, const PhaseAt& a) {
+    switch (a.kind) {
+        case Ph::ATTN: {
+            const bool tk = a.talker;
+            const int M = (!tk && a.s == 0) ? 2 : 1;
+            const int p0 = tk ? r.talker_pos() : (a.s == 0 ? 0 : a.s + 1);
+            r.attention(a.l, tk ? P.t : P.c, M, p0, tk ? P.n_splits : 1, tk);
+            break;
         }
-        for (int l = 0; l < P.c.L && r.live(); ++l)
-            layer<T>(r, P, P.c, l, M, s == 0 ? 0 : s + 1, 1, P.cx, BCX, l == 0 ? layer_tok : Tok::NONE, s, false);
-        // final norm of the last token -> head[s]
-        Gemv g{};
-        g.W = (const char*)P.cp_heads + (size_t)s * P.cpV * P.Hc * e; g.N = P.cpV; g.K = P.Hc; g.M = 1;
-        g.pro = Pro::NORM; g.tok = Tok::NONE; g.epi = Epi::STORE; g.src = P.cx + (size_t)(M - 1) * P.Hc;
-        g.src_ld = P.Hc; g.src_buf = BCX; g.norm_w = P.c.final_norm; g.dst = P.cpl; g.ld_dst = P.cpV;
-        g.dst_buf = BCPL;
-        r.gemv(g);
-        r.draw_cp(s);
+        case Ph::DRAW_CP: r.draw_cp(a.s); break;
+        case Ph::PREP_T: r.prepare_talker(); break;
+        case Ph::DRAW_T: r.draw_talker(); break;
+        default: r.gemv(phase_gemv<T>(a, P)); break;
     }
-    // talker
-    r.prepare_talker();
-    for (int l = 0; l < P.t.L && r.live(); ++l)
-        layer<T>(r, P, P.t, l, 1, r.talker_pos(), P.n_splits, P.x, BX, l == 0 ? Tok::TALK : Tok::NONE, 0, true);
-    Gemv g{};
-    g.W = P.codec_head; g.N = P.V; g.K = P.H; g.M = 1; g.pro = Pro::NORM; g.tok = Tok::NONE; g.epi = Epi::STORE;
-    g.src = P.x; g.src_ld = P.H; g.src_buf = BX; g.norm_w = P.t.final_norm; g.dst = P.logits; g.ld_dst = P.V;
-    g.dst_buf = BLOG; g.hout = P.h;
-    r.gemv(g);
-    r.draw_talker();
+}
+
+// Two walks of the same phase list.  FLAT: one loop, one call site per kind
+// of phase, which keeps the large unrolled FMA rows in the instruction cache
+// (measured on the 1.7B shape: 3.68 -> 3.08 ms per step).  Nested: a call
+// site per phase of a layer, each with its kind known at compile time, so the
+// compiler folds the phase's constants into compact tensor-core row code
+// (measured on the 0.6B shape: 2.37 ms nested, 2.56 ms flat).
+template <typename T, bool FLAT, class R>
+__device__ void frame_schedule(R& r, const FrameParams& P) {
+    if constexpr (FLAT) {
+        const int n = phase_count(P);
+        for (int i = 0; i < n && r.live(); ++i) run_phase<T>(r, P, phase_at(i, P));
+    } else {
+        const bool proj = P.H != P.Hc;
+        for (int s = 0; s < P.G - 1 && r.live(); ++s) {
+            if (proj) run_phase<T>(r, P, PhaseAt{Ph::PROJ, s, 0, false});
+            for (int l = 0; l < P.c.L && r.live(); ++l) {
+                run_phase<T>(r, P, PhaseAt{Ph::QKV, s, l, false});
+                run_phase<T>(r, P, PhaseAt{Ph::ATTN, s, l, false});
+                run_phase<T>(r, P, PhaseAt{Ph::O, s, l, false});
+                run_phase<T>(r, P, PhaseAt{Ph::GU, s, l, false});
+                run_phase<T>(r, P, PhaseAt{Ph::DOWN, s, l, false});
+            }
+            run_phase<T>(r, P, PhaseAt{Ph::HEAD, s, 0, false});
+            run_phase<T>(r, P, PhaseAt{Ph::DRAW_CP, s, 0, false});
+        }
+        run_phase<T>(r, P, PhaseAt{Ph::PREP_T, 0, 0, true});
+        for (int l = 0; l < P.t.L && r.live(); ++l) {
+            run_phase<T>(r, P, PhaseAt{Ph::QKV, 0, l, true});
+            run_phase<T>(r, P, PhaseAt{Ph::ATTN, 0, l, true});
+            run_phase<T>(r, P, PhaseAt{Ph::O, 0, l, true});
+            run_phase<T>(r, P, PhaseAt{Ph::GU, 0, l, true});
+            run_phase<T>(r, P, PhaseAt{Ph::DOWN, 0, l, true});
+        }
+        run_phase<T>(r, P, PhaseAt{Ph::HEAD, 0, 0, true});
+        run_phase<T>(r, P, PhaseAt{Ph::DRAW_T, 0, 0, true});
+    }
 }
 
 template <typename T, int GQ, bool TCR>
@@ -1316,7 +1438,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) frame_kernel(const FrameParams* _
         if ((threadIdx.x & 31) == 0) {
             Producer<T, TCR> pr{s, P};
             pr.pos = pos;
-            frame_schedule<T>(pr, P);
+            frame_schedule<T, !TCR>(pr, P);
             pr.drain();
         }
         return;
@@ -1325,7 +1447,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) frame_kernel(const FrameParams* _
     c.frame = frame;
     c.pos = pos;
     c.base = (unsigned)rs.sel << 10;
-    frame_schedule<T>(c, P);
+    frame_schedule<T, !TCR>(c, P);
 }
 
 // ------------------------------------------------------------------ host side
