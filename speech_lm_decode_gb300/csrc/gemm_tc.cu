@@ -441,7 +441,8 @@ cudaError_t launch_tc(const void* W, int N, int K, const float* X, int ldx, int 
     constexpr int STAGES = stages_for(NT, GATED);
     bf16* hi = (bf16*)tc.base;
     bf16* lo = hi + (size_t)M * K;
-    split_kernel<<<dim3((K + 1023) / 1024, M), 256, 0, st>>>(X, ldx, M, K, hi, lo);
+    // X = NULL: the producer of the operand wrote hi / lo itself
+    if (X) split_kernel<<<dim3((K + 1023) / 1024, M), 256, 0, st>>>(X, ldx, M, K, hi, lo);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap mw, mx, mx2;

@@ -18,10 +18,15 @@ struct TcScratch {
     size_t bytes = 0;
 };
 inline bool tc_fits(const TcScratch& s, int M, int K) { return s.base && (size_t)M * K * 4 <= s.bytes; }
+// true when launch_linear / launch_linear_gated over M tokens of width K take
+// the tensor-core path, whose operand can then be written pre-split (X = NULL)
+bool linear_takes_split(int dtype, int M, int K, const TcScratch& tc);
 
 // Y[m][n] (+)= sum_k W[n][k] X[m][k] (+ bias[n]); W [N][K] in the model dtype,
 // X [M][K] fp32 (leading dimension ldx), Y fp32 (leading dimension ldy).
-// accumulate: add into Y (residual).
+// accumulate: add into Y (residual).  X = NULL: the operand is already in the
+// tensor-core scratch as bf16 high / low parts (only where linear_takes_split;
+// cudaErrorInvalidValue otherwise).
 cudaError_t launch_linear(int dtype, const void* W, int N, int K, const float* X, int ldx, int M, float* Y, int ldy,
                           const float* bias, int accumulate, const TcScratch& tc, int* err, cudaStream_t st);
 // SwiGLU projection: out[m][n] = silu(g) * u with g = W[n].x, u = W[F+n].x,
@@ -41,6 +46,11 @@ void set_tc_min_tokens(int m);
 // row (negative: skip).
 cudaError_t launch_rmsnorm(const float* x, int ldx, int M, const float* w, int n, float eps, float* out, int ldo,
                            float* hout, int ldh, const int* out_row, cudaStream_t st);
+// The same normalized rows written straight into the tensor-core scratch as
+// bf16 high and low parts ([M][n] each: high = bf16(y), low = bf16(y - high)),
+// the operand launch_linear(X = NULL) expects.
+cudaError_t launch_rmsnorm_split(const float* x, int ldx, int M, const float* w, int n, float eps,
+                                 const TcScratch& tc, cudaStream_t st);
 
 // ---------------------------------------------------------------- attention.cu
 // Per token m (row tok_row[m], position tok_pos[m] >= 0): per-head RMSNorm of

@@ -163,10 +163,13 @@ static bool use_tc(int dtype, int M) {
     return dtype == Q3_BF16 && g_tc_min_tokens > 0 && M >= g_tc_min_tokens && tc_available();
 }
 
+bool linear_takes_split(int dtype, int M, int K, const TcScratch& tc) { return use_tc(dtype, M) && tc_fits(tc, M, K); }
+
 cudaError_t launch_linear(int dtype, const void* W, int N, int K, const float* X, int ldx, int M, float* Y, int ldy,
                           const float* bias, int accumulate, const TcScratch& tc, int* err, cudaStream_t st) {
-    if (use_tc(dtype, M) && tc_fits(tc, M, K))
+    if (linear_takes_split(dtype, M, K, tc))
         return launch_linear_tc(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, tc, err, st);
+    if (!X) return cudaErrorInvalidValue;
     if (dtype == Q3_BF16)
         return linear_impl<bf16, false>((const bf16*)W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, st);
     return linear_impl<float, false>((const float*)W, N, K, X, ldx, M, Y, ldy, bias, accumulate, 0, nullptr, 0, st);
@@ -174,17 +177,20 @@ cudaError_t launch_linear(int dtype, const void* W, int N, int K, const float* X
 
 cudaError_t launch_linear_gated(int dtype, const void* W, int F, int K, const float* X, int ldx, int M, float* out,
                                 int ldo, const TcScratch& tc, int* err, cudaStream_t st) {
-    if (use_tc(dtype, M) && tc_fits(tc, M, K))
+    if (linear_takes_split(dtype, M, K, tc))
         return launch_linear_gated_tc(W, F, K, X, ldx, M, out, ldo, tc, err, st);
+    if (!X) return cudaErrorInvalidValue;
     if (dtype == Q3_BF16)
         return linear_impl<bf16, true>((const bf16*)W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, st);
     return linear_impl<float, true>((const float*)W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, st);
 }
 
 // ------------------------------------------------------------------ RMSNorm
+// hi != NULL: the output goes to hi / lo (bf16 parts, row stride n) instead of out
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ x, int ldx, const float* __restrict__ w,
                                                       int n, float eps, float* __restrict__ out, int ldo,
-                                                      float* __restrict__ hout, int ldh, const int* __restrict__ out_row) {
+                                                      float* __restrict__ hout, int ldh, const int* __restrict__ out_row,
+                                                      bf16* __restrict__ hi, bf16* __restrict__ lo) {
     const int m = blockIdx.x;
     const int orow = out_row ? out_row[m] : m;
     if (orow < 0) return;
@@ -204,7 +210,13 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
     const float r = 1.0f / sqrtf(red[0] / (float)n + eps);
     for (int i = threadIdx.x; i < n; i += 256) {
         const float y = xr[i] * r * w[i];
-        out[(size_t)orow * ldo + i] = y;
+        if (hi) {
+            const bf16 h = __float2bfloat16_rn(y);
+            hi[(size_t)orow * n + i] = h;
+            lo[(size_t)orow * n + i] = __float2bfloat16_rn(y - __bfloat162float(h));
+        } else {
+            out[(size_t)orow * ldo + i] = y;
+        }
         if (hout) hout[(size_t)orow * ldh + i] = y;
     }
 }
@@ -212,7 +224,16 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
 cudaError_t launch_rmsnorm(const float* x, int ldx, int M, const float* w, int n, float eps, float* out, int ldo,
                            float* hout, int ldh, const int* out_row, cudaStream_t st) {
     if (M <= 0) return cudaSuccess;
-    rmsnorm_kernel<<<M, 256, 0, st>>>(x, ldx, w, n, eps, out, ldo, hout, ldh, out_row);
+    rmsnorm_kernel<<<M, 256, 0, st>>>(x, ldx, w, n, eps, out, ldo, hout, ldh, out_row, nullptr, nullptr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_split(const float* x, int ldx, int M, const float* w, int n, float eps,
+                                 const TcScratch& tc, cudaStream_t st) {
+    if (M <= 0) return cudaSuccess;
+    if (!tc_fits(tc, M, n)) return cudaErrorInvalidValue;
+    bf16* hi = (bf16*)tc.base;
+    rmsnorm_kernel<<<M, 256, 0, st>>>(x, ldx, w, n, eps, nullptr, 0, nullptr, 0, nullptr, hi, hi + (size_t)M * n);
     return cudaGetLastError();
 }
 

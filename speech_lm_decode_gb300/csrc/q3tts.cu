@@ -255,14 +255,20 @@ int enqueue_layers(q3tts* h, bool talker, int M, float* x, const int* trow, cons
     float* qkv = h->p<float>(h->L.qkv);
     const int splits = talker ? (M <= 2 * c.max_batch ? h->splits_t : 1) : 1;
     const float eps = c.rms_eps;
+    const bool presplit = linear_takes_split(c.dtype, M, H, h->tc());
     for (int l = 0; l < L; ++l) {
         const char* wqkv = (const char*)bw.wqkv + (size_t)l * nqkv * H * e;
         const char* wo = (const char*)bw.wo + (size_t)l * H * nq * hd * e;
         const char* wgu = (const char*)bw.wgu + (size_t)l * 2 * F * H * e;
         const char* wd = (const char*)bw.wd + (size_t)l * H * F * e;
-        CK(launch_rmsnorm(x, H, M, (const float*)bw.attn_norm + (size_t)l * H, H, eps, opA, H, nullptr, 0,
-                          nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
-        CK(launch_linear(c.dtype, wqkv, nqkv, H, opA, H, M, qkv, nqkv, nullptr, 0, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
+        // RMSNorm + q/k/v projection (the norm writes the tensor-core operand directly when that path runs)
+        if (presplit) {
+            CK(launch_rmsnorm_split(x, H, M, (const float*)bw.attn_norm + (size_t)l * H, H, eps, h->tc(), h->st)); debug_wait(h->st, "launch_rmsnorm_split");
+        } else {
+            CK(launch_rmsnorm(x, H, M, (const float*)bw.attn_norm + (size_t)l * H, H, eps, opA, H, nullptr, 0,
+                              nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
+        }
+        CK(launch_linear(c.dtype, wqkv, nqkv, H, presplit ? nullptr : opA, H, M, qkv, nqkv, nullptr, 0, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
         CK(launch_qk_rope_kv(c.dtype, qkv, nqkv, M, nq, nkv, (const float*)bw.q_norm + (size_t)l * hd,
                              (const float*)bw.k_norm + (size_t)l * hd, eps, h->p<float>(h->L.rope), h->L.rope_rows,
                              Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos, h->err(), h->st)); debug_wait(h->st, "launch_qk_rope_kv");
@@ -270,9 +276,13 @@ int enqueue_layers(q3tts* h, bool talker, int M, float* x, const int* trow, cons
                             splits, h->p<float>(h->L.pm), h->p<float>(h->L.pl), h->p<float>(h->L.pacc), opA, nq * hd,
                             h->st)); debug_wait(h->st, "launch_attention");
         CK(launch_linear(c.dtype, wo, H, nq * hd, opA, nq * hd, M, x, H, nullptr, 1, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
-        CK(launch_rmsnorm(x, H, M, (const float*)bw.mlp_norm + (size_t)l * H, H, eps, opA, H, nullptr, 0,
-                          nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
-        CK(launch_linear_gated(c.dtype, wgu, F, H, opA, H, M, opB, F, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear_gated");
+        if (presplit) {
+            CK(launch_rmsnorm_split(x, H, M, (const float*)bw.mlp_norm + (size_t)l * H, H, eps, h->tc(), h->st)); debug_wait(h->st, "launch_rmsnorm_split");
+        } else {
+            CK(launch_rmsnorm(x, H, M, (const float*)bw.mlp_norm + (size_t)l * H, H, eps, opA, H, nullptr, 0,
+                              nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
+        }
+        CK(launch_linear_gated(c.dtype, wgu, F, H, presplit ? nullptr : opA, H, M, opB, F, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear_gated");
         CK(launch_linear(c.dtype, wd, H, F, opB, F, M, x, H, nullptr, 1, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
     }
     return Q3_OK;
