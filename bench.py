@@ -45,6 +45,33 @@ def parse():
     return p.parse_args()
 
 
+# ---------------------------------------------------------------- ranks
+def job_totals(max_vals, sum_vals, device="cpu"):
+    """Whole-job figures of an N-rank run: the maximum over ranks of each entry
+    of max_vals (times) and the sum over ranks of each entry of sum_vals
+    (frames).  Without an initialised process group (one rank) the values come
+    back unchanged.  device: where the reduction tensors live (the rank's GPU
+    for NCCL, "cpu" for gloo)."""
+    max_vals, sum_vals = [float(v) for v in max_vals], [float(v) for v in sum_vals]
+    try:
+        import torch
+        import torch.distributed as dist
+    except ImportError:
+        return max_vals, sum_vals
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return max_vals, sum_vals
+    t_max = torch.tensor(max_vals or [0.0], dtype=torch.float64, device=device)
+    t_sum = torch.tensor(sum_vals or [0.0], dtype=torch.float64, device=device)
+    dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t_sum, op=dist.ReduceOp.SUM)
+    return t_max.tolist()[:len(max_vals)], t_sum.tolist()[:len(sum_vals)]
+
+
+def job_rate(frames_all: float, seconds_max: float) -> float:
+    """Frames of all ranks over the slowest rank's time."""
+    return frames_all / seconds_max if seconds_max > 0 else 0.0
+
+
 # ---------------------------------------------------------------- byte model
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 
@@ -154,8 +181,10 @@ def peaks():
 
 
 # ---------------------------------------------------------------- oracle (CPU baseline / reference arm)
-def oracle_rate(wl, w, inp, n_frames):
-    """Oracle frames/s on row 0 of the workload: prefill (untimed), then n_frames steps."""
+def oracle_rate(wl, w, inp, n_frames, warm_frames=0):
+    """Oracle frames/s on row 0 of the workload: prefill and warm_frames steps
+    (untimed), then n_frames timed steps.  Returns (rate, timed frames, seconds,
+    warm frames run)."""
     import oracle
     rows = [0]
     lens = [wl.prompt_lens[0]]
@@ -165,12 +194,16 @@ def oracle_rate(wl, w, inp, n_frames):
     o = oracle.Oracle(wl.dims, wl.dtype, w, 1, wl.max_ctx, T, capture=False)
     o.prefill(inp["prompt"][po[0]:po[1]], np.array([0, lens[0]], np.int32), inp["text"][to[0]:to[1]],
               np.array([0, to[1] - to[0]], np.int32), inp["tts_pad"], [wl.rows[0]], rows)
-    n = min(n_frames, T)
+    warm = max(0, min(warm_frames, T - 1))
+    if warm:
+        o.step(warm)
+    warm_done = int(o.get("frames")[0])
+    n = max(1, min(n_frames, T - warm))
     t0 = time.perf_counter()
     o.step(n)
     dt = time.perf_counter() - t0
-    done = int(o.get("frames")[0])
-    return done / dt, done, dt
+    done = int(o.get("frames")[0]) - warm_done
+    return done / dt, done, dt, warm
 
 
 def omp_threads():
@@ -249,13 +282,7 @@ def run_ours(args, wl, rank, world):
             steps_done += n
             timed_steps += n
             remaining -= n
-    times = torch.tensor([total_ms, float(total_frames), float(timed_steps)], dtype=torch.float64, device=dev)
-    if world > 1:
-        t = times.clone()
-        torch.distributed.all_reduce(t[0:1], op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.all_reduce(t[1:2], op=torch.distributed.ReduceOp.SUM)
-        times = t
-    max_ms, all_frames = float(times[0]), float(times[1])
+    (max_ms,), (all_frames,) = job_totals([total_ms], [total_frames], dev)
     res = dict(ms=max_ms, frames=all_frames, local_frames=total_frames, steps=timed_steps,
                wbytes=wbytes_total, kvbytes=kvbytes_total, kernels_per_step=kernels_per_step,
                clocks=clocks.summary(), local_ms=total_ms)
@@ -280,7 +307,9 @@ def run_ours(args, wl, rank, world):
         barrier()
         e2e_s = time.perf_counter() - t0
         in_bytes = inp["prompt"].nbytes + inp["text"].nbytes + inp["tts_pad"].nbytes
-        res["e2e"] = dict(frames=int(fr.sum()), seconds=e2e_s, steps=nsteps,
+        # whole job: every rank's frames over the slowest rank's time
+        (e2e_s,), (e2e_frames,) = job_totals([e2e_s], [int(fr.sum())], dev)
+        res["e2e"] = dict(frames=e2e_frames, seconds=e2e_s, steps=nsteps,
                           h2d_per_step=in_bytes / nsteps,
                           d2h_per_step=wl.batch * wl.dims.n_groups * 4 + wl.batch * ROWSTATE_BYTES + 16)
     q.close()
@@ -306,10 +335,11 @@ def main():
         w = synth.make_weights(wl.dims, wl.dtype, wl.weight_seed)
         inp = synth.make_inputs(wl)
         n = max(1, min(args.steps, 40))
-        rate, done, dt = oracle_rate(wl, w, inp, n)
-        sample = f"row 0 of the workload, {done} frames after its prefill (untimed), {dt:.1f} s"
+        rate, done, dt, warm = oracle_rate(wl, w, inp, n, warm_frames=min(args.warmup, 8))
+        sample = (f"row 0 of the workload, {done} frames after its prefill and {warm} warm-up frames (untimed), "
+                  f"{dt:.1f} s")
         line = {"impl": "reference", "metric": metric, "value": rate, "unit": unit, "n_gpus": args.gpus,
-                "steps": done, "warmup": 0, "ms_per_step": 1000.0 * dt / max(done, 1), "higher_is_better": True,
+                "steps": done, "warmup": warm, "ms_per_step": 1000.0 * dt / max(done, 1), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded random init)",
                 "config": config,
                 "cpu_baseline": {"value": rate, "unit": unit, "cores": omp_threads(), "kind": "oracle",
@@ -329,7 +359,7 @@ def main():
         return
     pk, pk_kind = peaks()
     sec = res["ms"] / 1000.0
-    value = res["frames"] / sec
+    value = job_rate(res["frames"], sec)
     bytes_total = res["wbytes"] + res["kvbytes"]
     achieved = bytes_total / (res["local_ms"] / 1000.0) / 1e9
     # at batch 1 one launch of the frame kernel is the whole step
@@ -349,12 +379,12 @@ def main():
             "clocks": res["clocks"]}
     if "e2e" in res:
         e = res["e2e"]
-        line["e2e"] = {"value": e["frames"] / e["seconds"], "unit": unit,
+        line["e2e"] = {"value": job_rate(e["frames"], e["seconds"]), "unit": unit,
                        "h2d_bytes_per_step": e["h2d_per_step"], "d2h_bytes_per_step": e["d2h_per_step"],
                        "note": "prefill from pinned host + one q3tts_step_frames(1) per step, codes to pinned host"}
     if not args.no_cpu_baseline and world == 1:
         n = args.cpu_frames or (20 if wl.dims.hidden <= 1024 else 10)
-        rate, done, dt = oracle_rate(wl, w, inp, n)
+        rate, done, dt, _ = oracle_rate(wl, w, inp, n)
         line["cpu_baseline"] = {"value": rate, "unit": unit, "cores": omp_threads(), "kind": "oracle",
                                 "sample": f"row 0, {done} frames after prefill, {dt:.1f} s"}
     print(json.dumps(line))
