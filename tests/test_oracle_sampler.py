@@ -233,3 +233,55 @@ def test_same_seed_same_draws_and_seed_matters():
     b = [oracle.sample(lg, s1, True, frame=f)[1] for f in range(200)]
     c = [oracle.sample(lg, s2, True, frame=f)[1] for f in range(200)]
     assert a == b and a != c
+
+
+def _cp_draws(lg, n, **kw):
+    s = sp(do_sample=1, cp_do_sample=1, **{k: v for k, v in kw.items()},
+           **{"cp_" + k: v for k, v in kw.items()})
+    out = []
+    for f in range(n):
+        err, idx, _, _ = oracle.sample(lg, s, talker=False, eos=-1, sup_lo=0, sup_hi=0, row=2, frame=f, step=5)
+        assert err == 0
+        out.append(idx)
+    return out
+
+
+def test_degenerate_settings_reduce_to_greedy():
+    """top-k 1 on a unique maximum, or a top-p below the largest probability,
+    leaves only the argmax: every draw is the greedy choice.  With a tie at the
+    top, top-k 1 keeps both tied ids (ties at the k-th value are kept) while a
+    tiny top-p keeps only the first in (value desc, index asc) order."""
+    rng = np.random.default_rng(11)
+    lg = rng.standard_normal(64).astype(np.float32)
+    lg[17] = lg.max() + 0.25
+    greedy = oracle.sample(lg, sp(), talker=False, eos=-1, sup_lo=0, sup_hi=0)[1]
+    assert greedy == 17
+    assert set(_cp_draws(lg, 300, temperature=1.3, top_k=1, top_p=1.0)) == {17}
+    assert set(_cp_draws(lg, 300, temperature=0.8, top_k=0, top_p=1e-4)) == {17}
+    lg[40] = lg[17]                    # tie at the top
+    assert oracle.sample(lg, sp(), talker=False, eos=-1, sup_lo=0, sup_hi=0)[1] == 17
+    assert set(_cp_draws(lg, 300, temperature=1.3, top_k=1, top_p=1.0)) == {17, 40}
+    assert set(_cp_draws(lg, 300, temperature=0.8, top_k=0, top_p=1e-4)) == {17}
+
+
+def test_unbounded_settings_keep_everything():
+    """top-k >= V and top-p = 1 keep the whole vocabulary: over many draws on
+    near-flat logits every id shows up, exactly as with both filters off."""
+    lg = np.linspace(0.0, 0.05, 16).astype(np.float32)
+    a = _cp_draws(lg, 2000, temperature=1.0, top_k=16, top_p=1.0)
+    b = _cp_draws(lg, 2000, temperature=1.0, top_k=0, top_p=1.0)
+    c = _cp_draws(lg, 2000, temperature=1.0, top_k=1000, top_p=1.0)
+    assert set(a) == set(range(16))
+    assert a == b == c      # the same noise and the same kept set give the same ids
+
+
+def test_top_p_keeps_the_smallest_prefix():
+    """Softmax mass 0.45 on id 2, 0.44 on id 7, 0.011 on each of the other ten:
+    top-p 0.4 keeps only id 2 (the mass before id 7 is 0.45 >= 0.4), top-p 0.5
+    keeps ids 2 and 7 (0.45 < 0.5; the mass before the next is 0.89), and the
+    rest never appear."""
+    p = np.full(12, 0.011)
+    p[2], p[7] = 0.45, 0.44
+    lg = np.log(p).astype(np.float32)
+    assert set(_cp_draws(lg, 400, temperature=1.0, top_k=0, top_p=0.4)) == {2}
+    assert set(_cp_draws(lg, 400, temperature=1.0, top_k=0, top_p=0.5)) == {2, 7}
