@@ -187,7 +187,12 @@ int q3tts_set_capture(q3tts_t* h, int n_rows, const int32_t* rows, float* talker
                       int max_frames);
 
 /* The logits processors and draw on caller-given logits, for testing the
- * sampler bit for bit (same kernel as the frame loop).
+ * sampler bit for bit (same kernel as the frame loop).  The chain and its
+ * order: repetition penalty over the row's drawn ids, EOS masked while
+ * k < min_new_tokens, suppression of [suppress_lo, suppress_hi) except EOS,
+ * then greedy or temperature -> top-k -> top-p -> argmax(p / Exp(1))
+ * (ncnn discussion 6832 §3.2 logits processors; "Qwen3-TTS 移植 ncnn 简明教程"
+ * §1 fact 3 and §6 processor order; Mizuoto page 速度 for the draw).
  *   n               logit sets
  *   logits          [n][V] f32 device; V = codec_vocab if talker else cp_vocab
  *   talker          1: talker chain (penalty, min_new, suppression) then draw;
