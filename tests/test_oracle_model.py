@@ -360,6 +360,31 @@ def test_rows_are_independent_and_forced_eos(tiny_weights):
         assert np.array_equal(alone.get("codes")[0], full.get("codes")[r])
 
 
+def test_degenerate_rows(tiny_weights):
+    """Rows at the edges of the loop, in one batch: a one-row prompt, EOS
+    forced at selection 0 (the row ends with no frame: one selection, no
+    predictor run, every code -1), max_frames = 1 (two selections, one
+    predictor run, finish reason length) and no trailing text (tts_pad from
+    the first step).  Each equals its own single-row run."""
+    kw = dict(do_sample=1, temperature=1.0, top_k=0, top_p=1.0, cp_do_sample=1, min_new_tokens=20)
+    rows = [RowSampling(max_frames=6, **kw), RowSampling(max_frames=6, force_eos_at_frame=0, **kw),
+            RowSampling(max_frames=1, **kw), RowSampling(max_frames=6, **kw)]
+    wl = Workload("edges", TINY, F32, 9, 4, [1, 5, 3, 4], [2, 2, 2, 0], 6, rows, 16, norm_std=0.1)
+    inp = synth.make_inputs(wl)
+    o = oracle.run(wl, tiny_weights, inp, capture=False)
+    frames, reason = o.get("frames"), o.get("reason")
+    sel, runs, codes = o.get("selections"), o.get("predictor_runs"), o.get("codes")
+    assert frames[0] == 6 and reason[0] == oracle.REASON_LENGTH and sel[0] == 7 and runs[0] == 6
+    assert frames[1] == 0 and reason[1] == oracle.REASON_EOS and sel[1] == 1 and runs[1] == 0
+    assert np.all(codes[1] == -1)
+    assert frames[2] == 1 and reason[2] == oracle.REASON_LENGTH and sel[2] == 2 and runs[2] == 1
+    assert np.all(codes[2, 1:] == -1) and np.all(codes[2, 0] >= 0)
+    assert frames[3] == 6 and reason[3] == oracle.REASON_LENGTH
+    for r in range(4):
+        alone = oracle.run(wl, tiny_weights, inp, rows=[r], capture=False)
+        assert np.array_equal(alone.get("codes")[0], codes[r]), r
+
+
 def test_teacher_forcing_reproduces_free_run(tiny_weights):
     wl = _tiny_wl(8, min_new_tokens=20)
     inp = synth.make_inputs(wl)
