@@ -41,6 +41,8 @@ def parse():
     p.add_argument("--workload", type=int, default=2)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--step-path", default="auto", choices=["auto", "graph", "frame", "cluster"],
+                   help="batch-1 step path (the library's default when auto)")
     p.add_argument("--cpu-frames", type=int, default=0, help="oracle frames timed for the CPU baseline (0: auto)")
     return p.parse_args()
 
@@ -221,7 +223,10 @@ def run_ours(args, wl, rank, world):
     inp = synth.make_inputs(wl)
     dw = q3.to_device_weights(w, dev)
     stream = torch.cuda.Stream(dev)
-    q = q3.Q3TTS(wl.dims, wl.dtype, dw, wl.batch, wl.max_ctx, max(max(wl.n_text), 1), stream=stream)
+    path = {"auto": q3.Q3_PATH_AUTO, "graph": q3.Q3_PATH_GRAPH, "frame": q3.Q3_PATH_FRAME,
+            "cluster": q3.Q3_PATH_CLUSTER}[args.step_path]
+    q = q3.Q3TTS(wl.dims, wl.dtype, dw, wl.batch, wl.max_ctx, max(max(wl.n_text), 1), stream=stream,
+                 step_path=path)
     d_inp = {k: (torch.from_numpy(v).to(dev) if k in ("prompt", "text", "tts_pad") else v) for k, v in inp.items()}
     codes_dev = torch.empty((wl.batch, wl.frames, wl.dims.n_groups), dtype=torch.int32, device=dev)
     lens = np.array(wl.prompt_lens)

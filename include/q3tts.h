@@ -85,7 +85,30 @@ typedef struct {
     int max_batch;      /* rows per handle                                     */
     int max_ctx;        /* talker positions per row (prompt + frames)          */
     int max_text;       /* trailing text rows per row                          */
+    /* Execution choices (all explicit; 0 selects the documented default).    */
+    int step_path;      /* batch-1 step: Q3_PATH_AUTO (the single-launch frame
+                           kernel where the shape allows, else per-layer
+                           kernels), or one path forced: Q3_PATH_GRAPH,
+                           Q3_PATH_FRAME, Q3_PATH_CLUSTER (create fails with
+                           Q3_ERR_ARG if it cannot serve)                      */
+    int tc_min_tokens;  /* tokens from which projections run as tcgen05 GEMMs
+                           (0: 16; negative: never)                            */
+    int debug_sync;     /* 1: wait for every launch outside graph capture and
+                           report it on stderr (diagnostics, slow)             */
+    int wait_limit_us;  /* bound of every device-side wait of the batch-1
+                           kernels, microseconds (0: 2,000,000)                */
+    int inject_timeout; /* test only (0 = off): the cluster kernel's
+                           cross-cluster exchange with this index is never
+                           written by CTA 0, so every wait on it runs out and
+                           the step returns Q3_ERR_TIMEOUT                     */
 } q3tts_config;
+
+/* step_path values */
+#define Q3_PATH_AUTO     0
+#define Q3_PATH_GRAPH    1  /* per-layer kernels replayed as a CUDA graph        */
+#define Q3_PATH_FRAME    2  /* one cooperative launch, epoch-tagged exchange words */
+#define Q3_PATH_CLUSTER  3  /* one cooperative launch of 8 x 8 thread-block
+                               clusters (one per KV head)                         */
 
 /* One decoder stack (talker or predictor), layer-stacked, device pointers.
  * Norm weights are fp32; matrices are in the config dtype. */
@@ -204,7 +227,9 @@ int q3tts_set_capture(q3tts_t* h, int n_rows, const int32_t* rows, float* talker
  *   step            noise step (0 talker, q = 1..15 predictor codebook)
  *   noise_row       [n] host: row index of the noise counter
  *   ids_out         [n] int32 host
- * Errors: Q3_ERR_NAN (ids_out of a NaN set is -1), Q3_ERR_ARG, Q3_ERR_CUDA. */
+ * Errors: Q3_ERR_NAN (ids_out of a NaN set is -1), Q3_ERR_ARG (also: a set
+ * that samples with temperature <= 0, or a talker set with repetition_penalty
+ * <= 0; nothing is run), Q3_ERR_CUDA. */
 int q3tts_sample_logits(q3tts_t* h, int n, const float* logits, int talker, const q3tts_sampling* params,
                         const uint8_t* seen, const int32_t* sel_index, int step, const int32_t* noise_row,
                         int32_t* ids_out);
@@ -229,8 +254,9 @@ int q3tts_sample_logits(q3tts_t* h, int n, const float* logits, int talker, cons
  * The first call on each device looks the array's address up, so make that
  * first call before any stream capture.  Every call reuses the same array:
  * calls that overlap on the GPU (other streams, other threads) race and must
- * be serialised by the caller.  Errors: Q3_ERR_CAPACITY, Q3_ERR_ARG,
- * Q3_ERR_NAN, Q3_ERR_CUDA. */
+ * be serialised by the caller.  Errors: Q3_ERR_CAPACITY, Q3_ERR_ARG (as in
+ * q3tts_sample_logits, including the per-set settings), Q3_ERR_NAN,
+ * Q3_ERR_CUDA. */
 int q3tts_sample_logits_noalloc(int n, int vocab, const float* logits, int talker, const q3tts_sampling* params,
                                 const uint8_t* seen, const int32_t* sel_index, int step, const int32_t* noise_row,
                                 int eos_id, int suppress_lo, int suppress_hi, int32_t* ids_out, void* stream);
@@ -239,6 +265,11 @@ int q3tts_sample_logits_noalloc(int n, int vocab, const float* logits, int talke
  * kernel nodes of the step's CUDA graph, which this call records if needed).
  * Errors: Q3_ERR_STATE (no prefill), Q3_ERR_CUDA. */
 int q3tts_step_kernel_count(q3tts_t* h, int* count);
+
+/* The path that runs one talker step of a batch of `batch` rows on this
+ * handle: Q3_PATH_CLUSTER, Q3_PATH_FRAME (batch 1 only) or Q3_PATH_GRAPH.
+ * Errors: Q3_ERR_ARG (NULL pointer, batch outside 1..max_batch). */
+int q3tts_step_path(const q3tts_t* h, int batch, int* path);
 
 /* One-line description of the last error on this handle. */
 const char* q3tts_last_error(const q3tts_t* h);

@@ -18,10 +18,12 @@ LIB_PATH = os.path.join(_HERE, "libq3tts.so")
 Q3_OK, Q3_ERR_ARG, Q3_ERR_CUDA, Q3_ERR_CAPACITY, Q3_ERR_STATE, Q3_ERR_NAN, Q3_ERR_TIMEOUT, Q3_ERR_BOUNDS = range(8)
 Q3_F32, Q3_BF16 = 0, 1
 Q3_RUNNING, Q3_FINISHED_EOS, Q3_FINISHED_LENGTH, Q3_FINISHED_ERROR = 0, 1, 2, 3
+Q3_PATH_AUTO, Q3_PATH_GRAPH, Q3_PATH_FRAME, Q3_PATH_CLUSTER = 0, 1, 2, 3
+PATH_NAMES = {Q3_PATH_GRAPH: "graph", Q3_PATH_FRAME: "frame", Q3_PATH_CLUSTER: "cluster"}
 
 EXPORTS = ("q3tts_workspace_bytes", "q3tts_create", "q3tts_prefill", "q3tts_step_frames", "q3tts_set_capture",
-           "q3tts_sample_logits", "q3tts_sample_logits_noalloc", "q3tts_step_kernel_count", "q3tts_last_error",
-           "q3tts_destroy")
+           "q3tts_sample_logits", "q3tts_sample_logits_noalloc", "q3tts_step_kernel_count", "q3tts_step_path",
+           "q3tts_last_error", "q3tts_destroy")
 
 
 class Q3Error(RuntimeError):
@@ -35,7 +37,11 @@ class Config(ctypes.Structure):
                                             "codec_vocab", "cp_layers", "cp_hidden", "cp_ffn", "cp_vocab",
                                             "n_groups", "eos_id", "suppress_lo", "suppress_hi")] + \
               [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)] + \
-              [(n, ctypes.c_int) for n in ("dtype", "max_batch", "max_ctx", "max_text")]
+              [(n, ctypes.c_int) for n in ("dtype", "max_batch", "max_ctx", "max_text", "step_path", "tc_min_tokens",
+                                           "debug_sync", "wait_limit_us", "inject_timeout")]
+
+# execution fields of the config (everything else comes from the model dims)
+EXEC_FIELDS = ("step_path", "tc_min_tokens", "debug_sync", "wait_limit_us", "inject_timeout")
 
 
 class BlockWeights(ctypes.Structure):
@@ -77,6 +83,7 @@ def lib():
         L.q3tts_set_capture.argtypes = [vp, i32, vp, vp, vp, i32]
         L.q3tts_sample_logits.argtypes = [vp, i32, vp, i32, vp, vp, vp, i32, vp, vp]
         L.q3tts_step_kernel_count.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+        L.q3tts_step_path.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int)]
         L.q3tts_sample_logits_noalloc.argtypes = [i32, i32, vp, i32, vp, vp, vp, i32, vp, i32, i32, i32, vp, vp]
         L.q3tts_last_error.restype = ctypes.c_char_p
         L.q3tts_last_error.argtypes = [vp]
@@ -85,10 +92,16 @@ def lib():
     return _lib
 
 
-def make_config(dims, dtype: int, max_batch: int, max_ctx: int, max_text: int) -> Config:
+def make_config(dims, dtype: int, max_batch: int, max_ctx: int, max_text: int, **exec_opts) -> Config:
+    """exec_opts: step_path, tc_min_tokens, debug_sync, wait_limit_us, inject_timeout (default 0)."""
+    unknown = set(exec_opts) - set(EXEC_FIELDS)
+    if unknown:
+        raise ValueError(f"unknown config options {sorted(unknown)}")
     c = Config()
     for f, _ in Config._fields_:
-        if f == "dtype":
+        if f in EXEC_FIELDS:
+            setattr(c, f, int(exec_opts.get(f, 0)))
+        elif f == "dtype":
             c.dtype = dtype
         elif f == "max_batch":
             c.max_batch = max_batch
@@ -148,11 +161,11 @@ class Q3TTS:
     """One handle: model weights (borrowed device tensors), a workspace and a stream."""
 
     def __init__(self, dims, dtype: int, device_weights: dict, max_batch: int, max_ctx: int, max_text: int,
-                 stream=None):
+                 stream=None, **exec_opts):
         import torch
         self._dw = device_weights
         self.dims, self.dtype = dims, dtype
-        self.cfg = make_config(dims, dtype, max_batch, max_ctx, max_text)
+        self.cfg = make_config(dims, dtype, max_batch, max_ctx, max_text, **exec_opts)
         nbytes = lib().q3tts_workspace_bytes(ctypes.byref(self.cfg))
         if nbytes == 0:
             raise Q3Error(Q3_ERR_ARG, "invalid configuration")
@@ -212,6 +225,12 @@ class Q3TTS:
             return out, frames, reasons
         return rc, out, frames, reasons
 
+    def step_path(self, batch: int) -> int:
+        """Q3_PATH_CLUSTER / Q3_PATH_FRAME / Q3_PATH_GRAPH: what runs a step of `batch` rows."""
+        p = ctypes.c_int(0)
+        self._check(lib().q3tts_step_path(self.h, batch, ctypes.byref(p)))
+        return p.value
+
     def step_kernel_count(self) -> int:
         n = ctypes.c_int(0)
         self._check(lib().q3tts_step_kernel_count(self.h, ctypes.byref(n)))
@@ -250,10 +269,21 @@ def sample_logits_noalloc(logits, talker: bool, params, sel_index, step: int, no
     seen ([n, V] uint8, optional) must already be CUDA tensors.  Returns the
     ids (host numpy).  Calls that overlap on the GPU race (one shared staging
     area per device)."""
+    import torch
+    # the library reads n * V * 4 bytes at logits and n * V at seen on the GPU,
+    # and n entries of each host array: check all of it before passing pointers
+    if not (isinstance(logits, torch.Tensor) and logits.is_cuda and logits.dtype == torch.float32 and
+            logits.dim() == 2 and logits.is_contiguous()):
+        raise ValueError("logits must be a contiguous 2-D float32 CUDA tensor")
     n, V = int(logits.shape[0]), int(logits.shape[1])
-    sp = (Sampling * max(n, 1))(*[make_sampling(r) for r in params])
+    if seen is not None and not (isinstance(seen, torch.Tensor) and seen.is_cuda and seen.dtype == torch.uint8 and
+                                 seen.is_contiguous() and tuple(seen.shape) == (n, V)):
+        raise ValueError("seen must be None or a contiguous [n, V] uint8 CUDA tensor")
     sel = np.ascontiguousarray(sel_index, dtype=np.int32)
     nr = np.ascontiguousarray(noise_row, dtype=np.int32)
+    if len(params) != n or sel.shape != (n,) or nr.shape != (n,):
+        raise ValueError("params, sel_index and noise_row must have one entry per logit set")
+    sp = (Sampling * max(n, 1))(*[make_sampling(r) for r in params])
     ids = np.full(max(n, 1), -1, np.int32)
     st = None if stream is None else stream.cuda_stream
     rc = lib().q3tts_sample_logits_noalloc(n, V, _ptr(logits), int(talker), ctypes.cast(sp, ctypes.c_void_p),

@@ -10,7 +10,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libq3tts.so")
-SOURCES = ["linear.cu", "gemm_tc.cu", "attention.cu", "sampler.cu", "loop.cu", "persist.cu", "q3tts.cu", "noalloc.cu"]
+SOURCES = ["linear.cu", "gemm_tc.cu", "attention.cu", "sampler.cu", "loop.cu", "persist.cu", "cluster_step.cu", "q3tts.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include"), "-I" + CSRC]

@@ -19,6 +19,7 @@ constexpr int SEEN_WORDS = MAX_VOCAB / 32;
 constexpr int ERRB_NAN = 1;
 constexpr int ERRB_BOUNDS = 2;
 constexpr int ERRB_TIMEOUT = 4;
+constexpr int ERRB_LAUNCH = 8;   // a kernel found itself launched in a shape it cannot serve
 
 // Per-row decode state, resident in the workspace.
 struct RowState {

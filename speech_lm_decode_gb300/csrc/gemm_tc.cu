@@ -45,7 +45,6 @@ constexpr int stages_for(int nt, bool gated) {
     return st > 8 ? 8 : st;
 }
 constexpr long long TC_WAIT_LIMIT = 2000000000LL;
-constexpr int kSMs = 148;      // CTAs for about one wave (one 192 KB CTA per SM)
 
 __device__ __forceinline__ uint32_t s_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -393,7 +392,7 @@ int cluster_capacity(int ks) {
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, (void*)umma_linear_kernel<NT, GATED, STAGES>, &cfg) != cudaSuccess) {
             cudaGetLastError();
-            n = ks == 1 ? kSMs : 0;
+            n = ks == 1 ? device_sm_count() : 0;
         }
         cap[ks] = n > 0 ? n : -1;
     }
@@ -403,7 +402,7 @@ int cluster_capacity(int ks) {
 // Resident CTAs of this kernel at once (1 CTA per SM: ~192 KB of shared memory).
 template <int NT, bool GATED>
 int resident_ctas(int ks) {
-    return ks == 1 ? kSMs : cluster_capacity<NT, GATED>(ks) * ks;
+    return ks == 1 ? device_sm_count() : cluster_capacity<NT, GATED>(ks) * ks;
 }
 
 // Cost of an NT-wide tile shape split ks ways: each CTA streams its operand

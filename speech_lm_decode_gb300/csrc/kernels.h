@@ -10,12 +10,23 @@ namespace q3 {
 
 struct RowState;
 
+// SMs of the current device (looked up once per device).
+int device_sm_count();
+
+// The draw settings every selection needs: temperature > 0 where the draw
+// samples, and (talker chain) a positive repetition penalty.
+inline bool sampling_ok(const q3tts_sampling& s, bool talker) {
+    if (talker) return (!s.do_sample || s.temperature > 0.f) && s.repetition_penalty > 0.f;
+    return !s.cp_do_sample || s.cp_temperature > 0.f;
+}
+
 // ---------------------------------------------------------------- linear.cu
 // Scratch of the tensor-core path: the fp32 operand split into bf16 high and
 // low parts ([M][K] each).
 struct TcScratch {
     void* base = nullptr;
     size_t bytes = 0;
+    int min_tokens = 16;   // tokens from which the tensor-core path runs (<= 0: never)
 };
 inline bool tc_fits(const TcScratch& s, int M, int K) { return s.base && (size_t)M * K * 4 <= s.bytes; }
 // true when launch_linear / launch_linear_gated over M tokens of width K take
@@ -39,8 +50,6 @@ cudaError_t launch_linear_tc(const void* W, int N, int K, const float* X, int ld
                              const float* bias, int accumulate, const TcScratch& tc, int* err, cudaStream_t st);
 cudaError_t launch_linear_gated_tc(const void* W, int F, int K, const float* X, int ldx, int M, float* out, int ldo,
                                    const TcScratch& tc, int* err, cudaStream_t st);
-// minimum token count for the tensor-core path (0 disables it)
-void set_tc_min_tokens(int m);
 // out[row(m)] = x[m] * rsqrt(mean(x[m]^2) + eps) * w; optionally hout (a
 // second copy).  out_row: NULL = identity, else the output row of each input
 // row (negative: skip).

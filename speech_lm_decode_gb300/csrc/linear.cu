@@ -138,7 +138,7 @@ static cudaError_t linear_impl(const T* W, int N, int K, const float* X, int ldx
     if (M <= 0 || N <= 0) return cudaSuccess;
     if (M <= 8) {
         // rows per warp: 2 when there are enough rows to cover the GPU twice over
-        const bool two = (N >= 4 * 2 * 152 * 2);
+        const bool two = (N >= 4 * 2 * device_sm_count() * 2);
         const int rows_per_block = 4 * (two ? 2 : 1);
         dim3 grid((N + rows_per_block - 1) / rows_per_block);
 #define GEMV_CASE(MM)                                                                                           \
@@ -157,13 +157,23 @@ static cudaError_t linear_impl(const T* W, int N, int K, const float* X, int ldx
     return cudaGetLastError();
 }
 
-static int g_tc_min_tokens = 16;
-void set_tc_min_tokens(int m) { g_tc_min_tokens = m; }
-static bool use_tc(int dtype, int M) {
-    return dtype == Q3_BF16 && g_tc_min_tokens > 0 && M >= g_tc_min_tokens && tc_available();
+int device_sm_count() {
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    if (!cache[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 1;
+    }
+    return cache[dev];
 }
 
-bool linear_takes_split(int dtype, int M, int K, const TcScratch& tc) { return use_tc(dtype, M) && tc_fits(tc, M, K); }
+static bool use_tc(int dtype, int M, const TcScratch& tc) {
+    return dtype == Q3_BF16 && tc.min_tokens > 0 && M >= tc.min_tokens && tc_available();
+}
+
+bool linear_takes_split(int dtype, int M, int K, const TcScratch& tc) { return use_tc(dtype, M, tc) && tc_fits(tc, M, K); }
 
 cudaError_t launch_linear(int dtype, const void* W, int N, int K, const float* X, int ldx, int M, float* Y, int ldy,
                           const float* bias, int accumulate, const TcScratch& tc, int* err, cudaStream_t st) {

@@ -72,6 +72,8 @@ extern "C" int q3tts_sample_logits_noalloc(int n, int vocab, const float* logits
         return Q3_ERR_ARG;
     if (talker && (eos_id < 0 || eos_id >= vocab || suppress_lo < 0 || suppress_hi > vocab || suppress_lo > suppress_hi))
         return Q3_ERR_ARG;
+    for (int i = 0; i < n; ++i)
+        if (!sampling_ok(params[i], talker != 0)) return Q3_ERR_ARG;
     NoAllocScratch* s = nullptr;
     if (scratch_for_current_device(&s) != cudaSuccess) return Q3_ERR_CUDA;
     cudaStream_t st = (cudaStream_t)stream;

@@ -13,6 +13,7 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include "common.cuh"
+#include "cluster_step.h"
 #include "frame_params.h"
 #include "kernels.h"
 
@@ -28,7 +29,8 @@ constexpr int MIN_SAMPLE_SETS = 256; // staging for q3tts_sample_logits
 struct Layout {
     size_t kvK, kvV, ckvK, ckvV, rope, rows, params, h, x, cx, tok, opA, opB, headop, qkv, pm, pl, pacc, logits,
         cplogits, t_row, t_pos, c_row, c_pos, last_row, codes, codes_stage, text, pad, err, s_params, s_logits, s_sel, s_row, s_ids, s_seen, cap_slot,
-        fparams, fctl, fpart, fll, tcs;
+        fparams, fctl, fpart, fll, tcs, clpack, clxr, cllg, clparams;
+    bool cl;                            // the cluster step kernel's regions are present
     size_t total;
     int mmax, kA, kB, rope_rows, frames_cap, n_sets, vmax, fsplits;
     size_t fll_words;                   // exchange words of the frame kernel
@@ -115,6 +117,15 @@ Layout make_layout(const q3tts_config& c) {
     }
     // tensor-core path: bf16 high / low parts of an fp32 operand [mmax][kmax]
     L.tcs = c.dtype == Q3_BF16 ? take((size_t)L.mmax * std::max(L.kA, L.kB) * 4) : take(256);
+    // cluster step kernel (batch 1): packed weight image, exchange words, parameters
+    L.cl = c.step_path == Q3_PATH_CLUSTER && cl_unsupported(c)[0] == 0;
+    if (L.cl) {
+        const ClLayout cl = cl_layout(c);
+        L.clpack = take(cl.pack_bytes);
+        L.clxr = take(cl.xr_words * sizeof(Word));
+        L.cllg = take(cl.lg_words * sizeof(Word));
+        L.clparams = take(sizeof(ClParams));
+    }
     L.total = off;
     return L;
 }
@@ -139,6 +150,10 @@ bool config_ok(const q3tts_config* c, std::string* why) {
     if (c->dtype != Q3_F32 && c->dtype != Q3_BF16) return bad("dtype must be Q3_F32 or Q3_BF16");
     if (c->max_batch < 1 || c->max_ctx < 2 || c->max_text < 0) return bad("bad max_batch / max_ctx / max_text");
     if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return bad("bad rms_eps / rope_theta");
+    if (c->step_path < Q3_PATH_AUTO || c->step_path > Q3_PATH_CLUSTER) return bad("step_path out of range");
+    if (c->wait_limit_us < 0 || c->inject_timeout < 0 || c->debug_sync < 0 || c->debug_sync > 1)
+        return bad("bad wait_limit_us / inject_timeout / debug_sync");
+    if (c->step_path == Q3_PATH_CLUSTER && cl_unsupported(*c)[0] != 0) return bad("cluster kernel: unsupported shape");
     return true;
 }
 
@@ -166,6 +181,7 @@ struct q3tts {
     int cap_T = 0;
     bool capturing = false;
     int splits_t = 1;
+    bool cl_ok = false;         // the cluster step kernel serves batch 1
     bool frame_ok = false;      // the persistent frame kernel can serve batch 1
     bool frame_tc = false;      // ... with its GEMV rows on the tensor cores
     size_t frame_smem = 0;
@@ -178,6 +194,7 @@ struct q3tts {
         TcScratch t;
         t.base = c.dtype == Q3_BF16 ? p<void>(L.tcs) : nullptr;
         t.bytes = c.dtype == Q3_BF16 ? (size_t)L.mmax * std::max(L.kA, L.kB) * 4 : 0;
+        t.min_tokens = c.tc_min_tokens == 0 ? 16 : c.tc_min_tokens;
         return t;
     }
     RowState* rows() const { return p<RowState>(L.rows); }
@@ -204,12 +221,12 @@ int fail(q3tts* h, int code, const char* fmt, ...) {
         if (e_ != cudaSuccess) return fail(h, Q3_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
     } while (0)
 
-// Opt-in launch-by-launch check (Q3TTS_DEBUG_SYNC=1): outside graph capture,
-// wait up to 20 s for each launch, report it on stderr, and end the process if
-// it did not finish (the driver then tears the context down).
-bool g_debug_sync = false;
-void debug_wait(cudaStream_t st, const char* what) {
-    if (!g_debug_sync) return;
+// Opt-in launch-by-launch check (config debug_sync = 1): outside graph
+// capture, wait up to 20 s for each launch, report it on stderr, and end the
+// process if it did not finish (the driver then tears the context down).
+void debug_wait(const q3tts* h, const char* what) {
+    if (!h->c.debug_sync) return;
+    cudaStream_t st = h->st;
     cudaStreamCaptureStatus cs;
     if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone) return;
     const auto t0 = std::chrono::steady_clock::now();
@@ -263,27 +280,27 @@ int enqueue_layers(q3tts* h, bool talker, int M, float* x, const int* trow, cons
         const char* wd = (const char*)bw.wd + (size_t)l * H * F * e;
         // RMSNorm + q/k/v projection (the norm writes the tensor-core operand directly when that path runs)
         if (presplit) {
-            CK(launch_rmsnorm_split(x, H, M, (const float*)bw.attn_norm + (size_t)l * H, H, eps, h->tc(), h->st)); debug_wait(h->st, "launch_rmsnorm_split");
+            CK(launch_rmsnorm_split(x, H, M, (const float*)bw.attn_norm + (size_t)l * H, H, eps, h->tc(), h->st)); debug_wait(h, "launch_rmsnorm_split");
         } else {
             CK(launch_rmsnorm(x, H, M, (const float*)bw.attn_norm + (size_t)l * H, H, eps, opA, H, nullptr, 0,
-                              nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
+                              nullptr, h->st)); debug_wait(h, "launch_rmsnorm");
         }
-        CK(launch_linear(c.dtype, wqkv, nqkv, H, presplit ? nullptr : opA, H, M, qkv, nqkv, nullptr, 0, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
+        CK(launch_linear(c.dtype, wqkv, nqkv, H, presplit ? nullptr : opA, H, M, qkv, nqkv, nullptr, 0, h->tc(), h->err(), h->st)); debug_wait(h, "launch_linear");
         CK(launch_qk_rope_kv(c.dtype, qkv, nqkv, M, nq, nkv, (const float*)bw.q_norm + (size_t)l * hd,
                              (const float*)bw.k_norm + (size_t)l * hd, eps, h->p<float>(h->L.rope), h->L.rope_rows,
-                             Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos, h->err(), h->st)); debug_wait(h->st, "launch_qk_rope_kv");
+                             Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos, h->err(), h->st)); debug_wait(h, "launch_qk_rope_kv");
         CK(launch_attention(c.dtype, qkv, nqkv, M, nq, nkv, Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos,
                             splits, h->p<float>(h->L.pm), h->p<float>(h->L.pl), h->p<float>(h->L.pacc), opA, nq * hd,
-                            h->st)); debug_wait(h->st, "launch_attention");
-        CK(launch_linear(c.dtype, wo, H, nq * hd, opA, nq * hd, M, x, H, nullptr, 1, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
+                            h->st)); debug_wait(h, "launch_attention");
+        CK(launch_linear(c.dtype, wo, H, nq * hd, opA, nq * hd, M, x, H, nullptr, 1, h->tc(), h->err(), h->st)); debug_wait(h, "launch_linear");
         if (presplit) {
-            CK(launch_rmsnorm_split(x, H, M, (const float*)bw.mlp_norm + (size_t)l * H, H, eps, h->tc(), h->st)); debug_wait(h->st, "launch_rmsnorm_split");
+            CK(launch_rmsnorm_split(x, H, M, (const float*)bw.mlp_norm + (size_t)l * H, H, eps, h->tc(), h->st)); debug_wait(h, "launch_rmsnorm_split");
         } else {
             CK(launch_rmsnorm(x, H, M, (const float*)bw.mlp_norm + (size_t)l * H, H, eps, opA, H, nullptr, 0,
-                              nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
+                              nullptr, h->st)); debug_wait(h, "launch_rmsnorm");
         }
-        CK(launch_linear_gated(c.dtype, wgu, F, H, presplit ? nullptr : opA, H, M, opB, F, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear_gated");
-        CK(launch_linear(c.dtype, wd, H, F, opB, F, M, x, H, nullptr, 1, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
+        CK(launch_linear_gated(c.dtype, wgu, F, H, presplit ? nullptr : opA, H, M, opB, F, h->tc(), h->err(), h->st)); debug_wait(h, "launch_linear_gated");
+        CK(launch_linear(c.dtype, wd, H, F, opB, F, M, x, H, nullptr, 1, h->tc(), h->err(), h->st)); debug_wait(h, "launch_linear");
     }
     return Q3_OK;
 }
@@ -293,18 +310,22 @@ int enqueue_cp_input(q3tts* h, int M) {
     const q3tts_config& c = h->c;
     if (c.hidden == c.cp_hidden) return Q3_OK;  // tokens were written to cx directly
     CK(launch_linear(c.dtype, h->w.cp_proj_w, c.cp_hidden, c.hidden, h->p<float>(h->L.tok), c.hidden, M,
-                     h->p<float>(h->L.cx), c.cp_hidden, (const float*)h->w.cp_proj_b, 0, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
+                     h->p<float>(h->L.cx), c.cp_hidden, (const float*)h->w.cp_proj_b, 0, h->tc(), h->err(), h->st)); debug_wait(h, "launch_linear");
     return Q3_OK;
 }
 
 // One talker step for the whole batch: complete frame k-1 through the code
 // predictor, assemble the next talker input, run the talker, select code0.
 int enqueue_frame(q3tts* h) {
-    CK(launch_frame(h->c.dtype, h->frame_tc, h->p<FrameParams>(h->L.fparams), h->frame_grid, h->frame_smem, h->st)); debug_wait(h->st, "launch_frame");
+    CK(launch_frame(h->c.dtype, h->frame_tc, h->p<FrameParams>(h->L.fparams), h->frame_grid, h->frame_smem, h->st)); debug_wait(h, "launch_frame");
     return Q3_OK;
 }
 
 int enqueue_step(q3tts* h) {
+    if (h->batch == 1 && h->cl_ok) {
+        CK(launch_cluster_step(h->p<ClParams>(h->L.clparams), h->st)); debug_wait(h, "launch_cluster_step");
+        return Q3_OK;
+    }
     if (h->batch == 1 && h->frame_ok) return enqueue_frame(h);
     const q3tts_config& c = h->c;
     const int B = h->batch, G1 = c.n_groups - 1;
@@ -323,45 +344,45 @@ int enqueue_step(q3tts* h) {
     const int* slot = h->p<int>(h->L.cap_slot);
     int r;
 
-    CK(launch_prepare_step(rs, B, t_row, t_pos, c_row, c_pos, G1, h->st)); debug_wait(h->st, "launch_prepare_step");
+    CK(launch_prepare_step(rs, B, t_row, t_pos, c_row, c_pos, G1, h->st)); debug_wait(h, "launch_prepare_step");
     // code predictor: 2-token prefill -> head[0] -> codebook 1
     CK(launch_cp_embed_prefill(c.dtype, rs, B, h->p<float>(h->L.h), h->w.codec_emb, c.hidden, c.codec_vocab, codes,
-                               h->L.frames_cap, tok, h->err(), h->st)); debug_wait(h->st, "launch_cp_embed_prefill");
+                               h->L.frames_cap, tok, h->err(), h->st)); debug_wait(h, "launch_cp_embed_prefill");
     if ((r = enqueue_cp_input(h, 2 * B))) return r;
     if ((r = enqueue_layers(h, false, 2 * B, cx, c_row, c_pos))) return r;
     CK(launch_rmsnorm(cx + c.cp_hidden, 2 * c.cp_hidden, B, (const float*)h->w.cp.final_norm, c.cp_hidden,
-                      c.rms_eps, opA, c.cp_hidden, nullptr, 0, nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
+                      c.rms_eps, opA, c.cp_hidden, nullptr, 0, nullptr, h->st)); debug_wait(h, "launch_rmsnorm");
     CK(launch_linear(c.dtype, h->w.cp_heads, c.cp_vocab, c.cp_hidden, opA, c.cp_hidden, B, cpl, c.cp_vocab, nullptr,
-                     0, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
+                     0, h->tc(), h->err(), h->st)); debug_wait(h, "launch_linear");
     CK(launch_cp_sample(cpl, c.cp_vocab, B, rs, P, 0, codes, h->L.frames_cap, h->err(), h->cap_c, slot, h->cap_T,
-                        c.n_groups, h->st)); debug_wait(h->st, "launch_cp_sample");
+                        c.n_groups, h->st)); debug_wait(h, "launch_cp_sample");
     // 14 autoregressive steps: table[s-1](code s) at position s+1 -> head[s] -> codebook s+1
     for (int s = 1; s < G1; ++s) {
         CK(launch_cp_embed_step(c.dtype, rs, B, h->w.cp_emb, c.hidden, c.cp_vocab, s, codes, h->L.frames_cap, tok,
-                                h->err(), h->st)); debug_wait(h->st, "launch_cp_embed_step");
+                                h->err(), h->st)); debug_wait(h, "launch_cp_embed_step");
         if ((r = enqueue_cp_input(h, B))) return r;
         if ((r = enqueue_layers(h, false, B, cx, c_row + (size_t)s * 2 * B, c_pos + (size_t)s * 2 * B))) return r;
         CK(launch_rmsnorm(cx, c.cp_hidden, B, (const float*)h->w.cp.final_norm, c.cp_hidden, c.rms_eps, opA,
-                          c.cp_hidden, nullptr, 0, nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
+                          c.cp_hidden, nullptr, 0, nullptr, h->st)); debug_wait(h, "launch_rmsnorm");
         const char* head = (const char*)h->w.cp_heads + (size_t)s * c.cp_vocab * c.cp_hidden * e;
         CK(launch_linear(c.dtype, head, c.cp_vocab, c.cp_hidden, opA, c.cp_hidden, B, cpl, c.cp_vocab, nullptr, 0,
-                         h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
+                         h->tc(), h->err(), h->st)); debug_wait(h, "launch_linear");
         CK(launch_cp_sample(cpl, c.cp_vocab, B, rs, P, s, codes, h->L.frames_cap, h->err(), h->cap_c, slot, h->cap_T,
-                            c.n_groups, h->st)); debug_wait(h->st, "launch_cp_sample");
+                            c.n_groups, h->st)); debug_wait(h, "launch_cp_sample");
     }
     // talker step
     float* x = h->p<float>(h->L.x);
     CK(launch_talker_embed(c.dtype, rs, B, h->w.codec_emb, h->w.cp_emb, c.hidden, c.codec_vocab, c.cp_vocab,
                            c.n_groups, codes, h->L.frames_cap, h->p<float>(h->L.text), h->p<float>(h->L.pad), x,
-                           c.eos_id, h->err(), h->st)); debug_wait(h->st, "launch_talker_embed");
+                           c.eos_id, h->err(), h->st)); debug_wait(h, "launch_talker_embed");
     if ((r = enqueue_layers(h, true, B, x, t_row, t_pos))) return r;
     CK(launch_rmsnorm(x, c.hidden, B, (const float*)h->w.talker.final_norm, c.hidden, c.rms_eps, opA,
-                      c.hidden, h->p<float>(h->L.h), c.hidden, nullptr, h->st)); debug_wait(h->st, "launch_rmsnorm");
+                      c.hidden, h->p<float>(h->L.h), c.hidden, nullptr, h->st)); debug_wait(h, "launch_rmsnorm");
     float* logits = h->p<float>(h->L.logits);
     CK(launch_linear(c.dtype, h->w.codec_head, c.codec_vocab, c.hidden, opA, c.hidden, B, logits, c.codec_vocab,
-                     nullptr, 0, h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
+                     nullptr, 0, h->tc(), h->err(), h->st)); debug_wait(h, "launch_linear");
     CK(launch_talker_sample(logits, c.codec_vocab, B, rs, P, c.eos_id, c.suppress_lo, c.suppress_hi, 1, h->err(),
-                            h->cap_t, slot, h->cap_T, h->st)); debug_wait(h->st, "launch_talker_sample");
+                            h->cap_t, slot, h->cap_T, h->st)); debug_wait(h, "launch_talker_sample");
     return Q3_OK;
 }
 
@@ -383,8 +404,45 @@ int record_step_graph(q3tts* h) {
     return Q3_OK;
 }
 
+// Parameters of the cluster step kernel (device copy in the workspace).
+int upload_cluster_params(q3tts* h) {
+    const q3tts_config& c = h->c;
+    ClParams P{};
+    P.pack = h->p<unsigned char>(h->L.clpack);
+    P.lay = cl_layout(c);
+    const q3tts_block_weights& t = h->w.talker;
+    const q3tts_block_weights& k = h->w.cp;
+    P.t_attn_norm = (const float*)t.attn_norm; P.t_q_norm = (const float*)t.q_norm; P.t_k_norm = (const float*)t.k_norm;
+    P.t_mlp_norm = (const float*)t.mlp_norm; P.t_final_norm = (const float*)t.final_norm;
+    P.c_attn_norm = (const float*)k.attn_norm; P.c_q_norm = (const float*)k.q_norm; P.c_k_norm = (const float*)k.k_norm;
+    P.c_mlp_norm = (const float*)k.mlp_norm; P.c_final_norm = (const float*)k.final_norm;
+    P.codec_emb = h->w.codec_emb; P.cp_emb = h->w.cp_emb; P.cp_proj_b = (const float*)h->w.cp_proj_b;
+    P.H = c.hidden; P.Hc = c.cp_hidden; P.F = c.ffn; P.Fc = c.cp_ffn; P.Lt = c.n_layers; P.Lc = c.cp_layers;
+    P.V = c.codec_vocab; P.cpV = c.cp_vocab; P.G = c.n_groups; P.eos = c.eos_id; P.sup_lo = c.suppress_lo;
+    P.sup_hi = c.suppress_hi; P.max_batch = c.max_batch; P.cap = c.max_ctx;
+    P.eps = c.rms_eps;
+    P.rope = h->p<float2>(h->L.rope);
+    P.Kc = h->p<void>(h->L.kvK); P.Vc = h->p<void>(h->L.kvV);
+    P.rows = h->rows(); P.P = h->p<q3tts_sampling>(h->L.params);
+    P.xr = h->p<Word>(h->L.clxr); P.lg = h->p<Word>(h->L.cllg);
+    P.h = h->p<float>(h->L.h);
+    P.codes = h->p<int32_t>(h->L.codes); P.frames_cap = h->L.frames_cap;
+    P.text = h->p<float>(h->L.text); P.pad = h->p<float>(h->L.pad);
+    P.ctl = h->p<unsigned>(h->L.fctl); P.err = h->err();
+    P.cap_t = h->cap_t; P.cap_c = h->cap_c; P.cap_slot = h->p<int>(h->L.cap_slot); P.cap_T = h->cap_T;
+    P.wait_ns = (long long)(c.wait_limit_us > 0 ? c.wait_limit_us : 2000000) * 1000;
+    P.inject_skip = c.inject_timeout > 0 ? c.inject_timeout : -1;
+    CK(cudaMemcpyAsync(h->p<ClParams>(h->L.clparams), &P, sizeof P, cudaMemcpyHostToDevice, h->st));
+    CK(cudaStreamSynchronize(h->st));
+    return Q3_OK;
+}
+
 // Parameters of the persistent frame kernel (device copy in the workspace).
 int upload_frame_params(q3tts* h) {
+    if (h->cl_ok) {
+        int r = upload_cluster_params(h);
+        if (r) return r;
+    }
     if (!h->frame_ok) return Q3_OK;
     const q3tts_config& c = h->c;
     FrameParams P{};
@@ -428,6 +486,7 @@ int read_errors(q3tts* h, const int* err_host) {
     if (err_host[0] & ERRB_BOUNDS) return fail(h, Q3_ERR_BOUNDS, "device bounds check failed (id or position)");
     if (err_host[0] & ERRB_NAN) return fail(h, Q3_ERR_NAN, "NaN or +inf logits at a selection");
     if (err_host[0] & ERRB_TIMEOUT) return fail(h, Q3_ERR_TIMEOUT, "a device wait timed out");
+    if (err_host[0] & ERRB_LAUNCH) return fail(h, Q3_ERR_CUDA, "the cluster step kernel was not launched as 8 x 8 clusters");
     return Q3_OK;
 }
 
@@ -494,8 +553,15 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
         // long weight slices and are bandwidth-bound
         h->frame_tc = tc_shape;
         h->frame_smem = frame_smem_bytes(cfg->dtype, h->frame_xin, h->frame_tc);
-        const char* env = getenv("Q3TTS_FRAME_KERNEL");
-        const bool want = !(env && env[0] == '0');
+        const int path = cfg->step_path;
+        // the cluster step kernel: shape supported, regions laid out, 8 x 8 clusters co-resident
+        if (L.cl && coop && cl_setup() == cudaSuccess) {
+            h->cl_ok = cl_pack_weights(*cfg, *w, h->p<unsigned char>(L.clpack), h->st) == cudaSuccess &&
+                       cudaStreamSynchronize(h->st) == cudaSuccess;
+        }
+        cudaGetLastError();
+        if (path == Q3_PATH_CLUSTER && !h->cl_ok) { q3tts_destroy(h); return Q3_ERR_ARG; }
+        const bool want = path == Q3_PATH_FRAME || path == Q3_PATH_AUTO;
         h->frame_ok = want && coop && sms >= cfg->n_kv_heads && h->frame_smem > 0 && tiles_fit &&
                       cfg->cp_vocab <= FRAME_CP_VMAX &&
                       cfg->n_q_heads == 2 * cfg->n_kv_heads;
@@ -536,15 +602,12 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
         const int per_split = (int)(tile / (2 * HD * e));
         h->frame_splits = std::max(1, std::min((cfg->max_ctx + per_split - 1) / per_split,
                                                std::min(16, std::max(1, grid / cfg->n_kv_heads))));
-        const char* ds = getenv("Q3TTS_DEBUG_SYNC");
-        g_debug_sync = ds && ds[0] == '1';
-        const char* tc = getenv("Q3TTS_TENSOR_CORES");
-        set_tc_min_tokens(tc && tc[0] == '0' ? 0 : 16);
+        if (path == Q3_PATH_FRAME && !h->frame_ok) { q3tts_destroy(h); return Q3_ERR_ARG; }
     }
     // split-KV partitions of the talker decode attention: enough blocks to fill
     // the GPU twice at small batch, one split at large batch
     const int blocks = cfg->max_batch * cfg->n_kv_heads;
-    int s = std::min((cfg->max_ctx + 31) / 32, (2 * 152 + blocks - 1) / blocks);
+    int s = std::min((cfg->max_ctx + 31) / 32, (2 * device_sm_count() + blocks - 1) / blocks);
     h->splits_t = std::max(1, std::min(s, MAX_SPLITS));
     // RoPE table: cos, sin of pos * inv_freq_j, inv_freq_j = theta^(-2j/128) in
     // fp32 and the angle formed in fp32 (inv_freq kept fp32 in bf16 models).
@@ -635,11 +698,16 @@ int q3tts_prefill(q3tts_t* h, int batch, const float* prompt, const int32_t* pro
     CK(cudaMemsetAsync(h->p<int32_t>(h->L.codes), 0xFF,
                        (size_t)c.max_batch * h->L.frames_cap * MAX_GROUPS * sizeof(int32_t), h->st));
     CK(cudaMemsetAsync(h->err(), 0, 4 * sizeof(int), h->st));
-    if (h->frame_ok) {
+    if (h->frame_ok || h->cl_ok) {
         // exchange words start at epoch 0 (never a live epoch); abort flag and
         // split counters start at 0
         CK(cudaMemsetAsync(h->p<Word>(h->L.fll), 0, h->L.fll_words * sizeof(Word), h->st));
         CK(cudaMemsetAsync(h->p<unsigned>(h->L.fctl), 0, FRAME_CTL_WORDS * sizeof(unsigned), h->st));
+    }
+    if (h->cl_ok) {
+        const ClLayout cl = cl_layout(c);
+        CK(cudaMemsetAsync(h->p<Word>(h->L.clxr), 0, cl.xr_words * sizeof(Word), h->st));
+        CK(cudaMemsetAsync(h->p<Word>(h->L.cllg), 0, cl.lg_words * sizeof(Word), h->st));
     }
 
     // prompt through the talker, in chunks of whole tokens across rows
@@ -666,16 +734,16 @@ int q3tts_prefill(q3tts_t* h, int batch, const float* prompt, const int32_t* pro
         int r = enqueue_layers(h, true, M, x, h->p<int>(h->L.t_row), h->p<int>(h->L.t_pos));
         if (r) return r;
         CK(launch_rmsnorm(x, H, M, (const float*)h->w.talker.final_norm, H, c.rms_eps, headop, H,
-                          h->p<float>(h->L.h), H, h->p<int>(h->L.last_row), h->st)); debug_wait(h->st, "launch_rmsnorm");
+                          h->p<float>(h->L.h), H, h->p<int>(h->L.last_row), h->st)); debug_wait(h, "launch_rmsnorm");
         // the host vectors are reused by the next chunk: let this chunk's copies finish
         CK(cudaStreamSynchronize(h->st));
     }
     float* logits = h->p<float>(h->L.logits);
     CK(launch_linear(c.dtype, h->w.codec_head, c.codec_vocab, H, headop, H, batch, logits, c.codec_vocab, nullptr, 0,
-                     h->tc(), h->err(), h->st)); debug_wait(h->st, "launch_linear");
+                     h->tc(), h->err(), h->st)); debug_wait(h, "launch_linear");
     CK(launch_talker_sample(logits, c.codec_vocab, batch, h->rows(), h->p<q3tts_sampling>(h->L.params), c.eos_id,
                             c.suppress_lo, c.suppress_hi, 0, h->err(), h->cap_t, h->p<int>(h->L.cap_slot), h->cap_T,
-                            h->st)); debug_wait(h->st, "launch_talker_sample");
+                            h->st)); debug_wait(h, "launch_talker_sample");
     int err_host[4];
     CK(cudaMemcpyAsync(err_host, h->err(), sizeof err_host, cudaMemcpyDeviceToHost, h->st));
     CK(cudaMemcpyAsync(rs.data(), h->rows(), rs.size() * sizeof(RowState), cudaMemcpyDeviceToHost, h->st));
@@ -711,14 +779,14 @@ int q3tts_step_frames(q3tts_t* h, int n_frames, int32_t* codes_out, int32_t* fra
         const int G = c.n_groups;
         if (dev) {
             CK(launch_pack_codes(h->p<int32_t>(h->L.codes), h->L.frames_cap, f0, n_frames, G, B, codes_out,
-                                 (long)n_frames * G, h->st)); debug_wait(h->st, "launch_pack_codes");
+                                 (long)n_frames * G, h->st)); debug_wait(h, "launch_pack_codes");
         } else {
             // through the staging area, at most frames_cap frames at a time
             for (long j0 = 0; j0 < n_frames; j0 += h->L.frames_cap) {
                 const long nc = std::min((long)h->L.frames_cap, n_frames - j0);
                 int32_t* stage = h->p<int32_t>(h->L.codes_stage);
                 CK(launch_pack_codes(h->p<int32_t>(h->L.codes), h->L.frames_cap, f0 + j0, (int)nc, G, B, stage,
-                                     nc * G, h->st)); debug_wait(h->st, "launch_pack_codes");
+                                     nc * G, h->st)); debug_wait(h, "launch_pack_codes");
                 CK(cudaMemcpy2DAsync(codes_out + j0 * G, (size_t)n_frames * G * sizeof(int32_t), stage,
                                      (size_t)nc * G * sizeof(int32_t), (size_t)nc * G * sizeof(int32_t), B,
                                      cudaMemcpyDeviceToHost, h->st));
@@ -767,6 +835,9 @@ int q3tts_sample_logits(q3tts_t* h, int n, const float* logits, int talker, cons
     if (n < 0 || n > h->L.n_sets) return fail(h, Q3_ERR_ARG, "n must be in 0..%d", h->L.n_sets);
     if (n == 0) return Q3_OK;
     if (!logits || !params || !sel_index || !noise_row || !ids_out) return fail(h, Q3_ERR_ARG, "NULL argument");
+    for (int i = 0; i < n; ++i)
+        if (!sampling_ok(params[i], talker != 0))
+            return fail(h, Q3_ERR_ARG, "set %d: temperature must be > 0 when sampling, repetition_penalty > 0", i);
     const int V = talker ? c.codec_vocab : c.cp_vocab;
     float* lg = h->p<float>(h->L.s_logits);
     uint8_t* sn = seen ? h->p<uint8_t>(h->L.s_seen) : nullptr;
@@ -780,12 +851,18 @@ int q3tts_sample_logits(q3tts_t* h, int n, const float* logits, int talker, cons
     CK(cudaMemsetAsync(serr, 0, sizeof(int), h->st));
     CK(launch_sample_sets(lg, n, V, talker, sp, sn, h->p<int>(h->L.s_sel), step,
                           h->p<int>(h->L.s_row), c.eos_id, c.suppress_lo, c.suppress_hi, h->p<int>(h->L.s_ids),
-                          serr, h->st)); debug_wait(h->st, "launch_sample_sets");
+                          serr, h->st)); debug_wait(h, "launch_sample_sets");
     int err_host[4] = {0, 0, 0, 0};
     CK(cudaMemcpyAsync(ids_out, h->p<int>(h->L.s_ids), (size_t)n * sizeof(int), cudaMemcpyDefault, h->st));
     CK(cudaMemcpyAsync(err_host, serr, sizeof(int), cudaMemcpyDeviceToHost, h->st));
     CK(cudaStreamSynchronize(h->st));
     return read_errors(h, err_host);
+}
+
+int q3tts_step_path(const q3tts_t* h, int batch, int* path) {
+    if (!h || !path || batch < 1 || batch > h->c.max_batch) return Q3_ERR_ARG;
+    *path = batch == 1 && h->cl_ok ? Q3_PATH_CLUSTER : batch == 1 && h->frame_ok ? Q3_PATH_FRAME : Q3_PATH_GRAPH;
+    return Q3_OK;
 }
 
 int q3tts_step_kernel_count(q3tts_t* h, int* count) {

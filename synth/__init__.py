@@ -124,6 +124,11 @@ DIMS_17B = Dims(hidden=2048, ffn=6144)
 DIMS_SMALL = Dims(n_layers=2, hidden=256, ffn=384, codec_vocab=96, cp_layers=2, cp_hidden=256,
                   cp_ffn=320, cp_vocab=64, n_groups=4, eos_id=80, suppress_lo=64, suppress_hi=96)
 DIMS_SMALL_PROJ = dataclasses.replace(DIMS_SMALL, hidden=384, ffn=512)
+# Small shapes the batch-1 cluster kernel serves (8 clusters x 8 CTAs: widths in
+# multiples of 128, FFN in multiples of 512, vocabularies in multiples of 1024).
+DIMS_CL = Dims(n_layers=2, hidden=256, ffn=512, codec_vocab=1024, cp_layers=2, cp_hidden=256, cp_ffn=512,
+               cp_vocab=1024, n_groups=4, eos_id=1000, suppress_lo=960, suppress_hi=1024)
+DIMS_CL_PROJ = dataclasses.replace(DIMS_CL, hidden=512, ffn=1024)
 
 
 @dataclasses.dataclass

@@ -24,9 +24,12 @@ class GpuRun:
     talker_logits: np.ndarray   # [n_cap, T+1, V]
     cp_logits: np.ndarray       # [n_cap, T, G-1, cpV]
     cap_rows: list
+    path: int = 0               # step path that ran (Q3_PATH_*)
 
 
-def run_gpu(wl, dev_weights, inputs, cap_rows, chunks=None):
+def run_gpu(wl, dev_weights, inputs, cap_rows, chunks=None, expect_path=None, **exec_opts):
+    """exec_opts: config execution fields (step_path, ...); expect_path: the
+    batch-1 step path the handle must report (checked when given)."""
     import torch
     import speech_lm_decode_gb300 as q3
     d = wl.dims
@@ -38,8 +41,11 @@ def run_gpu(wl, dev_weights, inputs, cap_rows, chunks=None):
     def log(msg):
         if verbose:
             print(f"[run_gpu] {msg}", file=sys.stderr, flush=True)
-    q = q3.Q3TTS(d, wl.dtype, dev_weights, wl.batch, wl.max_ctx, max(max(wl.n_text), 1))
+    q = q3.Q3TTS(d, wl.dtype, dev_weights, wl.batch, wl.max_ctx, max(max(wl.n_text), 1), **exec_opts)
     log("handle created")
+    path = q.step_path(wl.batch)
+    if expect_path is not None:
+        assert path == expect_path, (q3.PATH_NAMES.get(path), q3.PATH_NAMES.get(expect_path))
     tl = torch.full((len(cap_rows), T + 1, d.codec_vocab), float("nan"), device="cuda")
     cl = torch.full((len(cap_rows), max(T, 1), d.n_groups - 1, d.cp_vocab), float("nan"), device="cuda")
     q.set_capture(cap_rows, tl, cl, T)
@@ -54,7 +60,7 @@ def run_gpu(wl, dev_weights, inputs, cap_rows, chunks=None):
         parts.append(c)
     codes = np.concatenate(parts, axis=1)
     torch.cuda.synchronize()
-    out = GpuRun(code0, codes, frames, reasons, tl.cpu().numpy(), cl.cpu().numpy(), list(cap_rows))
+    out = GpuRun(code0, codes, frames, reasons, tl.cpu().numpy(), cl.cpu().numpy(), list(cap_rows), path)
     q.close()
     return out
 

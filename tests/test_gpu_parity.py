@@ -1,6 +1,5 @@
 """GPU parity of the frame loop against the oracle, through the C ABI."""
 import dataclasses
-import os
 
 import numpy as np
 import pytest
@@ -102,10 +101,15 @@ def test_full_size_workload(q3, idx):
     w = synth.make_weights(wl.dims, wl.dtype, wl.weight_seed)
     inp = synth.make_inputs(wl)
     rows = [0] if wl.batch == 1 else [0, wl.batch - 1]
-    g = run_gpu(wl, q3.to_device_weights(w), inp, cap_rows=rows)
+    # batch 1 runs on the single-launch frame kernel (what the benchmark times)
+    expect = q3.Q3_PATH_FRAME if wl.batch == 1 else q3.Q3_PATH_GRAPH
+    g = run_gpu(wl, q3.to_device_weights(w), inp, cap_rows=rows, expect_path=expect)
     check_run_properties(wl, g)
     s = compare(wl, w, inp, g, upto=40 if wl.batch > 32 else None)
     s.pop("details", None)
+    # most decisions are far from a tie: a margin that collapsed toward zero
+    # would leave the codes unchecked
+    assert s["checked"] >= 0.5 * s["decisions"], s
     print(f"workload {idx}: frames {g.frames[rows].tolist()} reasons {g.reasons[rows].tolist()} {s}")
 
 
@@ -153,35 +157,87 @@ def _single_inputs(inp, r):
 @pytest.mark.parametrize("path", ["frame", "graph"])
 @pytest.mark.parametrize("dims,dtype", [(synth.DIMS_SMALL, BF16), (synth.DIMS_SMALL, F32),
                                         (synth.DIMS_SMALL_PROJ, BF16)])
-def test_batch1_paths_parity(q3, monkeypatch, dims, dtype, path):
-    """Batch 1 runs on the persistent frame kernel (one launch per step); the
-    multi-kernel path is forced with Q3TTS_FRAME_KERNEL=0.  Both match the oracle."""
-    if path == "graph":
-        monkeypatch.setenv("Q3TTS_FRAME_KERNEL", "0")
-    else:
-        monkeypatch.delenv("Q3TTS_FRAME_KERNEL", raising=False)
+def test_batch1_paths_parity(q3, dims, dtype, path):
+    """Batch 1 on the single-launch frame kernel (epoch-tagged exchange words)
+    and on the per-layer kernels, each forced through the config; both match
+    the oracle."""
+    p = q3.Q3_PATH_FRAME if path == "frame" else q3.Q3_PATH_GRAPH
     wl = small_workload(dims, dtype, frames=10)
     w = small_weights(wl)
     inp = synth.make_inputs(wl)
     dw = q3.to_device_weights(w)
     for r in range(wl.batch):
         wl1, inp1 = _single_row(wl, r), _single_inputs(inp, r)
-        g = run_gpu(wl1, dw, inp1, cap_rows=[0])
-        dump = os.environ.get("Q3TTS_DUMP")
-        if dump:
-            np.savez(f"{dump}_{path}_{dtype}_{r}.npz", codes=g.codes, frames=g.frames, reasons=g.reasons,
-                     tl=g.talker_logits, cl=g.cp_logits)
+        g = run_gpu(wl1, dw, inp1, cap_rows=[0], step_path=p, expect_path=p)
         compare(wl1, w, inp1, g)
 
 
-def test_frame_kernel_chunked_and_repeatable(q3, monkeypatch):
-    monkeypatch.delenv("Q3TTS_FRAME_KERNEL", raising=False)
+def test_frame_kernel_chunked_and_repeatable(q3):
     wl = _single_row(small_workload(synth.DIMS_SMALL, BF16, frames=14), 1)
     w = small_weights(wl)
     inp = _single_inputs(synth.make_inputs(small_workload(synth.DIMS_SMALL, BF16, frames=14)), 1)
     dw = q3.to_device_weights(w)
-    a = run_gpu(wl, dw, inp, cap_rows=[0])
-    b = run_gpu(wl, dw, inp, cap_rows=[0], chunks=[3, 4, 7])
-    c = run_gpu(wl, dw, inp, cap_rows=[0])
+    opts = dict(step_path=q3.Q3_PATH_FRAME, expect_path=q3.Q3_PATH_FRAME)
+    a = run_gpu(wl, dw, inp, cap_rows=[0], **opts)
+    b = run_gpu(wl, dw, inp, cap_rows=[0], chunks=[3, 4, 7], **opts)
+    c = run_gpu(wl, dw, inp, cap_rows=[0], **opts)
     assert np.array_equal(a.codes, b.codes) and np.array_equal(a.codes, c.codes)
     assert np.array_equal(a.talker_logits, c.talker_logits, equal_nan=True)
+
+
+@pytest.mark.parametrize("dims", [synth.DIMS_CL, synth.DIMS_CL_PROJ], ids=["same-width", "projection"])
+def test_cluster_kernel_parity(q3, dims):
+    """Batch 1 on the cluster kernel (8 clusters x 8 CTAs, one per KV head),
+    every row of the small workload (greedy, sampled with top-k / top-p,
+    forced EOS, min_new_tokens) against the oracle."""
+    wl = small_workload(dims, BF16, frames=10)
+    w = small_weights(wl)
+    inp = synth.make_inputs(wl)
+    dw = q3.to_device_weights(w)
+    checked = decisions = 0
+    for r in range(wl.batch):
+        wl1, inp1 = _single_row(wl, r), _single_inputs(inp, r)
+        g = run_gpu(wl1, dw, inp1, cap_rows=[0], step_path=q3.Q3_PATH_CLUSTER, expect_path=q3.Q3_PATH_CLUSTER)
+        s = compare(wl1, w, inp1, g)
+        checked += s["checked"]
+        decisions += s["decisions"]
+    # 1024-way vocabularies leave closer top-2 logits than the 64-way ones of
+    # the other small shapes: a lower floor, still far from a collapsed margin
+    assert checked >= 0.3 * decisions, (checked, decisions)
+
+
+def test_cluster_kernel_chunked_and_repeatable(q3):
+    """Calls of 3 + 4 + 7 frames give the codes of one 14-frame call, and a
+    second run repeats the first bit for bit (fixed reduction orders)."""
+    full = small_workload(synth.DIMS_CL, BF16, frames=14)
+    wl = _single_row(full, 1)
+    w = small_weights(wl)
+    inp = _single_inputs(synth.make_inputs(full), 1)
+    dw = q3.to_device_weights(w)
+    opts = dict(step_path=q3.Q3_PATH_CLUSTER, expect_path=q3.Q3_PATH_CLUSTER)
+    a = run_gpu(wl, dw, inp, cap_rows=[0], **opts)
+    b = run_gpu(wl, dw, inp, cap_rows=[0], chunks=[3, 4, 7], **opts)
+    c = run_gpu(wl, dw, inp, cap_rows=[0], **opts)
+    assert np.array_equal(a.codes, b.codes) and np.array_equal(a.codes, c.codes)
+    assert np.array_equal(a.talker_logits, c.talker_logits, equal_nan=True)
+    assert np.array_equal(a.cp_logits, c.cp_logits, equal_nan=True)
+
+
+def test_cluster_kernel_wait_timeout(q3):
+    """A device-side wait that runs out: one cross-cluster exchange is never
+    written (test-only config field), every wait on it gives up after the
+    configured 2 ms, the step returns Q3_ERR_TIMEOUT and the handle can be
+    destroyed; a fresh handle on the same GPU then matches the oracle."""
+    wl = _single_row(small_workload(synth.DIMS_CL, BF16, frames=6), 0)
+    w = small_weights(wl)
+    inp = _single_inputs(synth.make_inputs(small_workload(synth.DIMS_CL, BF16, frames=6)), 0)
+    dw = q3.to_device_weights(w)
+    q = q3.Q3TTS(wl.dims, wl.dtype, dw, 1, wl.max_ctx, 8, step_path=q3.Q3_PATH_CLUSTER, wait_limit_us=2000,
+                 inject_timeout=3)
+    q.prefill(inp["prompt"], inp["prompt_offsets"], inp["text"], inp["text_offsets"], inp["tts_pad"], wl.rows)
+    rc, codes, frames, reasons = q.step_frames(2, check=False)
+    assert rc == q3.Q3_ERR_TIMEOUT, rc
+    assert frames[0] == 0 and reasons[0] == q3.Q3_RUNNING
+    q.close()
+    g = run_gpu(wl, dw, inp, cap_rows=[0], step_path=q3.Q3_PATH_CLUSTER, expect_path=q3.Q3_PATH_CLUSTER)
+    compare(wl, w, inp, g)

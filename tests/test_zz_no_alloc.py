@@ -1,9 +1,11 @@
 """The allocation-free draw entry point (for callers that cannot allocate
-device memory) gives the same ids as the handle-based q3tts_sample_logits,
-through the C ABI, on two calls in a row.  Collected last on purpose."""
+device memory) gives the same ids as the handle-based q3tts_sample_logits and
+as the oracle's processors + draw, through the C ABI, on two calls in a row.
+Collected last on purpose."""
 import numpy as np
 import pytest
 
+import oracle
 import synth
 from synth import RowSampling
 
@@ -48,6 +50,12 @@ def test_noalloc_matches_handle_entry_point(talker, V):
             got = q3.sample_logits_noalloc(lg_dev, talker, ps, sel, step, rows, d.eos_id, d.suppress_lo,
                                            d.suppress_hi, seen=seen_dev)
             assert np.array_equal(got, want), np.nonzero(got != want)[0][:10]
+            # and the oracle's own processors + draw on the same logits
+            for i in range(n):
+                err, oid, _, _ = oracle.sample(lg[i], ps[i], talker, seen=None if seen is None else seen[i],
+                                               sel_index=int(sel[i]), eos=d.eos_id, sup_lo=d.suppress_lo,
+                                               sup_hi=d.suppress_hi, row=int(rows[i]), frame=int(sel[i]), step=step)
+                assert err == 0 and oid == int(got[i]), (i, oid, int(got[i]))
         # a NaN set is reported, and the next call starts clean again
         lg = synth.random_logits(4, V, seed=99)
         lg[1, 5] = np.nan
@@ -66,5 +74,24 @@ def test_noalloc_matches_handle_entry_point(talker, V):
                                          np.zeros(1025, np.int32), d.eos_id, d.suppress_lo, d.suppress_hi,
                                          check=False)
         assert rc == q3.Q3_ERR_CAPACITY
+        # a sampling set with temperature 0 is rejected before anything runs
+        bad = _params(4, rng, talker)
+        bad[1].do_sample = bad[1].cp_do_sample = 1
+        bad[1].temperature = bad[1].cp_temperature = 0.0
+        rc, _ = q3.sample_logits_noalloc(torch.from_numpy(lg).cuda(), talker, bad, np.zeros(4, np.int32), 1,
+                                         np.zeros(4, np.int32), d.eos_id, d.suppress_lo, d.suppress_hi,
+                                         check=False)
+        assert rc == q3.Q3_ERR_ARG
+        # tensors the library cannot read safely never reach it
+        with pytest.raises(ValueError):
+            q3.sample_logits_noalloc(torch.from_numpy(lg).cuda().to(torch.bfloat16), talker, ps,
+                                     np.zeros(4, np.int32), 1, np.zeros(4, np.int32), d.eos_id, d.suppress_lo,
+                                     d.suppress_hi)
+        with pytest.raises(ValueError):
+            q3.sample_logits_noalloc(torch.from_numpy(lg), talker, ps, np.zeros(4, np.int32), 1,
+                                     np.zeros(4, np.int32), d.eos_id, d.suppress_lo, d.suppress_hi)
+        with pytest.raises(ValueError):
+            q3.sample_logits_noalloc(torch.from_numpy(lg).cuda(), talker, ps[:3], np.zeros(4, np.int32), 1,
+                                     np.zeros(4, np.int32), d.eos_id, d.suppress_lo, d.suppress_hi)
     finally:
         h.close()
