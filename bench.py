@@ -8,7 +8,10 @@ is selected.  Metric: 16-code frames per second (frames emitted by all rows).
 
 Default workload: 0.6B-shaped model in bf16, batch 1, 128-row prompt, 64 text
 rows then tts_pad, 100 greedy frames (the latency path).  --workload 3/4/5
-select the 1.7B batch-1, batch-32 and batch-256 workloads.
+select the 1.7B batch-1, batch-32 and batch-256 workloads.  With one rank the
+line also carries "batches": the batch-32 and batch-256 workloads (4 and 5)
+timed in the same run over a short window of steps, each with its HBM and
+tensor-pipe fractions (--no-batches skips them).
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle instead.
 """
@@ -44,6 +47,8 @@ def parse():
     p.add_argument("--step-path", default="auto", choices=["auto", "graph", "frame", "cluster"],
                    help="batch-1 step path (the library's default when auto)")
     p.add_argument("--cpu-frames", type=int, default=0, help="oracle frames timed for the CPU baseline (0: auto)")
+    p.add_argument("--no-batches", action="store_true", help="skip the batch-32 / batch-256 entries")
+    p.add_argument("--batch-steps", type=int, default=20, help="timed steps of each batch entry")
     return p.parse_args()
 
 
@@ -101,6 +106,24 @@ def measured_traffic(workload: int):
             return None, kv["kernel"]
         return float(kv["bytes"]), kv["kernel"]
     return None, None
+
+
+def row_flops(d) -> float:
+    """Algorithmic multiply-add FLOPs of the projections for one row and one
+    frame: the talker (1 token through 28 layers + codec head) and the
+    predictor (16 token passes through its layers: the 2-token prefill and 14
+    steps, 15 heads, and the input projection when the widths differ)."""
+    qkv = (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim
+
+    def layer(H, F):
+        return qkv * H + H * d.n_q_heads * d.head_dim + 2 * F * H + H * F
+    G1 = d.n_groups - 1
+    talker = d.n_layers * layer(d.hidden, d.ffn) + d.codec_vocab * d.hidden
+    passes = G1 + 1
+    pred = passes * d.cp_layers * layer(d.cp_hidden, d.cp_ffn) + G1 * d.cp_vocab * d.cp_hidden
+    if d.hidden != d.cp_hidden:
+        pred += passes * d.cp_hidden * d.hidden
+    return 2.0 * (talker + pred)
 
 
 def step_bytes(wl, live_pos):
@@ -183,10 +206,10 @@ def peaks():
 
 
 # ---------------------------------------------------------------- oracle (CPU baseline / reference arm)
-def oracle_rate(wl, w, inp, n_frames, warm_frames=0):
+def oracle_rate(wl, w, inp, n_frames, warm_frames=0, timed_threads=0):
     """Oracle frames/s on row 0 of the workload: prefill and warm_frames steps
-    (untimed), then n_frames timed steps.  Returns (rate, timed frames, seconds,
-    warm frames run)."""
+    (untimed), then n_frames timed steps (with timed_threads worker threads
+    when > 0).  Returns (rate, timed frames, seconds, warm frames run)."""
     import oracle
     rows = [0]
     lens = [wl.prompt_lens[0]]
@@ -201,9 +224,12 @@ def oracle_rate(wl, w, inp, n_frames, warm_frames=0):
         o.step(warm)
     warm_done = int(o.get("frames")[0])
     n = max(1, min(n_frames, T - warm))
+    prev = oracle.set_threads(timed_threads) if timed_threads > 0 else 0
     t0 = time.perf_counter()
     o.step(n)
     dt = time.perf_counter() - t0
+    if timed_threads > 0:
+        oracle.set_threads(prev)
     done = int(o.get("frames")[0]) - warm_done
     return done / dt, done, dt, warm
 
@@ -211,6 +237,24 @@ def oracle_rate(wl, w, inp, n_frames, warm_frames=0):
 def omp_threads():
     v = os.environ.get("OMP_NUM_THREADS")
     return int(v) if v else os.cpu_count()
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu part")):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 # ---------------------------------------------------------------- our arm
@@ -248,6 +292,10 @@ def run_ours(args, wl, rank, world):
         _, frames, reasons = q.step_frames(min(args.warmup, wl.frames), codes_out=codes_dev.view(-1))
         steps_done = min(args.warmup, wl.frames)
     kernels_per_step = q.step_kernel_count()
+    step_path = q3.PATH_NAMES.get(q.step_path(wl.batch), "graph")
+    rf = row_flops(wl.dims)
+    flops_total = 0.0
+    ctx_lo, ctx_hi = 1 << 30, 0
     remaining = args.steps
     total_ms = 0.0
     total_frames = 0
@@ -284,17 +332,21 @@ def run_ours(args, wl, rank, world):
                 wb, kb = step_bytes(wl, live)
                 wbytes_total += wb
                 kvbytes_total += kb
+                flops_total += rf * len(live)
+                if live:
+                    ctx_lo, ctx_hi = min(ctx_lo, min(live) + 1), max(ctx_hi, max(live) + 1)
             steps_done += n
             timed_steps += n
             remaining -= n
     (max_ms,), (all_frames,) = job_totals([total_ms], [total_frames], dev)
     res = dict(ms=max_ms, frames=all_frames, local_frames=total_frames, steps=timed_steps,
                wbytes=wbytes_total, kvbytes=kvbytes_total, kernels_per_step=kernels_per_step,
-               clocks=clocks.summary(), local_ms=total_ms)
+               clocks=clocks.summary(), local_ms=total_ms, flops=flops_total, ctx=(ctx_lo, ctx_hi),
+               step_path=step_path)
 
     # e2e: the whole request through the C ABI from pinned host buffers, one call per step,
     # codes read back to pinned host memory after every step
-    if not args.no_e2e:
+    if not getattr(args, "no_e2e", False):
         h_prompt = torch.from_numpy(inp["prompt"]).pin_memory()
         h_text = torch.from_numpy(inp["text"]).pin_memory()
         h_pad = torch.from_numpy(inp["tts_pad"]).pin_memory()
@@ -348,7 +400,7 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded random init)",
                 "config": config,
                 "cpu_baseline": {"value": rate, "unit": unit, "cores": omp_threads(), "kind": "oracle",
-                                 "sample": sample},
+                                 "cpu_model": cpu_model(), "sample": sample},
                 "e2e": {"value": rate, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -367,10 +419,11 @@ def main():
     value = job_rate(res["frames"], sec)
     bytes_total = res["wbytes"] + res["kvbytes"]
     achieved = bytes_total / (res["local_ms"] / 1000.0) / 1e9
-    # at batch 1 one launch of the frame kernel is the whole step
-    traffic, tk = measured_traffic(args.workload) if wl.batch == 1 else (None, None)
-    kernel_name = ("frame_kernel (one launch = the whole step; traffic from ncu, bytes per launch)"
-                   if wl.batch == 1 else "frame step (all kernels of one talker step)")
+    # the step's kernel, as the library reports the path it ran
+    kernel_name = {"frame": "frame_kernel (one launch = the whole step; traffic from ncu, bytes per launch)",
+                   "cluster": "cluster_step_kernel (one launch = the whole step)",
+                   "graph": "frame step (all kernels of one talker step)"}[res["step_path"]]
+    traffic, tk = measured_traffic(args.workload) if res["step_path"] == "frame" else (None, None)
     line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": res["steps"],
             "warmup": args.warmup, "ms_per_step": res["ms"] / max(res["steps"], 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == synth.BF16 else "f32",
@@ -380,6 +433,7 @@ def main():
                          "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / pk["hbm_gbs"], "peak_kind": pk_kind,
                          "traffic": traffic, "algorithmic_bytes_per_step": bytes_total / max(res["steps"], 1)},
+            "step_path": res["step_path"],
             "gpu_launches": res["kernels_per_step"] * res["steps"],
             "clocks": res["clocks"]}
     if "e2e" in res:
@@ -387,11 +441,43 @@ def main():
         line["e2e"] = {"value": job_rate(e["frames"], e["seconds"]), "unit": unit,
                        "h2d_bytes_per_step": e["h2d_per_step"], "d2h_bytes_per_step": e["d2h_per_step"],
                        "note": "prefill from pinned host + one q3tts_step_frames(1) per step, codes to pinned host"}
+    if not args.no_batches and world == 1 and args.workload not in (4, 5):
+        line["batches"] = []
+        del w, inp
+        for idx in (4, 5):
+            wlb = synth.workload(idx)
+            ba = argparse.Namespace(**vars(args))
+            ba.warmup, ba.steps, ba.no_e2e, ba.step_path = 3, args.batch_steps, True, "auto"
+            rb, _, _ = run_ours(ba, wlb, rank, world)
+            sb = rb["ms"] / 1000.0
+            bb = rb["wbytes"] + rb["kvbytes"]
+            ach_hbm = bb / sb / 1e9
+            ach_tc = rb["flops"] / sb / 1e12
+            line["batches"].append({
+                "workload": f"config {idx}: {wlb.name}", "batch": wlb.batch, "steps": rb["steps"],
+                "ms_per_step": rb["ms"] / max(rb["steps"], 1), "frames_per_s": job_rate(rb["frames"], sb),
+                "ctx_range": list(rb["ctx"]), "step_path": rb["step_path"],
+                "hbm": {"achieved": ach_hbm, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach_hbm / pk["hbm_gbs"],
+                        "bytes_per_step": bb / max(rb["steps"], 1), "peak_kind": pk_kind},
+                "tensor": {"achieved": ach_tc, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                           "frac": ach_tc / pk["bf16_tflops_sustained"], "flops_per_step": rb["flops"] / max(rb["steps"], 1),
+                           "peak_kind": pk_kind + " (sustained)",
+                           "note": "algorithmic FLOPs (one bf16 product per weight); the MMAs run the fp32 "
+                                   "operand as bf16 high + low parts, twice that work"},
+                "bound": "hbm" if ach_hbm / pk["hbm_gbs"] >= ach_tc / pk["bf16_tflops_sustained"] else "tensor",
+                "gpu_launches_per_step": rb["kernels_per_step"], "clocks": rb["clocks"]})
+            import torch
+            torch.cuda.empty_cache()
+        w = synth.make_weights(wl.dims, wl.dtype, wl.weight_seed) if not args.no_cpu_baseline else None
+        inp = synth.make_inputs(wl) if not args.no_cpu_baseline else None
     if not args.no_cpu_baseline and world == 1:
         n = args.cpu_frames or (20 if wl.dims.hidden <= 1024 else 10)
         rate, done, dt, _ = oracle_rate(wl, w, inp, n)
+        r1, n1, dt1, _ = oracle_rate(wl, w, inp, 2 if wl.dims.hidden <= 1024 else 1, timed_threads=1)
         line["cpu_baseline"] = {"value": rate, "unit": unit, "cores": omp_threads(), "kind": "oracle",
-                                "sample": f"row 0, {done} frames after prefill, {dt:.1f} s"}
+                                "cpu_model": cpu_model(),
+                                "sample": f"row 0, {done} frames after prefill, {dt:.1f} s",
+                                "single_thread": {"value": r1, "unit": unit, "sample": f"row 0, {n1} frames, {dt1:.1f} s"}}
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

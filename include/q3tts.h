@@ -101,6 +101,9 @@ typedef struct {
                            cross-cluster exchange with this index is never
                            written by CTA 0, so every wait on it runs out and
                            the step returns Q3_ERR_TIMEOUT                     */
+    int text_vocab;     /* text side (q3tts_text_embed): BPE vocabulary
+                           (151936 upstream); 0 = no text path                */
+    int text_hidden;    /* width of the text embedding (2048)                 */
 } q3tts_config;
 
 /* step_path values */
@@ -133,6 +136,13 @@ typedef struct {
     const void* cp_heads;    /* [n_groups-1][cp_vocab][cp_hidden] head s -> code s+1 */
     const void* cp_proj_w;   /* [cp_hidden][H] or NULL when H == cp_hidden           */
     const void* cp_proj_b;   /* [cp_hidden] f32 or NULL                              */
+    /* text side, NULL when config.text_vocab == 0: embedding and ResizeMLP
+     * (text_hidden -> text_hidden -> H with SiLU between the two layers)     */
+    const void* text_emb;    /* [text_vocab][text_hidden]                            */
+    const void* text_fc1_w;  /* [text_hidden][text_hidden]                           */
+    const void* text_fc1_b;  /* [text_hidden] f32                                    */
+    const void* text_fc2_w;  /* [H][text_hidden]                                     */
+    const void* text_fc2_b;  /* [H] f32                                              */
 } q3tts_weights;
 
 /* Per-row generation settings (talker and predictor draws). */
@@ -199,6 +209,21 @@ int q3tts_prefill(q3tts_t* h, int batch, const float* prompt, const int32_t* pro
  * Q3_FINISHED_ERROR, the others continue), Q3_ERR_BOUNDS, Q3_ERR_CUDA. */
 int q3tts_step_frames(q3tts_t* h, int n_frames, int32_t* codes_out, int32_t* frames_emitted,
                       int32_t* finish_reason);
+
+/* Talker-width rows of text tokens ("Qwen3-TTS 移植 ncnn 简明教程" section 1,
+ * talker bullet: Qwen2 BPE ids -> 2048-d text embedding -> ResizeMLP
+ * (2048 -> 2048 -> talker width, SiLU); the trailing-text rows that q3tts_prefill
+ * takes, one consumed per talker step):
+ *   rows_out[i] = fc2_w . silu(fc1_w . text_emb[ids[i]] + fc1_b) + fc2_b
+ * Every step runs on the GPU (an embedding gather, then the two projections
+ * as tensor-core GEMMs from 16 ids on, GEMVs below).
+ *   n         ids, >= 0
+ *   ids       [n] int32, host or device, each in [0, text_vocab)
+ *   rows_out  [n][hidden] f32, host or device
+ * Errors: Q3_ERR_ARG (no text path in the config or weights, NULL pointer, a
+ * host id out of range), Q3_ERR_BOUNDS (a device id out of range; its row is
+ * left zero), Q3_ERR_CUDA.  Ends with one synchronisation of the stream. */
+int q3tts_text_embed(q3tts_t* h, int n, const int32_t* ids, float* rows_out);
 
 /* Parity capture: while set, every talker selection of the listed rows stores
  * its raw fp32 logits to talker_logits[slot][k][codec_vocab] (k = selection

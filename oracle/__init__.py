@@ -70,6 +70,10 @@ def _L():
             lib.oracle_create.restype = vp
             lib.oracle_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), i32, i32, i32, i32]
             lib.oracle_destroy.argtypes = [vp]
+            lib.oracle_set_threads.restype = i32
+            lib.oracle_set_threads.argtypes = [i32]
+            lib.oracle_text_embed.restype = i32
+            lib.oracle_text_embed.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, i32, vp]
             lib.oracle_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
             lib.oracle_step.argtypes = [vp, i32, vp]
             lib.oracle_get.argtypes = [vp, i32, vp]
@@ -94,6 +98,31 @@ def _L():
 
 def lib():
     return _L()
+
+
+def text_embed(w: dict, dtype: int, ids) -> np.ndarray:
+    """Talker-width rows of text ids through the embedding and ResizeMLP (fp64).
+    w: text_emb [V][T], text_fc1_w [T][T], text_fc1_b [T] f32, text_fc2_w [H][T],
+    text_fc2_b [H] f32 (bf16 matrices as uint16 bit patterns)."""
+    emb = np.ascontiguousarray(w["text_emb"])
+    w1 = np.ascontiguousarray(w["text_fc1_w"])
+    w2 = np.ascontiguousarray(w["text_fc2_w"])
+    b1 = np.ascontiguousarray(w["text_fc1_b"], dtype=np.float32)
+    b2 = np.ascontiguousarray(w["text_fc2_b"], dtype=np.float32)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    V, T = emb.shape
+    H = w2.shape[0]
+    out = np.zeros((len(ids), H), np.float64)
+    err = _L().oracle_text_embed(emb.ctypes.data, w1.ctypes.data, b1.ctypes.data, w2.ctypes.data, b2.ctypes.data,
+                                 dtype, V, T, H, ids.ctypes.data, len(ids), out.ctypes.data)
+    if err:
+        raise ValueError("text id out of range")
+    return out
+
+
+def set_threads(n: int) -> int:
+    """Worker threads of the oracle's parallel loops (timing only); returns the previous count."""
+    return int(_L().oracle_set_threads(int(n)))
 
 
 def make_config(dims, dtype: int) -> Config:

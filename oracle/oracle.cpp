@@ -35,6 +35,9 @@
 //
 // Parity of end-to-end logits for random-init weights is unpinned beyond the
 // invariants the tests check (the pages print no logits for any weights).
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -652,6 +655,46 @@ void* oracle_create(const oracle_config* c, const oracle_weights* w, int batch, 
 }
 
 void oracle_destroy(void* h) { delete (Oracle*)h; }
+
+// Text side ("Qwen3-TTS 移植 ncnn 简明教程" section 1, talker bullet: BPE ids
+// -> 2048-d text embedding -> ResizeMLP(2048 -> 2048 -> talker width) with
+// SiLU between its two linear layers): for each id, in this order,
+//   e = emb[id];  a = silu(W1 e + b1);  out = W2 a + b2   (fp64).
+// Returns ERR_ARG for an id outside [0, vocab).
+int oracle_text_embed(const void* emb, const void* w1, const float* b1, const void* w2, const float* b2, int dtype,
+                      int vocab, int T, int H, const int32_t* ids, int n, double* out) {
+    const Mat E{emb, dtype}, W1{w1, dtype}, W2{w2, dtype};
+    std::vector<double> e(T), a(T);
+    for (int i = 0; i < n; ++i) {
+        const int id = ids[i];
+        if (id < 0 || id >= vocab) return ERR_ARG;
+        for (int k = 0; k < T; ++k) e[k] = E.at((size_t)id * T + k);
+        for (int j = 0; j < T; ++j) {
+            double acc = 0.0;
+            for (int k = 0; k < T; ++k) acc += W1.at((size_t)j * T + k) * e[k];
+            a[j] = silu(acc + (double)b1[j]);
+        }
+        for (int j = 0; j < H; ++j) {
+            double acc = 0.0;
+            for (int k = 0; k < T; ++k) acc += W2.at((size_t)j * T + k) * a[k];
+            out[(size_t)i * H + j] = acc + (double)b2[j];
+        }
+    }
+    return ERR_OK;
+}
+
+// Worker threads of the parallel loops from now on (timing only; results do
+// not depend on it); returns the count in effect before the call.
+int oracle_set_threads(int n) {
+#ifdef _OPENMP
+    const int old = omp_get_max_threads();
+    if (n > 0) omp_set_num_threads(n);
+    return old;
+#else
+    (void)n;
+    return 1;
+#endif
+}
 
 // Prefill: prompt rows through the talker, then selection 0 of each row.
 // row_ids: the row index each row uses in the noise counter.

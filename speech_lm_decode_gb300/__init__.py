@@ -23,7 +23,7 @@ PATH_NAMES = {Q3_PATH_GRAPH: "graph", Q3_PATH_FRAME: "frame", Q3_PATH_CLUSTER: "
 
 EXPORTS = ("q3tts_workspace_bytes", "q3tts_create", "q3tts_prefill", "q3tts_step_frames", "q3tts_set_capture",
            "q3tts_sample_logits", "q3tts_sample_logits_noalloc", "q3tts_step_kernel_count", "q3tts_step_path",
-           "q3tts_last_error", "q3tts_destroy")
+           "q3tts_text_embed", "q3tts_last_error", "q3tts_destroy")
 
 
 class Q3Error(RuntimeError):
@@ -38,7 +38,8 @@ class Config(ctypes.Structure):
                                             "n_groups", "eos_id", "suppress_lo", "suppress_hi")] + \
               [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)] + \
               [(n, ctypes.c_int) for n in ("dtype", "max_batch", "max_ctx", "max_text", "step_path", "tc_min_tokens",
-                                           "debug_sync", "wait_limit_us", "inject_timeout")]
+                                           "debug_sync", "wait_limit_us", "inject_timeout", "text_vocab",
+                                           "text_hidden")]
 
 # execution fields of the config (everything else comes from the model dims)
 EXEC_FIELDS = ("step_path", "tc_min_tokens", "debug_sync", "wait_limit_us", "inject_timeout")
@@ -52,7 +53,10 @@ class BlockWeights(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [("talker", BlockWeights), ("codec_emb", ctypes.c_void_p), ("codec_head", ctypes.c_void_p),
                 ("cp", BlockWeights), ("cp_emb", ctypes.c_void_p), ("cp_heads", ctypes.c_void_p),
-                ("cp_proj_w", ctypes.c_void_p), ("cp_proj_b", ctypes.c_void_p)]
+                ("cp_proj_w", ctypes.c_void_p), ("cp_proj_b", ctypes.c_void_p)] + \
+              [(n, ctypes.c_void_p) for n in ("text_emb", "text_fc1_w", "text_fc1_b", "text_fc2_w", "text_fc2_b")]
+
+TEXT_KEYS = ("text_emb", "text_fc1_w", "text_fc1_b", "text_fc2_w", "text_fc2_b")
 
 
 class Sampling(ctypes.Structure):
@@ -84,6 +88,7 @@ def lib():
         L.q3tts_sample_logits.argtypes = [vp, i32, vp, i32, vp, vp, vp, i32, vp, vp]
         L.q3tts_step_kernel_count.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
         L.q3tts_step_path.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int)]
+        L.q3tts_text_embed.argtypes = [vp, i32, vp, vp]
         L.q3tts_sample_logits_noalloc.argtypes = [i32, i32, vp, i32, vp, vp, vp, i32, vp, i32, i32, i32, vp, vp]
         L.q3tts_last_error.restype = ctypes.c_char_p
         L.q3tts_last_error.argtypes = [vp]
@@ -110,7 +115,7 @@ def make_config(dims, dtype: int, max_batch: int, max_ctx: int, max_text: int, *
         elif f == "max_text":
             c.max_text = max_text
         else:
-            setattr(c, f, getattr(dims, f))
+            setattr(c, f, getattr(dims, f, 0))
     return c
 
 
@@ -152,7 +157,7 @@ def make_weights(dw: dict) -> Weights:
         b = getattr(ws, blk)
         for k, _ in BlockWeights._fields_:
             setattr(b, k, _ptr(dw[blk][k]))
-    for k in ("codec_emb", "codec_head", "cp_emb", "cp_heads", "cp_proj_w", "cp_proj_b"):
+    for k in ("codec_emb", "codec_head", "cp_emb", "cp_heads", "cp_proj_w", "cp_proj_b") + TEXT_KEYS:
         setattr(ws, k, _ptr(dw.get(k)))
     return ws
 
@@ -224,6 +229,20 @@ class Q3TTS:
             self._check(rc)
             return out, frames, reasons
         return rc, out, frames, reasons
+
+    def text_embed(self, ids, out=None, check=True):
+        """Talker-width rows of text token ids (gather + ResizeMLP on the GPU).
+        ids: int32 numpy array or torch tensor (host or cuda); out: None (host
+        numpy returned) or an [n, hidden] float32 array / tensor to fill."""
+        n = int(len(ids))
+        if isinstance(ids, np.ndarray) or not hasattr(ids, "data_ptr"):
+            ids = np.ascontiguousarray(ids, dtype=np.int32)
+        rows = np.empty((n, self.dims.hidden), np.float32) if out is None else out
+        rc = lib().q3tts_text_embed(self.h, n, _ptr(ids) if n else None, _ptr(rows) if n else None)
+        if check:
+            self._check(rc)
+            return rows
+        return rc, rows
 
     def step_path(self, batch: int) -> int:
         """Q3_PATH_CLUSTER / Q3_PATH_FRAME / Q3_PATH_GRAPH: what runs a step of `batch` rows."""

@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const float* __restrict
 __global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
                                                            const float* __restrict__ pacc, int n_splits, int nq,
                                                            const int* __restrict__ tok_pos, float* __restrict__ out,
-                                                           int ldo) {
+                                                           int ldo, bf16* __restrict__ hi, bf16* __restrict__ lo) {
     const int m = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
     float res = 0.f;
     if (tok_pos[m] >= 0) {
@@ -226,13 +226,21 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restri
         }
         res = num / den;
     }
-    out[(size_t)m * ldo + (size_t)h * HD + t] = res;
+    const size_t i = (size_t)h * HD + t;
+    if (hi) {
+        // the O projection's tensor-core operand: bf16 high and low parts, [M][nq * 128]
+        const bf16 hv = __float2bfloat16_rn(res);
+        hi[(size_t)m * nq * HD + i] = hv;
+        lo[(size_t)m * nq * HD + i] = __float2bfloat16_rn(res - __bfloat162float(hv));
+    } else {
+        out[(size_t)m * ldo + i] = res;
+    }
 }
 
 template <typename T>
 static cudaError_t attention_impl(const float* qkv, int ldq, int M, int nq, int nkv, const T* Kc, const T* Vc, int cap,
                                   const int* tok_row, const int* tok_pos, int n_splits, float* pm, float* pl,
-                                  float* pacc, float* out, int ldo, cudaStream_t st) {
+                                  float* pacc, float* out, int ldo, bf16* hi, bf16* lo, cudaStream_t st) {
     dim3 grid(n_splits, nkv, M);
     const int gq = nq / nkv;
     switch (gq) {
@@ -243,19 +251,27 @@ static cudaError_t attention_impl(const float* qkv, int ldq, int M, int nq, int 
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    attn_combine_kernel<<<dim3(M, nq), 128, 0, st>>>(pm, pl, pacc, n_splits, nq, tok_pos, out, ldo);
+    attn_combine_kernel<<<dim3(M, nq), 128, 0, st>>>(pm, pl, pacc, n_splits, nq, tok_pos, out, ldo, hi, lo);
     return cudaGetLastError();
 }
 
 cudaError_t launch_attention(int dtype, const float* qkv, int ldq, int M, int nq, int nkv, const void* Kc,
                              const void* Vc, int cap, const int* tok_row, const int* tok_pos, int n_splits,
-                             float* part_m, float* part_l, float* part_acc, float* out, int ldo, cudaStream_t st) {
+                             float* part_m, float* part_l, float* part_acc, float* out, int ldo, cudaStream_t st,
+                             const TcScratch* split) {
     if (M <= 0) return cudaSuccess;
+    bf16* hi = nullptr;
+    bf16* lo = nullptr;
+    if (split) {
+        if (!tc_fits(*split, M, nq * HD)) return cudaErrorInvalidValue;
+        hi = (bf16*)split->base;
+        lo = hi + (size_t)M * nq * HD;
+    }
     if (dtype == Q3_BF16)
         return attention_impl<bf16>(qkv, ldq, M, nq, nkv, (const bf16*)Kc, (const bf16*)Vc, cap, tok_row, tok_pos,
-                                    n_splits, part_m, part_l, part_acc, out, ldo, st);
+                                    n_splits, part_m, part_l, part_acc, out, ldo, hi, lo, st);
     return attention_impl<float>(qkv, ldq, M, nq, nkv, (const float*)Kc, (const float*)Vc, cap, tok_row, tok_pos,
-                                 n_splits, part_m, part_l, part_acc, out, ldo, st);
+                                 n_splits, part_m, part_l, part_acc, out, ldo, hi, lo, st);
 }
 
 }  // namespace q3

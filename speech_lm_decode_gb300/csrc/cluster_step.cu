@@ -71,7 +71,10 @@ constexpr int STG = 512;                 // staged outputs
 constexpr int XW = 2048;                 // width of a reduction word row
 constexpr int TACC = 256;                // talker input slice
 constexpr int SIDE = 2048 + 4 * HD;      // per-op vectors: RMSNorm weights [H], q / k norms, RoPE rows
-constexpr int PF_AHEAD = 4;              // L2 prefetch distance (schedule ops)
+#ifndef PF_WINDOWS
+#define PF_WINDOWS 0
+#endif
+constexpr int PF_AHEAD = PF_WINDOWS;     // weight windows prefetched into L2 ahead of the ring
 
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -444,17 +447,26 @@ struct Producer {
         ++seq;
         return true;
     }
-    __device__ __forceinline__ void prefetch(int i, int nops) {
-        if (i >= nops) return;
-        const Op o = op_at(i, P);
-        const Gv g = gemv_of(o, P, cta);
-        if (g.ok) prefetch_l2(g.src, (unsigned)((size_t)g.R * g.K * 2));
+    // L2 prefetch cursor: the window PF_AHEAD windows past the last one issued
+    int pf_op = 0, pf_win = 0;
+    unsigned pf_seq = 0;
+    __device__ __forceinline__ void prefetch_to(unsigned target, int nops) {
+        while (pf_seq < target && pf_op < nops) {
+            const Gv g = gemv_of(op_at(pf_op, P), P, cta);
+            if (!g.ok) { ++pf_op; pf_win = 0; continue; }
+            const Win w = win_of(g.R, g.K);
+            if (pf_win >= w.nwin) { ++pf_op; pf_win = 0; continue; }
+            int off, bytes;
+            win_range(w, pf_win, off, bytes);
+            prefetch_l2(g.src + off, (unsigned)bytes);
+            ++pf_win;
+            ++pf_seq;
+        }
     }
     __device__ __forceinline__ void run() {
         const int nops = n_ops(P);
-        for (int i = 0; i < PF_AHEAD; ++i) prefetch(i, nops);
+        unsigned wseq = 0;   // weight windows issued
         for (int i = 0; i < nops && ok; ++i) {
-            prefetch(i + PF_AHEAD, nops);
             const Op o = op_at(i, P);
             if (!side(o)) return;
             if (o.kind == OP_ATT) {
@@ -476,6 +488,8 @@ struct Producer {
             for (int k = 0; k < w.nwin; ++k) {
                 int off, bytes, slot;
                 win_range(w, k, off, bytes);
+                if (PF_AHEAD > 0) prefetch_to(wseq + PF_AHEAD + 1, nops);
+                ++wseq;
                 if (!take(slot)) return;
                 mbar_expect(&s.full[slot], (unsigned)bytes);
                 bulk_g2s(s.ring[slot], g.src + off, (unsigned)bytes, &s.full[slot]);

@@ -158,7 +158,8 @@ __global__ void __launch_bounds__(128, 1) umma_linear_kernel(const __grid_consta
                                                              const __grid_constant__ CUtensorMap tmX2, int N, int K,
                                                              int M, float* __restrict__ Y, int ldy,
                                                              const float* __restrict__ bias, int accumulate, int F,
-                                                             float* __restrict__ Gout, int ldg, int kbs, int* err) {
+                                                             float* __restrict__ Gout, int ldg, bf16* __restrict__ Ghi,
+                                                             bf16* __restrict__ Glo, int kbs, int* err) {
     extern __shared__ __align__(1024) unsigned char raw[];
     // 1024-byte alignment of the swizzled tiles
     unsigned char* base = (unsigned char*)(((uintptr_t)raw + 1023) & ~(uintptr_t)1023);
@@ -243,7 +244,17 @@ __global__ void __launch_bounds__(128, 1) umma_linear_kernel(const __grid_consta
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int m = m0 + c0 + j;
-                    if (m < M) Gout[(size_t)m * ldg + n] = v[j] / (1.0f + expf(-v[j])) * u[j];
+                    if (m < M) {
+                        const float a = v[j] / (1.0f + expf(-v[j])) * u[j];
+                        if (Ghi) {
+                            // the next projection's tensor-core operand, [M][F] bf16 high / low
+                            const bf16 h = __float2bfloat16_rn(a);
+                            Ghi[(size_t)m * F + n] = h;
+                            Glo[(size_t)m * F + n] = __float2bfloat16_rn(a - __bfloat162float(h));
+                        } else {
+                            Gout[(size_t)m * ldg + n] = a;
+                        }
+                    }
                 }
             }
         } else if (n < N) {
@@ -436,7 +447,7 @@ double best_split(int nrows, int M, int K, int* ks_out) {
 template <int NT, bool GATED>
 cudaError_t launch_tc(const void* W, int N, int K, const float* X, int ldx, int M, float* Y, int ldy,
                       const float* bias, int accumulate, int F, float* G, int ldg, int ks, const TcScratch& tc,
-                      int* err, cudaStream_t st) {
+                      int* err, cudaStream_t st, const TcScratch* gsplit = nullptr) {
     constexpr int STAGES = stages_for(NT, GATED);
     bf16* hi = (bf16*)tc.base;
     bf16* lo = hi + (size_t)M * K;
@@ -472,8 +483,15 @@ cudaError_t launch_tc(const void* W, int N, int K, const float* X, int ldx, int 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    bf16* ghi = nullptr;
+    bf16* glo = nullptr;
+    if (gsplit) {
+        if (!GATED || !tc_fits(*gsplit, M, F)) return cudaErrorInvalidValue;
+        ghi = (bf16*)gsplit->base;
+        glo = ghi + (size_t)M * F;
+    }
     return cudaLaunchKernelEx(&cfg, umma_linear_kernel<NT, GATED, STAGES>, mw, mx, mx2, N, K, M, Y, ldy, bias,
-                              accumulate, F, G, ldg, kbs, err);
+                              accumulate, F, G, ldg, ghi, glo, kbs, err);
 }
 
 // Tile width and K split of least cost among the widths the tokens allow.
@@ -505,13 +523,13 @@ cudaError_t launch_linear_tc(const void* W, int N, int K, const float* X, int ld
 }
 
 cudaError_t launch_linear_gated_tc(const void* W, int F, int K, const float* X, int ldx, int M, float* out, int ldo,
-                                   const TcScratch& tc, int* err, cudaStream_t st) {
+                                   const TcScratch& tc, int* err, cudaStream_t st, const TcScratch* out_split) {
     int nt = 32, ks = 1;
     pick_shape<true>(F, M, K, &nt, &ks);
     switch (nt) {
-        case 128: return launch_tc<128, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, ks, tc, err, st);
-        case 64: return launch_tc<64, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, ks, tc, err, st);
-        default: return launch_tc<32, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, ks, tc, err, st);
+        case 128: return launch_tc<128, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, ks, tc, err, st, out_split);
+        case 64: return launch_tc<64, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, ks, tc, err, st, out_split);
+        default: return launch_tc<32, true>(W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, ks, tc, err, st, out_split);
     }
 }
 

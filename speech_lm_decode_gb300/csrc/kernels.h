@@ -41,15 +41,19 @@ bool linear_takes_split(int dtype, int M, int K, const TcScratch& tc);
 cudaError_t launch_linear(int dtype, const void* W, int N, int K, const float* X, int ldx, int M, float* Y, int ldy,
                           const float* bias, int accumulate, const TcScratch& tc, int* err, cudaStream_t st);
 // SwiGLU projection: out[m][n] = silu(g) * u with g = W[n].x, u = W[F+n].x,
-// W [2F][K]; out fp32 with leading dimension ldo.
+// W [2F][K]; out fp32 with leading dimension ldo, or (out_split != NULL, only
+// where linear_takes_split) the bf16 high / low parts [M][F] in out_split,
+// the operand of a following launch_linear(X = NULL) on that scratch.
 cudaError_t launch_linear_gated(int dtype, const void* W, int F, int K, const float* X, int ldx, int M, float* out,
-                                int ldo, const TcScratch& tc, int* err, cudaStream_t st);
+                                int ldo, const TcScratch& tc, int* err, cudaStream_t st,
+                                const TcScratch* out_split = nullptr);
 // tensor-core (tcgen05) variants for bf16 weights and many tokens (gemm_tc.cu)
 bool tc_available();
 cudaError_t launch_linear_tc(const void* W, int N, int K, const float* X, int ldx, int M, float* Y, int ldy,
                              const float* bias, int accumulate, const TcScratch& tc, int* err, cudaStream_t st);
 cudaError_t launch_linear_gated_tc(const void* W, int F, int K, const float* X, int ldx, int M, float* out, int ldo,
-                                   const TcScratch& tc, int* err, cudaStream_t st);
+                                   const TcScratch& tc, int* err, cudaStream_t st,
+                                   const TcScratch* out_split = nullptr);
 // out[row(m)] = x[m] * rsqrt(mean(x[m]^2) + eps) * w; optionally hout (a
 // second copy).  out_row: NULL = identity, else the output row of each input
 // row (negative: skip).
@@ -69,10 +73,13 @@ cudaError_t launch_qk_rope_kv(int dtype, float* qkv, int ldq, int M, int nq, int
                               const float* k_norm, float eps, const float* rope_cs, int rope_rows, void* Kc, void* Vc,
                               int cap, const int* tok_row, const int* tok_pos, int* err, cudaStream_t st);
 // Split-KV grouped-query decode attention over positions 0..tok_pos[m] of the
-// token's row, then the combine writing the O-projection operand [M][nq*128].
+// token's row, then the combine writing the O-projection operand [M][nq*128]:
+// fp32 into out, or (split != NULL) as the bf16 high / low parts the
+// tensor-core projection reads with X = NULL.
 cudaError_t launch_attention(int dtype, const float* qkv, int ldq, int M, int nq, int nkv, const void* Kc,
                              const void* Vc, int cap, const int* tok_row, const int* tok_pos, int n_splits,
-                             float* part_m, float* part_l, float* part_acc, float* out, int ldo, cudaStream_t st);
+                             float* part_m, float* part_l, float* part_acc, float* out, int ldo, cudaStream_t st,
+                             const TcScratch* split = nullptr);
 
 // ---------------------------------------------------------------- sampler.cu
 size_t sampler_smem_bytes();
@@ -103,6 +110,12 @@ cudaError_t launch_cp_embed_prefill(int dtype, RowState* rs, int B, const float*
 // Predictor step s (1..14) token table[s-1](code_s) -> dst row b (width H).
 cudaError_t launch_cp_embed_step(int dtype, const RowState* rs, int B, const void* cp_emb, int H, int cpV, int s,
                                  const int32_t* codes_ws, int frames_cap, float* dst, int* err, cudaStream_t st);
+
+// Text side: out[i] = emb[ids[i]] as fp32 rows of `width` (a zero row and the
+// bounds bit for an id outside [0, vocab)); x = SiLU(x) over n values.
+cudaError_t launch_text_gather(int dtype, const void* emb, const int32_t* ids, int n, int vocab, int width, float* out,
+                               int* err, cudaStream_t st);
+cudaError_t launch_silu(float* x, long n, cudaStream_t st);
 
 // dst[b*pitch + j*G + q] = codes of frame f0+j of row b (-1 past the buffer).
 cudaError_t launch_pack_codes(const int32_t* codes_ws, int frames_cap, long f0, int n, int G, int B, int32_t* dst,

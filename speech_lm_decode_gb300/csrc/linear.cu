@@ -186,10 +186,10 @@ cudaError_t launch_linear(int dtype, const void* W, int N, int K, const float* X
 }
 
 cudaError_t launch_linear_gated(int dtype, const void* W, int F, int K, const float* X, int ldx, int M, float* out,
-                                int ldo, const TcScratch& tc, int* err, cudaStream_t st) {
+                                int ldo, const TcScratch& tc, int* err, cudaStream_t st, const TcScratch* out_split) {
     if (linear_takes_split(dtype, M, K, tc))
-        return launch_linear_gated_tc(W, F, K, X, ldx, M, out, ldo, tc, err, st);
-    if (!X) return cudaErrorInvalidValue;
+        return launch_linear_gated_tc(W, F, K, X, ldx, M, out, ldo, tc, err, st, out_split);
+    if (!X || out_split) return cudaErrorInvalidValue;
     if (dtype == Q3_BF16)
         return linear_impl<bf16, true>((const bf16*)W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, st);
     return linear_impl<float, true>((const float*)W, F, K, X, ldx, M, nullptr, 0, nullptr, 0, F, out, ldo, st);

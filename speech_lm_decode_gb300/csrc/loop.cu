@@ -177,3 +177,45 @@ cudaError_t launch_pack_codes(const int32_t* codes_ws, int frames_cap, long f0, 
 }
 
 }  // namespace q3
+
+namespace q3 {
+
+// ------------------------------------------------------------------ text side
+// out[i][:] = emb[ids[i]][:] (fp32), one block per id; an id outside
+// [0, vocab) leaves a zero row and sets the bounds bit.
+template <typename T>
+__global__ void __launch_bounds__(256) text_gather_kernel(const T* __restrict__ emb, const int32_t* __restrict__ ids,
+                                                          int vocab, int width, float* __restrict__ out, int* err) {
+    const int i = blockIdx.x;
+    const int id = ids[i];
+    const bool ok = id >= 0 && id < vocab;
+    if (!ok && threadIdx.x == 0) atomicOr(err, ERRB_BOUNDS);
+    for (int k = threadIdx.x; k < width; k += 256)
+        out[(size_t)i * width + k] = ok ? to_f(emb[(size_t)id * width + k]) : 0.0f;
+}
+
+__global__ void silu_kernel(float* __restrict__ x, long n) {
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+        const float v = x[i];
+        x[i] = v / (1.0f + expf(-v));
+    }
+}
+
+cudaError_t launch_text_gather(int dtype, const void* emb, const int32_t* ids, int n, int vocab, int width, float* out,
+                               int* err, cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    if (dtype == Q3_BF16)
+        text_gather_kernel<bf16><<<n, 256, 0, st>>>((const bf16*)emb, ids, vocab, width, out, err);
+    else
+        text_gather_kernel<float><<<n, 256, 0, st>>>((const float*)emb, ids, vocab, width, out, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_silu(float* x, long n, cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    const int blocks = (int)std::min<long>((n + 255) / 256, 4L * device_sm_count());
+    silu_kernel<<<blocks, 256, 0, st>>>(x, n);
+    return cudaGetLastError();
+}
+
+}  // namespace q3

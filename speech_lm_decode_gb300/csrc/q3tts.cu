@@ -29,7 +29,7 @@ constexpr int MIN_SAMPLE_SETS = 256; // staging for q3tts_sample_logits
 struct Layout {
     size_t kvK, kvV, ckvK, ckvV, rope, rows, params, h, x, cx, tok, opA, opB, headop, qkv, pm, pl, pacc, logits,
         cplogits, t_row, t_pos, c_row, c_pos, last_row, codes, codes_stage, text, pad, err, s_params, s_logits, s_sel, s_row, s_ids, s_seen, cap_slot,
-        fparams, fctl, fpart, fll, tcs, clpack, clxr, cllg, clparams;
+        fparams, fctl, fpart, fll, tcs, tcs2, clpack, clxr, cllg, clparams;
     bool cl;                            // the cluster step kernel's regions are present
     size_t total;
     int mmax, kA, kB, rope_rows, frames_cap, n_sets, vmax, fsplits;
@@ -51,8 +51,8 @@ Layout make_layout(const q3tts_config& c) {
     const size_t B = (size_t)c.max_batch, hd = (size_t)c.head_dim;
     const int nqkv = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
     L.mmax = std::max(std::min(PREFILL_CHUNK, c.max_batch * c.max_ctx), 2 * c.max_batch);
-    L.kA = std::max(std::max(c.hidden, c.cp_hidden), c.n_q_heads * c.head_dim);
-    L.kB = std::max(std::max(c.ffn, c.cp_ffn), c.hidden);
+    L.kA = std::max(std::max(std::max(c.hidden, c.cp_hidden), c.n_q_heads * c.head_dim), c.text_hidden);
+    L.kB = std::max(std::max(std::max(c.ffn, c.cp_ffn), c.hidden), c.text_hidden);
     L.rope_rows = std::max(c.max_ctx, 16);
     L.frames_cap = c.max_ctx;
     L.n_sets = std::max(c.max_batch, MIN_SAMPLE_SETS);
@@ -117,6 +117,9 @@ Layout make_layout(const q3tts_config& c) {
     }
     // tensor-core path: bf16 high / low parts of an fp32 operand [mmax][kmax]
     L.tcs = c.dtype == Q3_BF16 ? take((size_t)L.mmax * std::max(L.kA, L.kB) * 4) : take(256);
+    // a second one: the SiLU(g)*u operand of the down projection, written while the
+    // gate/up projection still reads the first
+    L.tcs2 = c.dtype == Q3_BF16 ? take((size_t)L.mmax * std::max(L.kA, L.kB) * 4) : take(256);
     // cluster step kernel (batch 1): packed weight image, exchange words, parameters
     L.cl = c.step_path == Q3_PATH_CLUSTER && cl_unsupported(c)[0] == 0;
     if (L.cl) {
@@ -154,6 +157,9 @@ bool config_ok(const q3tts_config* c, std::string* why) {
     if (c->wait_limit_us < 0 || c->inject_timeout < 0 || c->debug_sync < 0 || c->debug_sync > 1)
         return bad("bad wait_limit_us / inject_timeout / debug_sync");
     if (c->step_path == Q3_PATH_CLUSTER && cl_unsupported(*c)[0] != 0) return bad("cluster kernel: unsupported shape");
+    if (c->text_vocab < 0 || c->text_hidden < 0 || (c->text_vocab > 0) != (c->text_hidden > 0) ||
+        (c->text_hidden > 0 && c->text_hidden % 8))
+        return bad("text_vocab / text_hidden: both 0, or both positive with text_hidden a multiple of 8");
     return true;
 }
 
@@ -195,6 +201,11 @@ struct q3tts {
         t.base = c.dtype == Q3_BF16 ? p<void>(L.tcs) : nullptr;
         t.bytes = c.dtype == Q3_BF16 ? (size_t)L.mmax * std::max(L.kA, L.kB) * 4 : 0;
         t.min_tokens = c.tc_min_tokens == 0 ? 16 : c.tc_min_tokens;
+        return t;
+    }
+    TcScratch tc2() const {
+        TcScratch t = tc();
+        t.base = c.dtype == Q3_BF16 ? p<void>(L.tcs2) : nullptr;
         return t;
     }
     RowState* rows() const { return p<RowState>(L.rows); }
@@ -273,6 +284,11 @@ int enqueue_layers(q3tts* h, bool talker, int M, float* x, const int* trow, cons
     const int splits = talker ? (M <= 2 * c.max_batch ? h->splits_t : 1) : 1;
     const float eps = c.rms_eps;
     const bool presplit = linear_takes_split(c.dtype, M, H, h->tc());
+    // the attention combine writes the O projection's operand, and the gate/up
+    // projection the down projection's, when those run on the tensor cores
+    const TcScratch tcs = h->tc(), tcs2 = h->tc2();
+    const bool presplit_o = linear_takes_split(c.dtype, M, c.n_q_heads * c.head_dim, tcs);
+    const bool presplit_d = presplit && linear_takes_split(c.dtype, M, F, tcs2);
     for (int l = 0; l < L; ++l) {
         const char* wqkv = (const char*)bw.wqkv + (size_t)l * nqkv * H * e;
         const char* wo = (const char*)bw.wo + (size_t)l * H * nq * hd * e;
@@ -291,16 +307,19 @@ int enqueue_layers(q3tts* h, bool talker, int M, float* x, const int* trow, cons
                              Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos, h->err(), h->st)); debug_wait(h, "launch_qk_rope_kv");
         CK(launch_attention(c.dtype, qkv, nqkv, M, nq, nkv, Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos,
                             splits, h->p<float>(h->L.pm), h->p<float>(h->L.pl), h->p<float>(h->L.pacc), opA, nq * hd,
-                            h->st)); debug_wait(h, "launch_attention");
-        CK(launch_linear(c.dtype, wo, H, nq * hd, opA, nq * hd, M, x, H, nullptr, 1, h->tc(), h->err(), h->st)); debug_wait(h, "launch_linear");
+                            h->st, presplit_o ? &tcs : nullptr)); debug_wait(h, "launch_attention");
+        CK(launch_linear(c.dtype, wo, H, nq * hd, presplit_o ? nullptr : opA, nq * hd, M, x, H, nullptr, 1, tcs, h->err(),
+                         h->st)); debug_wait(h, "launch_linear");
         if (presplit) {
             CK(launch_rmsnorm_split(x, H, M, (const float*)bw.mlp_norm + (size_t)l * H, H, eps, h->tc(), h->st)); debug_wait(h, "launch_rmsnorm_split");
         } else {
             CK(launch_rmsnorm(x, H, M, (const float*)bw.mlp_norm + (size_t)l * H, H, eps, opA, H, nullptr, 0,
                               nullptr, h->st)); debug_wait(h, "launch_rmsnorm");
         }
-        CK(launch_linear_gated(c.dtype, wgu, F, H, presplit ? nullptr : opA, H, M, opB, F, h->tc(), h->err(), h->st)); debug_wait(h, "launch_linear_gated");
-        CK(launch_linear(c.dtype, wd, H, F, opB, F, M, x, H, nullptr, 1, h->tc(), h->err(), h->st)); debug_wait(h, "launch_linear");
+        CK(launch_linear_gated(c.dtype, wgu, F, H, presplit ? nullptr : opA, H, M, opB, F, tcs, h->err(), h->st,
+                               presplit_d ? &tcs2 : nullptr)); debug_wait(h, "launch_linear_gated");
+        CK(launch_linear(c.dtype, wd, H, F, presplit_d ? nullptr : opB, F, M, x, H, nullptr, 1, presplit_d ? tcs2 : tcs,
+                         h->err(), h->st)); debug_wait(h, "launch_linear");
     }
     return Q3_OK;
 }
@@ -498,6 +517,8 @@ bool weights_ok(const q3tts_config& c, const q3tts_weights* w) {
             return false;
     if (!w->codec_emb || !w->codec_head || !w->cp_emb || !w->cp_heads) return false;
     if (c.hidden != c.cp_hidden && (!w->cp_proj_w || !w->cp_proj_b)) return false;
+    if (c.text_vocab > 0 && (!w->text_emb || !w->text_fc1_w || !w->text_fc1_b || !w->text_fc2_w || !w->text_fc2_b))
+        return false;
     return true;
 }
 
@@ -803,6 +824,54 @@ int q3tts_step_frames(q3tts_t* h, int n_frames, int32_t* codes_out, int32_t* fra
         if (frames_emitted) frames_emitted[r] = rs[r].frames;
         if (finish_reason) finish_reason[r] = rs[r].finished ? rs[r].reason : Q3_RUNNING;
     }
+    return read_errors(h, err_host);
+}
+
+int q3tts_text_embed(q3tts_t* h, int n, const int32_t* ids, float* rows_out) {
+    if (!h) return Q3_ERR_ARG;
+    NvtxRange nvtx("q3tts_text_embed");
+    const q3tts_config& c = h->c;
+    if (c.text_vocab <= 0) return fail(h, Q3_ERR_ARG, "the configuration has no text path (text_vocab 0)");
+    if (n < 0) return fail(h, Q3_ERR_ARG, "negative n");
+    if (n == 0) return Q3_OK;
+    if (!ids || !rows_out) return fail(h, Q3_ERR_ARG, "NULL argument");
+    auto on_device = [](const void* p) {
+        cudaPointerAttributes pa;
+        const bool d = cudaPointerGetAttributes(&pa, p) == cudaSuccess &&
+                       (pa.type == cudaMemoryTypeDevice || pa.type == cudaMemoryTypeManaged);
+        cudaGetLastError();
+        return d;
+    };
+    const bool ids_dev = on_device(ids), out_dev = on_device(rows_out);
+    if (!ids_dev)
+        for (int i = 0; i < n; ++i)
+            if (ids[i] < 0 || ids[i] >= c.text_vocab) return fail(h, Q3_ERR_ARG, "id %d at %d outside [0, %d)", ids[i], i, c.text_vocab);
+    const int T = c.text_hidden, H = c.hidden;
+    int* dids = h->p<int>(h->L.t_row);          // [mmax] ids of one chunk
+    float* e = h->p<float>(h->L.opA);          // [mmax][T] gathered embeddings
+    float* a = h->p<float>(h->L.opB);          // [mmax][T] SiLU(fc1)
+    float* y = h->p<float>(h->L.x);            // [mmax][H] staging of host-bound rows
+    int* err = h->err() + 3;                    // own error word
+    CK(cudaMemsetAsync(err, 0, sizeof(int), h->st));
+    for (int i0 = 0; i0 < n; i0 += h->L.mmax) {
+        const int m = std::min(h->L.mmax, n - i0);
+        CK(cudaMemcpyAsync(dids, ids + i0, (size_t)m * sizeof(int), cudaMemcpyDefault, h->st));
+        CK(launch_text_gather(c.dtype, h->w.text_emb, dids, m, c.text_vocab, T, e, err, h->st)); debug_wait(h, "launch_text_gather");
+        CK(launch_linear(c.dtype, h->w.text_fc1_w, T, T, e, T, m, a, T, (const float*)h->w.text_fc1_b, 0, h->tc(),
+                         h->err(), h->st)); debug_wait(h, "launch_linear");
+        CK(launch_silu(a, (long)m * T, h->st)); debug_wait(h, "launch_silu");
+        float* dst = out_dev ? rows_out + (size_t)i0 * H : y;
+        CK(launch_linear(c.dtype, h->w.text_fc2_w, H, T, a, T, m, dst, H, (const float*)h->w.text_fc2_b, 0, h->tc(),
+                         h->err(), h->st)); debug_wait(h, "launch_linear");
+        if (!out_dev)
+            CK(cudaMemcpyAsync(rows_out + (size_t)i0 * H, y, (size_t)m * H * sizeof(float), cudaMemcpyDeviceToHost,
+                               h->st));
+        // the chunk's buffers are reused by the next one (host ids / rows are read or written in the call)
+        CK(cudaStreamSynchronize(h->st));
+    }
+    int err_host[4] = {0, 0, 0, 0};
+    CK(cudaMemcpyAsync(err_host, err, sizeof(int), cudaMemcpyDeviceToHost, h->st));
+    CK(cudaStreamSynchronize(h->st));
     return read_errors(h, err_host);
 }
 

@@ -116,9 +116,13 @@ class Dims:
     suppress_hi: int = 3072
     rms_eps: float = 1e-6
     rope_theta: float = 1e6
+    text_vocab: int = 0      # text side (BPE vocabulary; 0 = none)
+    text_hidden: int = 0     # text embedding width
 
 
 DIMS_06B = Dims()
+# the text side of the released models: Qwen2 BPE vocabulary, 2048-d embedding
+TEXT_VOCAB, TEXT_HIDDEN = 151936, 2048
 DIMS_17B = Dims(hidden=2048, ffn=6144)
 # Small shapes with the same structure, for fast tests (head_dim stays 128).
 DIMS_SMALL = Dims(n_layers=2, hidden=256, ffn=384, codec_vocab=96, cp_layers=2, cp_hidden=256,
@@ -260,6 +264,18 @@ def make_weights(d: Dims, dtype: int, seed: int, norm_std: float = 0.0) -> dict:
         w["cp_proj_w"] = None
         w["cp_proj_b"] = None
     return w
+
+
+def make_text_weights(d: Dims, dtype: int, seed: int) -> dict:
+    """Random-init text side: embedding [text_vocab, text_hidden] ~ N(0, 1) (the
+    scale of the prompt rows), ResizeMLP layers ~ N(0, 0.02) with biases:
+    text_fc1_w [T, T], text_fc1_b [T], text_fc2_w [H, T], text_fc2_b [H]."""
+    V, T, H = d.text_vocab, d.text_hidden, d.hidden
+    return {"text_emb": normal((V, T), seed, _stream(0x400), 1.0, dtype),
+            "text_fc1_w": normal((T, T), seed, _stream(0x401), 0.02, dtype),
+            "text_fc1_b": normal((T,), seed, _stream(0x402), 0.02),
+            "text_fc2_w": normal((H, T), seed, _stream(0x403), 0.02, dtype),
+            "text_fc2_b": normal((H,), seed, _stream(0x404), 0.02)}
 
 
 def weight_bytes(d: Dims, dtype: int) -> dict:

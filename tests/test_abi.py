@@ -48,3 +48,34 @@ def test_workspace_size_and_config_validation():
     h = ctypes.c_void_p()
     w = q3.Weights()
     assert L.q3tts_create(ctypes.byref(c), ctypes.byref(w), None, 0, None, ctypes.byref(h)) == q3.Q3_ERR_ARG
+
+
+def test_execution_fields_are_validated():
+    """The execution choices are explicit config fields: out-of-range values
+    make the configuration invalid, and the cluster path (whose packed weight
+    image sits in the workspace) grows the workspace only when it is asked for
+    and the shape is one it serves."""
+    import speech_lm_decode_gb300 as q3
+    import synth
+    L = q3.lib()
+
+    def size(d=synth.DIMS_06B, **kw):
+        c = q3.make_config(d, q3.Q3_BF16, 1, 228, 64, **kw)
+        return L.q3tts_workspace_bytes(ctypes.byref(c))
+    base = size()
+    assert base > 0
+    for kw in ({"step_path": 4}, {"step_path": -1}, {"wait_limit_us": -1}, {"inject_timeout": -2},
+               {"debug_sync": 2}):
+        assert size(**kw) == 0, kw
+    for p in (q3.Q3_PATH_GRAPH, q3.Q3_PATH_FRAME):
+        assert size(step_path=p) == base
+    # the packed image holds every matrix once more (about 1.2 GB for the 0.6B shape)
+    assert size(step_path=q3.Q3_PATH_CLUSTER) > base + 10 ** 9
+    # a shape the cluster kernel does not serve cannot ask for it
+    assert size(d=synth.DIMS_SMALL, step_path=q3.Q3_PATH_CLUSTER) == 0
+    assert size(d=synth.DIMS_CL, step_path=q3.Q3_PATH_CLUSTER) > 0
+    # the text side: both sizes or neither
+    import dataclasses
+    assert size(d=dataclasses.replace(synth.DIMS_06B, text_vocab=100)) == 0
+    assert size(d=dataclasses.replace(synth.DIMS_06B, text_vocab=100, text_hidden=2048)) >= base
+    assert size(d=dataclasses.replace(synth.DIMS_06B, text_vocab=100, text_hidden=4096)) > base

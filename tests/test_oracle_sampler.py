@@ -285,3 +285,108 @@ def test_top_p_keeps_the_smallest_prefix():
     lg = np.log(p).astype(np.float32)
     assert set(_cp_draws(lg, 400, temperature=1.0, top_k=0, top_p=0.4)) == {2}
     assert set(_cp_draws(lg, 400, temperature=1.0, top_k=0, top_p=0.5)) == {2, 7}
+
+
+# ---------------------------------------------------------------- decision margin
+# Reading of "codes must agree where the top-1 margin exceeds 0.05" for sampled
+# draws (a draw whose kept set a 0.05 logit perturbation could change is not
+# a decision the tolerance can hold to): the winner's log-score lead over every
+# id a small perturbation could keep -- the kept ids and the ids within 0.05 of
+# the top-k threshold or of the top-p boundary -- and, when the winner itself
+# survives top-k or top-p only narrowly, its distance to that boundary.  Each
+# case below is built so that one specific term sets the margin; the noise
+# values come from the Philox generator pinned above, and the scores are
+# recomputed here with the math library.
+
+def _E(seed, step, i, row=0, frame=0):
+    u = oracle.lib().oracle_noise_uniform(seed, row, frame, step, i)
+    assert 0.0 < u < 1.0
+    return -math.log(u)
+
+
+def _scores(l, ids, seed, step):
+    mx = max(float(l[i]) for i in ids)
+    return {i: math.exp(float(l[i]) - mx) / _E(seed, step, i) for i in ids}
+
+
+def _draw(l, seed, step, top_k=0, top_p=1.0):
+    # a predictor draw (no penalty, suppression or min_new): its cp_* settings apply
+    s = sp(do_sample=1, temperature=1.0, seed=seed, top_k=top_k, top_p=top_p, cp_do_sample=1, cp_temperature=1.0,
+           cp_top_k=top_k, cp_top_p=top_p)
+    err, oid, margin, _ = oracle.sample(np.asarray(l, np.float32), s, False, row=0, frame=0, step=step)
+    assert err == 0
+    return oid, margin
+
+
+def _seed_where(pred, step, limit=400):
+    for seed in range(limit):
+        if pred(seed):
+            return seed
+    raise AssertionError("no seed in range satisfies the case")
+
+
+def test_margin_score_ratio_without_filters():
+    """No top-k / top-p: every id is a competitor; the margin is the winner's
+    smallest log-score lead."""
+    l = np.array([0.0, 0.3, -0.2, 0.1], np.float32)
+    for seed in (1, 2, 3, 11, 40):
+        sc = _scores(l, range(4), seed, 5)
+        best = max(range(4), key=lambda i: (sc[i], -i))
+        want = min(math.log(sc[best] / sc[i]) for i in range(4) if i != best)
+        oid, margin = _draw(l, seed, 5)
+        assert oid == best
+        assert margin >= 0.0 and abs(margin - want) < 1e-5, (seed, margin, want)
+
+
+def test_margin_counts_an_id_just_outside_top_k():
+    """top-k 1 keeps id 0 only; id 1 sits 0.03 below the threshold, so a
+    perturbation could keep it: its score counts, and so does the winner's
+    distance to the next logit below the threshold."""
+    l = np.array([10.0, 9.97, 0.0], np.float32)
+    gap = float(np.float32(10.0)) - float(np.float32(9.97))
+    # noise where id 1 would have outscored the winner: the score term binds
+    seed = _seed_where(lambda s: _E(s, 2, 1) < _E(s, 2, 0), 2)
+    sc = _scores(l, [0, 1], seed, 2)
+    oid, margin = _draw(l, seed, 2, top_k=1)
+    assert oid == 0
+    assert abs(margin - math.log(sc[0] / sc[1])) < 1e-5 and margin < gap
+    # noise where it would not: the threshold distance binds
+    seed = _seed_where(lambda s: _E(s, 2, 1) > _E(s, 2, 0), 2)
+    oid, margin = _draw(l, seed, 2, top_k=1)
+    assert oid == 0 and abs(margin - gap) < 1e-6
+
+
+def test_margin_counts_an_id_just_outside_top_p():
+    """Three equal logits with top-p 0.665: ids 0 and 1 are kept, id 2 falls
+    out with its prefix sum 0.25 % above the boundary, so it stays a
+    competitor; chosen noise makes it the closest one."""
+    l = np.zeros(3, np.float32)
+
+    def case(s):
+        E = [_E(s, 4, i) for i in range(3)]
+        best = 0 if E[0] <= E[1] else 1
+        other = 1 - best
+        return E[2] < E[other] and E[2] > E[best]
+    seed = _seed_where(case, 4)
+    E = [_E(seed, 4, i) for i in range(3)]
+    best = 0 if E[0] <= E[1] else 1
+    oid, margin = _draw(l, seed, 4, top_p=0.665)
+    assert oid == best
+    assert abs(margin - math.log(E[2] / E[best])) < 1e-5
+    assert margin < math.log(E[1 - best] / E[best])
+
+
+def test_margin_of_a_winner_on_the_boundary():
+    """The winner survives only narrowly: (a) top-p 0.51 over two equal logits
+    keeps id 1 with its prefix sum 2 % under the boundary; (b) top-k 1 keeps id
+    0 with a 0.01 lead over the next logit.  The margin is that distance."""
+    l = np.zeros(2, np.float32)
+    dist = math.log(2.0 * float(np.float32(0.51)))
+    seed = _seed_where(lambda s: math.log(_E(s, 6, 0) / _E(s, 6, 1)) > dist, 6)
+    oid, margin = _draw(l, seed, 6, top_p=0.51)
+    assert oid == 1 and abs(margin - dist) < 1e-9
+    l = np.array([1.0, 0.99, -3.0], np.float32)
+    gap = float(np.float32(1.0)) - float(np.float32(0.99))
+    seed = _seed_where(lambda s: _E(s, 7, 1) > _E(s, 7, 0) * 1.2, 7)
+    oid, margin = _draw(l, seed, 7, top_k=1)
+    assert oid == 0 and abs(margin - gap) < 1e-9
