@@ -338,11 +338,26 @@ def run_ours(args, wl, rank, world):
             steps_done += n
             timed_steps += n
             remaining -= n
+    # time to the first frame: the prefill (prompt through the talker, selection
+    # 0), then one step (frame 0 through the predictor, selection 1); median of 3
+    pre, ttff = [], []
+    for _ in range(3):
+        barrier()
+        ev0.record(stream)
+        prefill()
+        ev1.record(stream)
+        q.step_frames(1, codes_out=codes_dev.view(-1)[: wl.batch * wl.dims.n_groups])
+        ev2 = torch.cuda.Event(enable_timing=True)
+        ev2.record(stream)
+        barrier()
+        pre.append(ev0.elapsed_time(ev1))
+        ttff.append(ev0.elapsed_time(ev2))
+    prefill_ms, ttff_ms = statistics.median(pre), statistics.median(ttff)
     (max_ms,), (all_frames,) = job_totals([total_ms], [total_frames], dev)
     res = dict(ms=max_ms, frames=all_frames, local_frames=total_frames, steps=timed_steps,
                wbytes=wbytes_total, kvbytes=kvbytes_total, kernels_per_step=kernels_per_step,
                clocks=clocks.summary(), local_ms=total_ms, flops=flops_total, ctx=(ctx_lo, ctx_hi),
-               step_path=step_path)
+               step_path=step_path, prefill_ms=prefill_ms, ttff_ms=ttff_ms)
 
     # e2e: the whole request through the C ABI from pinned host buffers, one call per step,
     # codes read back to pinned host memory after every step
@@ -434,6 +449,7 @@ def main():
                          "frac": achieved / pk["hbm_gbs"], "peak_kind": pk_kind,
                          "traffic": traffic, "algorithmic_bytes_per_step": bytes_total / max(res["steps"], 1)},
             "step_path": res["step_path"],
+            "prefill_ms": res["prefill_ms"], "time_to_first_frame_ms": res["ttff_ms"],
             "gpu_launches": res["kernels_per_step"] * res["steps"],
             "clocks": res["clocks"]}
     if "e2e" in res:
@@ -457,6 +473,7 @@ def main():
                 "workload": f"config {idx}: {wlb.name}", "batch": wlb.batch, "steps": rb["steps"],
                 "ms_per_step": rb["ms"] / max(rb["steps"], 1), "frames_per_s": job_rate(rb["frames"], sb),
                 "ctx_range": list(rb["ctx"]), "step_path": rb["step_path"],
+                "prefill_ms": rb["prefill_ms"], "time_to_first_frame_ms": rb["ttff_ms"],
                 "hbm": {"achieved": ach_hbm, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach_hbm / pk["hbm_gbs"],
                         "bytes_per_step": bb / max(rb["steps"], 1), "peak_kind": pk_kind},
                 "tensor": {"achieved": ach_tc, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",

@@ -275,3 +275,228 @@ cudaError_t launch_attention(int dtype, const float* qkv, int ldq, int M, int nq
 }
 
 }  // namespace q3
+
+namespace q3 {
+
+// ------------------------------------------------------------------ tiled causal prefill attention
+// One block: 64 consecutive prompt tokens of one row (a query tile) and one
+// KV head (its GQ = 2 q heads), over the row's cached positions 0..last.  K
+// and V are staged in shared memory 64 positions at a time and read once for
+// all 128 query rows (64 tokens x 2 heads).  Q Kt and P V run on the tensor
+// cores (mma.m16n8k16, bf16 in, fp32 accumulate) with the fp32 operands Q and
+// P as bf16 high + low parts, so the products keep fp32 accuracy; softmax is
+// online (running max and sum per query row).  Warp w owns query rows
+// 16 w .. 16 w + 15 (head w / 4, tokens 16 (w % 4) ..).
+namespace pa {
+constexpr int TQ = 64;          // tokens per query tile
+constexpr int KB = 64;          // positions per K/V block
+constexpr int KP = HD + 8;      // padded K row (bf16): fragment loads of 8 rows hit distinct banks
+constexpr int VP = KB + 8;      // padded V^T row (bf16)
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+    const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+    return a | (b << 16);
+}
+// x = hi + lo in bf16 (two elements per register)
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& h, uint32_t& l) {
+    const float h0 = __bfloat162float(__float2bfloat16_rn(x0)), h1 = __bfloat162float(__float2bfloat16_rn(x1));
+    h = pack2(h0, h1);
+    l = pack2(x0 - h0, x1 - h1);
+}
+__device__ __forceinline__ void mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                    uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+}  // namespace pa
+
+// tiles[t] = {first token m0, tokens n (1..64), row, position of token m0}
+template <typename T>
+__global__ void __launch_bounds__(256) prefill_attn_kernel(const float* __restrict__ qkv, int ldq, int nq, int nkv,
+                                                           const T* __restrict__ Kc, const T* __restrict__ Vc,
+                                                           int cap, const int4* __restrict__ tiles,
+                                                           float* __restrict__ out, int ldo, bf16* __restrict__ ohi,
+                                                           bf16* __restrict__ olo) {
+    using namespace pa;
+    constexpr int GQ = 2;
+    __shared__ __align__(16) bf16 sK[KB][KP];
+    __shared__ __align__(16) bf16 sVt[HD][VP];
+    const int4 tile = tiles[blockIdx.x];
+    const int m0 = tile.x, ntok = tile.y, row = tile.z, p0 = tile.w;
+    const int g = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, q4 = lane & 3;
+    const int hh = warp >> 2;                 // q head within the group
+    const int t0 = (warp & 3) * 16;           // first token of the warp's 16 query rows
+    const int qh = g * GQ + hh;
+    const float scale = 0.08838834764831845f; // 1/sqrt(128)
+
+    // Q fragments (A operand of Q Kt): rows t0 + gq and t0 + gq + 8, high and low parts
+    uint32_t qa[HD / 16][4], ql[HD / 16][4];
+    {
+        const int tr0 = min(t0 + gq, ntok - 1), tr1 = min(t0 + gq + 8, ntok - 1);
+        const float* q0 = qkv + (size_t)(m0 + tr0) * ldq + (size_t)qh * HD;
+        const float* q1 = qkv + (size_t)(m0 + tr1) * ldq + (size_t)qh * HD;
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks) {
+            const int d = ks * 16 + 2 * q4;
+            split2(q0[d] * scale, q0[d + 1] * scale, qa[ks][0], ql[ks][0]);
+            split2(q1[d] * scale, q1[d + 1] * scale, qa[ks][1], ql[ks][1]);
+            split2(q0[d + 8] * scale, q0[d + 9] * scale, qa[ks][2], ql[ks][2]);
+            split2(q1[d + 8] * scale, q1[d + 9] * scale, qa[ks][3], ql[ks][3]);
+        }
+    }
+    // positions of this lane's two query rows
+    const int pr0 = p0 + t0 + gq, pr1 = p0 + t0 + gq + 8;
+    float o[HD / 8][4];
+#pragma unroll
+    for (int n = 0; n < HD / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float mx0 = -INFINITY, mx1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+    const int last = p0 + ntok - 1;           // last position any query of the tile sees
+    const size_t base = ((size_t)row * nkv + g) * cap * HD;
+    for (int kb0 = 0; kb0 <= last; kb0 += KB) {
+        const int nk = min(KB, last + 1 - kb0);
+        __syncthreads();   // the previous block's K / V are no longer read
+        // stage K [pos][dim] and V^T [dim][pos] (bf16); positions past nk are zero
+        for (int i = tid; i < KB * (HD / 8); i += 256) {
+            const int j = i / (HD / 8), c = (i % (HD / 8)) * 8;
+            float kv[8], vv[8];
+            if (j < nk) {
+                load8(Kc + base + (size_t)(kb0 + j) * HD + c, kv);
+                load8(Vc + base + (size_t)(kb0 + j) * HD + c, vv);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) kv[e] = vv[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                sK[j][c + e] = __float2bfloat16_rn(kv[e]);
+                sVt[c + e][j] = __float2bfloat16_rn(vv[e]);
+            }
+        }
+        __syncthreads();
+        // S = Q Kt for the warp's 16 rows x 64 positions
+        float sc[KB / 8][4];
+#pragma unroll
+        for (int n = 0; n < KB / 8; ++n) {
+            sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+            const bf16* kr = &sK[n * 8 + gq][0];
+#pragma unroll
+            for (int ks = 0; ks < HD / 16; ++ks) {
+                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kr + ks * 16 + 2 * q4);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kr + ks * 16 + 2 * q4 + 8);
+                mma(sc[n], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+                mma(sc[n], ql[ks][0], ql[ks][1], ql[ks][2], ql[ks][3], b0, b1);
+            }
+        }
+        // causal mask and online softmax: lane holds rows gq (c0, c1) and gq + 8 (c2, c3)
+        float bm0 = -INFINITY, bm1 = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < KB / 8; ++n) {
+            const int j = kb0 + n * 8 + 2 * q4;
+            if (j > pr0 || j - kb0 >= nk) sc[n][0] = -INFINITY;
+            if (j + 1 > pr0 || j + 1 - kb0 >= nk) sc[n][1] = -INFINITY;
+            if (j > pr1 || j - kb0 >= nk) sc[n][2] = -INFINITY;
+            if (j + 1 > pr1 || j + 1 - kb0 >= nk) sc[n][3] = -INFINITY;
+            bm0 = fmaxf(bm0, fmaxf(sc[n][0], sc[n][1]));
+            bm1 = fmaxf(bm1, fmaxf(sc[n][2], sc[n][3]));
+        }
+        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, 1));
+        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, 2));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, 1));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, 2));
+        const float nm0 = fmaxf(mx0, bm0), nm1 = fmaxf(mx1, bm1);
+        // rows with nothing visible yet keep a zero state (their max stays -inf)
+        const float c0 = nm0 == -INFINITY ? 1.f : expf(mx0 - nm0);
+        const float c1 = nm1 == -INFINITY ? 1.f : expf(mx1 - nm1);
+        float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+        for (int n = 0; n < KB / 8; ++n) {
+            sc[n][0] = nm0 == -INFINITY ? 0.f : expf(sc[n][0] - nm0);
+            sc[n][1] = nm0 == -INFINITY ? 0.f : expf(sc[n][1] - nm0);
+            sc[n][2] = nm1 == -INFINITY ? 0.f : expf(sc[n][2] - nm1);
+            sc[n][3] = nm1 == -INFINITY ? 0.f : expf(sc[n][3] - nm1);
+            rs0 += sc[n][0] + sc[n][1];
+            rs1 += sc[n][2] + sc[n][3];
+        }
+        rs0 += __shfl_xor_sync(0xffffffffu, rs0, 1);
+        rs0 += __shfl_xor_sync(0xffffffffu, rs0, 2);
+        rs1 += __shfl_xor_sync(0xffffffffu, rs1, 1);
+        rs1 += __shfl_xor_sync(0xffffffffu, rs1, 2);
+        l0 = l0 * c0 + rs0;
+        l1 = l1 * c1 + rs1;
+        mx0 = nm0;
+        mx1 = nm1;
+#pragma unroll
+        for (int n = 0; n < HD / 8; ++n) { o[n][0] *= c0; o[n][1] *= c0; o[n][2] *= c1; o[n][3] *= c1; }
+        // O += P V: the S fragments of positions 16 k .. 16 k + 15 are the A fragment of step k
+#pragma unroll
+        for (int k = 0; k < KB / 16; ++k) {
+            uint32_t ph[4], pl[4];
+            split2(sc[2 * k][0], sc[2 * k][1], ph[0], pl[0]);
+            split2(sc[2 * k][2], sc[2 * k][3], ph[1], pl[1]);
+            split2(sc[2 * k + 1][0], sc[2 * k + 1][1], ph[2], pl[2]);
+            split2(sc[2 * k + 1][2], sc[2 * k + 1][3], ph[3], pl[3]);
+#pragma unroll
+            for (int n = 0; n < HD / 8; ++n) {
+                const bf16* vr = &sVt[n * 8 + gq][k * 16];
+                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(vr + 2 * q4);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(vr + 2 * q4 + 8);
+                mma(o[n], ph[0], ph[1], ph[2], ph[3], b0, b1);
+                mma(o[n], pl[0], pl[1], pl[2], pl[3], b0, b1);
+            }
+        }
+    }
+    // normalise and store rows t0 + gq (c0, c1) and t0 + gq + 8 (c2, c3)
+    const float i0 = 1.0f / l0, i1 = 1.0f / l1;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+        const int tr = t0 + gq + 8 * hr;
+        if (tr >= ntok) continue;
+        const int m = m0 + tr;
+        const float inv = hr ? i1 : i0;
+#pragma unroll
+        for (int n = 0; n < HD / 8; ++n) {
+            const int d = n * 8 + 2 * q4;
+            const float v0 = o[n][2 * hr] * inv, v1 = o[n][2 * hr + 1] * inv;
+            const size_t col = (size_t)qh * HD + d;
+            if (ohi) {
+                const bf16 h0 = __float2bfloat16_rn(v0), h1 = __float2bfloat16_rn(v1);
+                ohi[(size_t)m * nq * HD + col] = h0;
+                ohi[(size_t)m * nq * HD + col + 1] = h1;
+                olo[(size_t)m * nq * HD + col] = __float2bfloat16_rn(v0 - __bfloat162float(h0));
+                olo[(size_t)m * nq * HD + col + 1] = __float2bfloat16_rn(v1 - __bfloat162float(h1));
+            } else {
+                out[(size_t)m * ldo + col] = v0;
+                out[(size_t)m * ldo + col + 1] = v1;
+            }
+        }
+    }
+}
+
+cudaError_t launch_prefill_attention(int dtype, const float* qkv, int ldq, int M, int nq, int nkv, const void* Kc,
+                                     const void* Vc, int cap, const int4* tiles, int n_tiles, float* out, int ldo,
+                                     cudaStream_t st, const TcScratch* split) {
+    if (n_tiles <= 0) return cudaSuccess;
+    if (nq != 2 * nkv) return cudaErrorInvalidValue;
+    bf16* hi = nullptr;
+    bf16* lo = nullptr;
+    if (split) {
+        if (!tc_fits(*split, M, nq * HD)) return cudaErrorInvalidValue;
+        hi = (bf16*)split->base;
+        lo = hi + (size_t)M * nq * HD;
+    }
+    dim3 grid(n_tiles, nkv);
+    if (dtype == Q3_BF16)
+        prefill_attn_kernel<bf16><<<grid, 256, 0, st>>>(qkv, ldq, nq, nkv, (const bf16*)Kc, (const bf16*)Vc, cap,
+                                                          tiles, out, ldo, hi, lo);
+    else
+        prefill_attn_kernel<float><<<grid, 256, 0, st>>>(qkv, ldq, nq, nkv, (const float*)Kc, (const float*)Vc, cap,
+                                                           tiles, out, ldo, hi, lo);
+    return cudaGetLastError();
+}
+
+}  // namespace q3

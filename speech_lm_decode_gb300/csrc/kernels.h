@@ -81,6 +81,15 @@ cudaError_t launch_attention(int dtype, const float* qkv, int ldq, int M, int nq
                              float* part_m, float* part_l, float* part_acc, float* out, int ldo, cudaStream_t st,
                              const TcScratch* split = nullptr);
 
+// Causal attention of prompt tokens, tiled: tiles[t] = {first token, tokens
+// (1..64, consecutive positions of one row), row, position of the first};
+// every token of a tile attends to positions 0..its own of its row's cache
+// (bf16 caches: K / V enter the tensor cores exactly).  Output as in
+// launch_attention (fp32 into out, or the bf16 high / low split).
+cudaError_t launch_prefill_attention(int dtype, const float* qkv, int ldq, int M, int nq, int nkv, const void* Kc,
+                                     const void* Vc, int cap, const int4* tiles, int n_tiles, float* out, int ldo,
+                                     cudaStream_t st, const TcScratch* split = nullptr);
+
 // ---------------------------------------------------------------- sampler.cu
 size_t sampler_smem_bytes();
 cudaError_t sampler_init();

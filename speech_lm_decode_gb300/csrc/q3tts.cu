@@ -29,7 +29,7 @@ constexpr int MIN_SAMPLE_SETS = 256; // staging for q3tts_sample_logits
 struct Layout {
     size_t kvK, kvV, ckvK, ckvV, rope, rows, params, h, x, cx, tok, opA, opB, headop, qkv, pm, pl, pacc, logits,
         cplogits, t_row, t_pos, c_row, c_pos, last_row, codes, codes_stage, text, pad, err, s_params, s_logits, s_sel, s_row, s_ids, s_seen, cap_slot,
-        fparams, fctl, fpart, fll, tcs, tcs2, clpack, clxr, cllg, clparams;
+        fparams, fctl, fpart, fll, tcs, tcs2, clpack, clxr, cllg, clparams, ptiles;
     bool cl;                            // the cluster step kernel's regions are present
     size_t total;
     int mmax, kA, kB, rope_rows, frames_cap, n_sets, vmax, fsplits;
@@ -85,6 +85,7 @@ Layout make_layout(const q3tts_config& c) {
     L.c_row = take((size_t)MAX_GROUPS * 2 * B * sizeof(int));
     L.c_pos = take((size_t)MAX_GROUPS * 2 * B * sizeof(int));
     L.last_row = take((size_t)L.mmax * sizeof(int));
+    L.ptiles = take((size_t)L.mmax * 4 * sizeof(int));   // prefill attention tiles of one chunk
     L.codes = take(B * L.frames_cap * MAX_GROUPS * sizeof(int32_t));
     L.codes_stage = take(B * L.frames_cap * MAX_GROUPS * sizeof(int32_t));
     L.text = take(B * std::max(c.max_text, 1) * c.hidden * sizeof(float));
@@ -265,7 +266,10 @@ void invalidate_graph(q3tts* h) {
 }
 
 // One decoder stack over M tokens (talker or predictor), residual x [M][H].
-int enqueue_layers(q3tts* h, bool talker, int M, float* x, const int* trow, const int* tpos) {
+// tiles / n_tiles: prompt tokens of a prefill chunk, whose attention runs tiled
+// (bf16 caches); NULL for decode steps.
+int enqueue_layers(q3tts* h, bool talker, int M, float* x, const int* trow, const int* tpos,
+                   const int4* tiles = nullptr, int n_tiles = 0) {
     const q3tts_config& c = h->c;
     const q3tts_block_weights& bw = talker ? h->w.talker : h->w.cp;
     const int L = talker ? c.n_layers : c.cp_layers;
@@ -305,9 +309,16 @@ int enqueue_layers(q3tts* h, bool talker, int M, float* x, const int* trow, cons
         CK(launch_qk_rope_kv(c.dtype, qkv, nqkv, M, nq, nkv, (const float*)bw.q_norm + (size_t)l * hd,
                              (const float*)bw.k_norm + (size_t)l * hd, eps, h->p<float>(h->L.rope), h->L.rope_rows,
                              Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos, h->err(), h->st)); debug_wait(h, "launch_qk_rope_kv");
-        CK(launch_attention(c.dtype, qkv, nqkv, M, nq, nkv, Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos,
-                            splits, h->p<float>(h->L.pm), h->p<float>(h->L.pl), h->p<float>(h->L.pacc), opA, nq * hd,
-                            h->st, presplit_o ? &tcs : nullptr)); debug_wait(h, "launch_attention");
+        if (tiles && c.dtype == Q3_BF16) {
+            CK(launch_prefill_attention(c.dtype, qkv, nqkv, M, nq, nkv, Kc + l * kv_layer, Vc + l * kv_layer, cap,
+                                        tiles, n_tiles, opA, nq * hd, h->st, presplit_o ? &tcs : nullptr));
+            debug_wait(h, "launch_prefill_attention");
+        } else {
+            CK(launch_attention(c.dtype, qkv, nqkv, M, nq, nkv, Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos,
+                                splits, h->p<float>(h->L.pm), h->p<float>(h->L.pl), h->p<float>(h->L.pacc), opA,
+                                nq * hd, h->st, presplit_o ? &tcs : nullptr));
+            debug_wait(h, "launch_attention");
+        }
         CK(launch_linear(c.dtype, wo, H, nq * hd, presplit_o ? nullptr : opA, nq * hd, M, x, H, nullptr, 1, tcs, h->err(),
                          h->st)); debug_wait(h, "launch_linear");
         if (presplit) {
@@ -734,6 +745,8 @@ int q3tts_prefill(q3tts_t* h, int batch, const float* prompt, const int32_t* pro
     // prompt through the talker, in chunks of whole tokens across rows
     const int total = prompt_offsets[batch];
     std::vector<int> trow(h->L.mmax), tpos(h->L.mmax), last(h->L.mmax);
+    std::vector<int4> tiles;
+    tiles.reserve(h->L.mmax);
     std::vector<int> tok_row(total), tok_pos(total);
     for (int r = 0; r < batch; ++r)
         for (int p = prompt_offsets[r]; p < prompt_offsets[r + 1]; ++p) { tok_row[p] = r; tok_pos[p] = p - prompt_offsets[r]; }
@@ -751,8 +764,18 @@ int q3tts_prefill(q3tts_t* h, int batch, const float* prompt, const int32_t* pro
         CK(cudaMemcpyAsync(h->p<int>(h->L.t_row), trow.data(), M * sizeof(int), cudaMemcpyHostToDevice, h->st));
         CK(cudaMemcpyAsync(h->p<int>(h->L.t_pos), tpos.data(), M * sizeof(int), cudaMemcpyHostToDevice, h->st));
         CK(cudaMemcpyAsync(h->p<int>(h->L.last_row), last.data(), M * sizeof(int), cudaMemcpyHostToDevice, h->st));
+        // attention tiles: runs of up to 64 consecutive tokens of one row
+        tiles.clear();
+        for (int m = 0; m < M; ++m) {
+            if (tiles.empty() || tiles.back().z != trow[m] || tiles.back().y == 64)
+                tiles.push_back(make_int4(m, 0, trow[m], tpos[m]));
+            tiles.back().y += 1;
+        }
+        CK(cudaMemcpyAsync(h->p<int4>(h->L.ptiles), tiles.data(), tiles.size() * sizeof(int4), cudaMemcpyHostToDevice,
+                           h->st));
         CK(cudaMemcpyAsync(x, prompt + (size_t)t0 * H, (size_t)M * H * sizeof(float), cudaMemcpyDefault, h->st));
-        int r = enqueue_layers(h, true, M, x, h->p<int>(h->L.t_row), h->p<int>(h->L.t_pos));
+        int r = enqueue_layers(h, true, M, x, h->p<int>(h->L.t_row), h->p<int>(h->L.t_pos), h->p<int4>(h->L.ptiles),
+                               (int)tiles.size());
         if (r) return r;
         CK(launch_rmsnorm(x, H, M, (const float*)h->w.talker.final_norm, H, c.rms_eps, headop, H,
                           h->p<float>(h->L.h), H, h->p<int>(h->L.last_row), h->st)); debug_wait(h, "launch_rmsnorm");

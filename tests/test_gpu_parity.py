@@ -241,3 +241,18 @@ def test_cluster_kernel_wait_timeout(q3):
     q.close()
     g = run_gpu(wl, dw, inp, cap_rows=[0], step_path=q3.Q3_PATH_CLUSTER, expect_path=q3.Q3_PATH_CLUSTER)
     compare(wl, w, inp, g)
+
+
+def test_prefill_attention_tiles(q3):
+    """Prompt lengths around the 64-token attention tiles (1, 63, 64, 65, 130,
+    200) in one batch: 523 prompt tokens, so one row straddles the 512-token
+    prefill chunks.  Every selection's logits depend on the prompt's K / V."""
+    lens = [1, 63, 64, 65, 130, 200]
+    rows = [RowSampling(max_frames=4) for _ in lens]
+    rows[1] = RowSampling(max_frames=4, do_sample=1, temperature=0.9, top_k=8, cp_do_sample=1, seed=5)
+    wl = Workload("prefill tiles", synth.DIMS_SMALL, BF16, 23, len(lens), lens, [2] * len(lens), 4, rows,
+                  max(lens) + 8, norm_std=0.1)
+    w = small_weights(wl)
+    inp = synth.make_inputs(wl)
+    g = run_gpu(wl, q3.to_device_weights(w), inp, cap_rows=list(range(len(lens))))
+    compare(wl, w, inp, g)
