@@ -24,11 +24,11 @@ REASON_RUNNING, REASON_EOS, REASON_LENGTH = 0, 1, 2
 
 
 def build(force: bool = False) -> str:
-    src = os.path.join(_HERE, "oracle.cpp")
-    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(src):
+    srcs = [os.path.join(_HERE, f) for f in ("oracle.cpp", "codec.cpp")]
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < max(os.path.getmtime(f) for f in srcs):
         tmp = _SO + f".tmp{os.getpid()}"
         subprocess.check_call(["g++", "-std=c++17", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
-                               src, "-o", tmp])
+                               *srcs, "-o", tmp])
         os.replace(tmp, _SO)
     return _SO
 
@@ -92,6 +92,12 @@ def _L():
             lib.oracle_rope.argtypes = [vp, i32, i32, f32]
             lib.oracle_mrope.argtypes = [vp, i32, vp, vp, i32, f32]
             lib.oracle_attend.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp]
+            lib.oracle_codec_decode.restype = i32
+            lib.oracle_codec_decode.argtypes = [vp, vp, vp, i32, vp, vp]
+            lib.oracle_codec_attention.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp]
+            lib.oracle_codec_conv1d.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp]
+            lib.oracle_codec_conv_transpose.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp]
+            lib.oracle_codec_snake.argtypes = [vp, i32, i32, vp, vp]
             _lib = lib
     return _lib
 
