@@ -47,8 +47,11 @@ def parse():
     p.add_argument("--step-path", default="auto", choices=["auto", "graph", "frame", "cluster"],
                    help="batch-1 step path (the library's default when auto)")
     p.add_argument("--cpu-frames", type=int, default=0, help="oracle frames timed for the CPU baseline (0: auto)")
-    p.add_argument("--no-batches", action="store_true", help="skip the batch-32 / batch-256 entries")
-    p.add_argument("--batch-steps", type=int, default=20, help="timed steps of each batch entry")
+    p.add_argument("--no-batches", action="store_true", help="skip the batch entries")
+    p.add_argument("--batches", type=lambda v: [int(x) for x in v.split(",") if x], default=[4, 5, 6, 7],
+                   help="workloads of the batch entries (4, 5: batch 32 / 256 of the 0.6B shape; 6, 7: 1.7B)")
+    p.add_argument("--batch-steps", type=int, default=0,
+                   help="timed steps of each batch entry (0: the whole request after 3 warm-up steps)")
     return p.parse_args()
 
 
@@ -457,13 +460,14 @@ def main():
         line["e2e"] = {"value": job_rate(e["frames"], e["seconds"]), "unit": unit,
                        "h2d_bytes_per_step": e["h2d_per_step"], "d2h_bytes_per_step": e["d2h_per_step"],
                        "note": "prefill from pinned host + one q3tts_step_frames(1) per step, codes to pinned host"}
-    if not args.no_batches and world == 1 and args.workload not in (4, 5):
+    if not args.no_batches and world == 1 and wl.batch == 1:
         line["batches"] = []
         del w, inp
-        for idx in (4, 5):
+        for idx in args.batches:
             wlb = synth.workload(idx)
             ba = argparse.Namespace(**vars(args))
-            ba.warmup, ba.steps, ba.no_e2e, ba.step_path = 3, args.batch_steps, True, "auto"
+            ba.warmup, ba.no_e2e, ba.step_path = 3, True, "auto"
+            ba.steps = args.batch_steps or (wlb.frames - ba.warmup)
             rb, _, _ = run_ours(ba, wlb, rank, world)
             sb = rb["ms"] / 1000.0
             bb = rb["wbytes"] + rb["kvbytes"]

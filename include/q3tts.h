@@ -97,10 +97,12 @@ typedef struct {
                            report it on stderr (diagnostics, slow)             */
     int wait_limit_us;  /* bound of every device-side wait of the batch-1
                            kernels, microseconds (0: 2,000,000)                */
-    int inject_timeout; /* test only (0 = off): the cluster kernel's
-                           cross-cluster exchange with this index is never
-                           written by CTA 0, so every wait on it runs out and
-                           the step returns Q3_ERR_TIMEOUT                     */
+    int inject_timeout; /* test only (0 = off).  Frame kernel: the readers of
+                           phase n of the first step after a prefill wait for
+                           an epoch no phase writes (n < 1024).  Cluster
+                           kernel: the cross-cluster exchange with index n is
+                           never written by CTA 0.  Every wait on it runs out
+                           and the step returns Q3_ERR_TIMEOUT                 */
     int text_vocab;     /* text side (q3tts_text_embed): BPE vocabulary
                            (151936 upstream); 0 = no text path                */
     int text_hidden;    /* width of the text embedding (2048)                 */

@@ -237,6 +237,287 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restri
     }
 }
 
+// ------------------------------------------------------------------ bulk-staged decode attention (bf16 cache)
+// grid (n_splits, nkv, M), 256 threads, two CTAs per SM.  A split's cached
+// positions of one (row, kv head) are contiguous in the cache, so K and V
+// blocks of ab::P positions are each ONE cp.async.bulk into a ring of ab::NS
+// shared-memory stages (completion on an mbarrier), issued by thread 0 as far
+// ahead as the ring allows: up to 96 KB of the cache in flight per CTA.
+// Eight lanes cover one position: lane s holds dims 8s..8s+7 and 64+8s..64+8s+7
+// (each load of the group is 128 contiguous bytes of a row, no bank
+// conflict); the 32 groups take positions grp and grp + 32 of every stage and
+// keep an online softmax (max, sum, weighted V) per q head of the kv group in
+// fp32, rescaled once per stage.  Groups then warps are merged in a fixed
+// order.  One split: the normalised output (fp32, or the O projection's bf16
+// high / low operand) is written directly; more: unnormalised partials for
+// attn_combine_kernel.  A wait that runs out sets the TIMEOUT bit and the CTA
+// leaves after a bounded wait for its own copies.
+namespace ab {
+constexpr int P = 64;                 // positions per stage
+constexpr int NS = 3;                 // ring stages
+constexpr int NT = 256;
+constexpr int NG = NT / 8;            // lane groups (one position each)
+constexpr int NW = NT / 32;
+constexpr size_t RING = (size_t)2 * NS * P * HD * sizeof(bf16);
+constexpr size_t SMEM = RING + NS * sizeof(uint64_t);
+constexpr long long WAIT_CYCLES = 2000000000LL;
+static_assert(P == 2 * NG, "two positions per group and stage");
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ bool try_wait(uint64_t* b, unsigned parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(su32(b)), "r"(parity) : "memory");
+    return ok != 0;
+}
+// the lane's 16 elements of a 128-wide bf16 row in shared memory (dims 8s..8s+7, 64+8s..64+8s+7)
+__device__ __forceinline__ void row16(const bf16* row, int sub, float (&v)[16]) {
+    float a[8], b[8];
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(row + 8 * sub), a);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(row + 64 + 8 * sub), b);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { v[i] = a[i]; v[8 + i] = b[i]; }
+}
+__device__ __forceinline__ bool wait_bounded(uint64_t* b, unsigned parity) {
+    if (try_wait(b, parity)) return true;
+    const long long t0 = clock64();
+    while (!try_wait(b, parity))
+        if (clock64() - t0 > WAIT_CYCLES) return false;
+    return true;
+}
+}  // namespace ab
+
+template <int GQ>
+__global__ void __launch_bounds__(ab::NT, 2) attn_bulk_kernel(const float* __restrict__ qkv, int ldq, int nq, int nkv,
+                                                              const bf16* __restrict__ Kc, const bf16* __restrict__ Vc,
+                                                              int cap, const int* __restrict__ tok_row,
+                                                              const int* __restrict__ tok_pos, int n_splits,
+                                                              float* __restrict__ pm, float* __restrict__ pl,
+                                                              float* __restrict__ pacc, float* __restrict__ out,
+                                                              int ldo, bf16* __restrict__ hi, bf16* __restrict__ lo,
+                                                              int* __restrict__ err) {
+    using namespace ab;
+    extern __shared__ __align__(128) unsigned char ab_smem[];
+    bf16* sK = reinterpret_cast<bf16*>(ab_smem);
+    bf16* sV = sK + NS * P * HD;
+    uint64_t* full = reinterpret_cast<uint64_t*>(ab_smem + RING);
+    const int split = blockIdx.x, g = blockIdx.y, m = blockIdx.z;
+    const int pos = tok_pos[m];
+    if (pos < 0) {
+        // a skipped token: zeros in the single-split output, nothing otherwise
+        if (n_splits == 1)
+            for (int i = threadIdx.x; i < GQ * HD; i += NT) {
+                const size_t o = (size_t)g * GQ * HD + i;
+                if (hi) { hi[(size_t)m * nq * HD + o] = __float2bfloat16_rn(0.f); lo[(size_t)m * nq * HD + o] = __float2bfloat16_rn(0.f); }
+                else out[(size_t)m * ldo + o] = 0.f;
+            }
+        return;
+    }
+    if (pos >= cap) {   // the host checks capacity first; never read past the row's cache
+        if (threadIdx.x == 0) atomicOr(err, ERRB_BOUNDS);
+        return;
+    }
+    const int n = pos + 1;
+    const int chunk = (n + n_splits - 1) / n_splits;
+    const int j0 = min(n, split * chunk), j1 = min(n, j0 + chunk);
+    const int cnt = j1 - j0;
+    const int nst = (cnt + P - 1) / P;
+    const size_t base = (((size_t)tok_row[m] * nkv + g) * cap + j0) * HD;
+    const bf16* Kg = Kc + base;
+    const bf16* Vg = Vc + base;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(&full[i])), "r"(1) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    auto issue = [&](int t) {
+        const int slot = t % NS;
+        const unsigned bytes = (unsigned)min(P, cnt - t * P) * HD * (unsigned)sizeof(bf16);
+        unsigned long long st;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 %0, [%1], %2;"
+                     : "=l"(st) : "r"(su32(&full[slot])), "r"(2 * bytes) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(su32(sK + (size_t)slot * P * HD)), "l"(Kg + (size_t)t * P * HD), "r"(bytes),
+                       "r"(su32(&full[slot])) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(su32(sV + (size_t)slot * P * HD)), "l"(Vg + (size_t)t * P * HD), "r"(bytes),
+                       "r"(su32(&full[slot])) : "memory");
+    };
+    if (threadIdx.x == 0)
+        for (int t = 0; t < min(NS, nst); ++t) issue(t);
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane & 7, grp = threadIdx.x >> 3;
+    const float scale = 0.08838834764831845f;  // 1/sqrt(128)
+    float q[GQ][16], acc[GQ][16], mx[GQ], l[GQ];
+#pragma unroll
+    for (int hh = 0; hh < GQ; ++hh) {
+        const float* qs = qkv + (size_t)m * ldq + (size_t)(g * GQ + hh) * HD;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            q[hh][i] = qs[8 * sub + i] * scale;
+            q[hh][8 + i] = qs[64 + 8 * sub + i] * scale;
+        }
+        mx[hh] = -INFINITY; l[hh] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[hh][i] = 0.f;
+    }
+    int issued = min(NS, nst);
+    bool fail = false;
+    for (int t = 0; t < nst; ++t) {
+        const int slot = t % NS;
+        if (!fail && !wait_bounded(&full[slot], (unsigned)(t / NS) & 1u)) fail = true;
+        // the shuffles below need the whole warp
+        if (!__any_sync(0xffffffffu, fail)) {
+            const int c = min(P, cnt - t * P);
+            const bf16* ks = sK + (size_t)slot * P * HD;
+            const bf16* vs = sV + (size_t)slot * P * HD;
+            float s[2][GQ];
+            bool val[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int pl_ = grp + NG * r;
+                val[r] = pl_ < c;
+                float k[16];
+                if (val[r]) {
+                    row16(ks + pl_ * HD, sub, k);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) k[i] = 0.f;
+                }
+#pragma unroll
+                for (int hh = 0; hh < GQ; ++hh) {
+                    float d = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) d = fmaf(q[hh][i], k[i], d);
+                    d += __shfl_xor_sync(0xffffffffu, d, 1);
+                    d += __shfl_xor_sync(0xffffffffu, d, 2);
+                    d += __shfl_xor_sync(0xffffffffu, d, 4);
+                    s[r][hh] = d;
+                }
+            }
+            if (val[0]) {   // the group's second position exists only with its first
+                float v0[16], v1[16];
+                row16(vs + grp * HD, sub, v0);
+                if (val[1]) {
+                    row16(vs + (grp + NG) * HD, sub, v1);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v1[i] = 0.f;
+                }
+#pragma unroll
+                for (int hh = 0; hh < GQ; ++hh) {
+                    const float mn = val[1] ? fmaxf(fmaxf(mx[hh], s[0][hh]), s[1][hh]) : fmaxf(mx[hh], s[0][hh]);
+                    const float cf = expf(mx[hh] - mn);
+                    const float p0 = expf(s[0][hh] - mn);
+                    const float p1 = val[1] ? expf(s[1][hh] - mn) : 0.f;
+                    l[hh] = l[hh] * cf + p0 + p1;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[hh][i] = fmaf(p1, v1[i], fmaf(p0, v0[i], acc[hh][i] * cf));
+                    mx[hh] = mn;
+                }
+            }
+        }
+        // every thread is done with this slot: refill it
+        if (__syncthreads_or(fail)) { fail = true; break; }
+        if (threadIdx.x == 0 && issued < nst) issue(issued);
+        issued += issued < nst ? 1 : 0;
+    }
+    if (fail) {
+        if (threadIdx.x == 0) {
+            atomicOr(err, ERRB_TIMEOUT);
+            // copies in flight must land before the CTA leaves
+            for (int t = max(0, issued - NS); t < issued; ++t) ab::wait_bounded(&full[t % NS], (unsigned)(t / NS) & 1u);
+        }
+        return;
+    }
+    // merge the 4 groups of the warp (lanes sub, sub+8, sub+16, sub+24)
+#pragma unroll
+    for (int hh = 0; hh < GQ; ++hh) {
+        float ma = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 8));
+        ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 16));
+        const float cf = (ma == -INFINITY) ? 0.f : expf(mx[hh] - ma);
+        float lv = l[hh] * cf;
+        lv += __shfl_xor_sync(0xffffffffu, lv, 8);
+        lv += __shfl_xor_sync(0xffffffffu, lv, 16);
+        l[hh] = lv;
+        mx[hh] = ma;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float a = acc[hh][i] * cf;
+            a += __shfl_xor_sync(0xffffffffu, a, 8);
+            a += __shfl_xor_sync(0xffffffffu, a, 16);
+            acc[hh][i] = a;
+        }
+    }
+    // the ring is drained (every issued stage was waited on): reuse it
+    float* s_acc = reinterpret_cast<float*>(ab_smem);          // [NW][GQ][HD]
+    float* s_m = s_acc + NW * GQ * HD;                            // [NW][GQ]
+    float* s_l = s_m + NW * GQ;
+    if (lane < 8) {
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                s_acc[(warp * GQ + hh) * HD + 8 * sub + i] = acc[hh][i];
+                s_acc[(warp * GQ + hh) * HD + 64 + 8 * sub + i] = acc[hh][8 + i];
+            }
+            if (sub == 0) { s_m[warp * GQ + hh] = mx[hh]; s_l[warp * GQ + hh] = l[hh]; }
+        }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < GQ * HD; idx += NT) {
+        const int hh = idx / HD, d = idx - hh * HD;
+        float ma = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) ma = fmaxf(ma, s_m[w * GQ + hh]);
+        float lsum = 0.f, a = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float cf = (ma == -INFINITY) ? 0.f : expf(s_m[w * GQ + hh] - ma);
+            lsum += s_l[w * GQ + hh] * cf;
+            a += s_acc[(w * GQ + hh) * HD + d] * cf;
+        }
+        const size_t o = (size_t)(g * GQ + hh) * HD + d;
+        if (n_splits == 1) {
+            const float res = a / lsum;
+            if (hi) {
+                const bf16 hv = __float2bfloat16_rn(res);
+                hi[(size_t)m * nq * HD + o] = hv;
+                lo[(size_t)m * nq * HD + o] = __float2bfloat16_rn(res - __bfloat162float(hv));
+            } else {
+                out[(size_t)m * ldo + o] = res;
+            }
+        } else {
+            const size_t pi = ((size_t)m * n_splits + split) * nq + g * GQ + hh;
+            pacc[pi * HD + d] = a;
+            if (d == 0) { pm[pi] = ma; pl[pi] = lsum; }
+        }
+    }
+}
+
+template <int GQ>
+static cudaError_t attention_bulk(const float* qkv, int ldq, int M, int nq, int nkv, const bf16* Kc, const bf16* Vc,
+                                  int cap, const int* tok_row, const int* tok_pos, int n_splits, float* pm, float* pl,
+                                  float* pacc, float* out, int ldo, bf16* hi, bf16* lo, int* err, cudaStream_t st) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(attn_bulk_kernel<GQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)ab::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    attn_bulk_kernel<GQ><<<dim3(n_splits, nkv, M), ab::NT, ab::SMEM, st>>>(qkv, ldq, nq, nkv, Kc, Vc, cap, tok_row,
+                                                                          tok_pos, n_splits, pm, pl, pacc, out, ldo,
+                                                                          hi, lo, err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || n_splits == 1) return e;
+    attn_combine_kernel<<<dim3(M, nq), 128, 0, st>>>(pm, pl, pacc, n_splits, nq, tok_pos, out, ldo, hi, lo);
+    return cudaGetLastError();
+}
+
 template <typename T>
 static cudaError_t attention_impl(const float* qkv, int ldq, int M, int nq, int nkv, const T* Kc, const T* Vc, int cap,
                                   const int* tok_row, const int* tok_pos, int n_splits, float* pm, float* pl,
@@ -257,8 +538,8 @@ static cudaError_t attention_impl(const float* qkv, int ldq, int M, int nq, int 
 
 cudaError_t launch_attention(int dtype, const float* qkv, int ldq, int M, int nq, int nkv, const void* Kc,
                              const void* Vc, int cap, const int* tok_row, const int* tok_pos, int n_splits,
-                             float* part_m, float* part_l, float* part_acc, float* out, int ldo, cudaStream_t st,
-                             const TcScratch* split) {
+                             float* part_m, float* part_l, float* part_acc, float* out, int ldo, int* err,
+                             cudaStream_t st, const TcScratch* split) {
     if (M <= 0) return cudaSuccess;
     bf16* hi = nullptr;
     bf16* lo = nullptr;
@@ -267,6 +548,9 @@ cudaError_t launch_attention(int dtype, const float* qkv, int ldq, int M, int nq
         hi = (bf16*)split->base;
         lo = hi + (size_t)M * nq * HD;
     }
+    if (dtype == Q3_BF16 && nq == 2 * nkv)
+        return attention_bulk<2>(qkv, ldq, M, nq, nkv, (const bf16*)Kc, (const bf16*)Vc, cap, tok_row, tok_pos,
+                                 n_splits, part_m, part_l, part_acc, out, ldo, hi, lo, err, st);
     if (dtype == Q3_BF16)
         return attention_impl<bf16>(qkv, ldq, M, nq, nkv, (const bf16*)Kc, (const bf16*)Vc, cap, tok_row, tok_pos,
                                     n_splits, part_m, part_l, part_acc, out, ldo, hi, lo, st);

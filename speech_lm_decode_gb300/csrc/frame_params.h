@@ -64,6 +64,8 @@ struct FrameParams {
     const int* cap_slot;
     int cap_T;
     int xin_bytes;  // shared-memory bytes of the attention scratch region
+    long long wait_cycles;  // SM cycles before a device wait gives up
+    unsigned inject_ep;     // test only: waits for words of this epoch never end (0: none)
 };
 
 constexpr int FRAME_CTL_WORDS = 64;

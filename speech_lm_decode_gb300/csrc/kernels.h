@@ -73,13 +73,15 @@ cudaError_t launch_qk_rope_kv(int dtype, float* qkv, int ldq, int M, int nq, int
                               const float* k_norm, float eps, const float* rope_cs, int rope_rows, void* Kc, void* Vc,
                               int cap, const int* tok_row, const int* tok_pos, int* err, cudaStream_t st);
 // Split-KV grouped-query decode attention over positions 0..tok_pos[m] of the
-// token's row, then the combine writing the O-projection operand [M][nq*128]:
-// fp32 into out, or (split != NULL) as the bf16 high / low parts the
-// tensor-core projection reads with X = NULL.
+// token's row, then (n_splits > 1) the combine, writing the O-projection
+// operand [M][nq*128]: fp32 into out, or (split != NULL) as the bf16 high /
+// low parts the tensor-core projection reads with X = NULL.  bf16 caches with
+// two q heads per kv head stream the cache through shared memory with bulk
+// copies; a wait that runs out there sets the TIMEOUT bit of err.
 cudaError_t launch_attention(int dtype, const float* qkv, int ldq, int M, int nq, int nkv, const void* Kc,
                              const void* Vc, int cap, const int* tok_row, const int* tok_pos, int n_splits,
-                             float* part_m, float* part_l, float* part_acc, float* out, int ldo, cudaStream_t st,
-                             const TcScratch* split = nullptr);
+                             float* part_m, float* part_l, float* part_acc, float* out, int ldo, int* err,
+                             cudaStream_t st, const TcScratch* split = nullptr);
 
 // Causal attention of prompt tokens, tiled: tiles[t] = {first token, tokens
 // (1..64, consecutive positions of one row), row, position of the first};

@@ -64,7 +64,6 @@ struct Ring {
     static constexpr int TILE = 24576;
 };
 constexpr int CP_VMAX = 2048;                // predictor vocabulary bound of the frame kernel
-constexpr long long WAIT_LIMIT = 4000000000LL;  // cycles (~2 s) before a wait gives up
 constexpr int NORM_MAX = FRAME_MAX_NORM;     // widest vector an RMSNorm prologue normalizes
 constexpr int ROW_PAD = 32;                  // bytes after each bf16 weight row in the ring
 constexpr int KSMAX = 8;                     // K splits of one GEMV phase (tensor-core rows)
@@ -142,7 +141,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, unsigned parity, const Fr
     const long long t0 = clock64();
     while (!mbar_try_wait(b, parity)) {
         if (aborted(P)) return false;
-        if (clock64() - t0 > WAIT_LIMIT) {
+        if (clock64() - t0 > P.wait_cycles) {
             raise_abort(P, ERRB_TIMEOUT);
             return false;
         }
@@ -158,6 +157,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, unsigned parity, const Fr
 template <int N>
 __device__ __forceinline__ bool ll_poll(Word (&w)[N], const Word* base, int first, int step, int limit, unsigned e,
                                         const FrameParams& P) {
+    if (e == P.inject_ep) e |= 0x80000000u;   // an epoch no phase writes
 #pragma unroll
     for (int j = 0; j < N; ++j) w[j] = first + step * j < limit ? ll_ld(base + first + step * j) : ((Word)e << 32);
     long long t0 = 0;
@@ -169,7 +169,7 @@ __device__ __forceinline__ bool ll_poll(Word (&w)[N], const Word* base, int firs
         if (it == 0) t0 = clock64();
         if ((it & 15u) == 15u) {
             if (aborted(P)) return false;
-            if (clock64() - t0 > WAIT_LIMIT) {
+            if (clock64() - t0 > P.wait_cycles) {
                 raise_abort(P, ERRB_TIMEOUT);
                 return false;
             }
@@ -373,7 +373,7 @@ struct Producer {
         for (unsigned t = (seq > NSLOT ? seq - NSLOT : 0); t < seq; ++t) {
             const long long t0 = clock64();
             while (!mbar_try_wait(&s.full[t % NSLOT], (t / NSLOT) & 1))
-                if (clock64() - t0 > WAIT_LIMIT) break;
+                if (clock64() - t0 > P.wait_cycles) break;
         }
     }
 };

@@ -22,7 +22,7 @@ using namespace q3;
 namespace {
 
 constexpr size_t ALIGN = 256;
-constexpr int PREFILL_CHUNK = 512;   // prompt tokens per prefill pass
+constexpr int PREFILL_CHUNK = 8192;  // prompt tokens per prefill pass (enough token tiles to fill the GPU)
 constexpr int MAX_SPLITS = 16;       // split-KV partitions per (token, kv head)
 constexpr int MIN_SAMPLE_SETS = 256; // staging for q3tts_sample_logits
 
@@ -74,7 +74,9 @@ Layout make_layout(const q3tts_config& c) {
     L.opB = take((size_t)L.mmax * L.kB * sizeof(float));
     L.headop = take(B * c.hidden * sizeof(float));
     L.qkv = take((size_t)L.mmax * nqkv * sizeof(float));
-    const size_t np = (size_t)L.mmax * MAX_SPLITS * c.n_q_heads;
+    // split-KV partials: up to MAX_SPLITS splits for decode batches (<= 2B tokens),
+    // one split for longer prefill chunks
+    const size_t np = std::max((size_t)L.mmax, 2 * B * MAX_SPLITS) * c.n_q_heads;
     L.pm = take(np * sizeof(float));
     L.pl = take(np * sizeof(float));
     L.pacc = take(np * hd * sizeof(float));
@@ -316,7 +318,7 @@ int enqueue_layers(q3tts* h, bool talker, int M, float* x, const int* trow, cons
         } else {
             CK(launch_attention(c.dtype, qkv, nqkv, M, nq, nkv, Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos,
                                 splits, h->p<float>(h->L.pm), h->p<float>(h->L.pl), h->p<float>(h->L.pacc), opA,
-                                nq * hd, h->st, presplit_o ? &tcs : nullptr));
+                                nq * hd, h->err(), h->st, presplit_o ? &tcs : nullptr));
             debug_wait(h, "launch_attention");
         }
         CK(launch_linear(c.dtype, wo, H, nq * hd, presplit_o ? nullptr : opA, nq * hd, M, x, H, nullptr, 1, tcs, h->err(),
@@ -507,6 +509,11 @@ int upload_frame_params(q3tts* h) {
     P.ctl = h->p<unsigned>(h->L.fctl); P.err = h->err();
     P.cap_t = h->cap_t; P.cap_c = h->cap_c; P.cap_slot = h->p<int>(h->L.cap_slot); P.cap_T = h->cap_T;
     P.xin_bytes = h->frame_xin;
+    // cycles at the highest SM clock, so the wait lasts at least the limit
+    P.wait_cycles = (long long)(c.wait_limit_us > 0 ? c.wait_limit_us : 2000000) * 2070;
+    // test only: the readers of one phase of the first step after a prefill
+    // (selection 1, epochs 1024 + phase) wait for an epoch nobody writes
+    P.inject_ep = c.inject_timeout > 0 && c.inject_timeout < FRAME_MAX_PHASES ? (1u << 10) + c.inject_timeout : 0u;
     CK(cudaMemcpyAsync(h->p<FrameParams>(h->L.fparams), &P, sizeof P, cudaMemcpyHostToDevice, h->st));
     CK(cudaStreamSynchronize(h->st));
     return Q3_OK;

@@ -177,7 +177,8 @@ def _rows(batch, frames, **kw):
 
 
 def workload(idx: int) -> Workload:
-    """The five frame-loop workloads (1-based index)."""
+    """The frame-loop workloads (1-based index): the five configurations, then
+    the 1.7B shape at batch 32 (6) and batch 256 (7)."""
     if idx == 1:   # tiny oracle check, fp32
         return Workload("0.6B fp32 b1 prompt16 4 frames greedy", DIMS_06B, F32, 0, 1, [16], [0], 4,
                         _rows(1, 4), 20)
@@ -200,6 +201,23 @@ def workload(idx: int) -> Workload:
     if idx == 5:
         b = 256
         return Workload("0.6B bf16 b256 prompt256 1024 frames T0.9 k50 p0.95", DIMS_06B, BF16, 4, b,
+                        [256] * b, [64] * b, 1024,
+                        _rows(b, 1024, do_sample=1, temperature=0.9, top_k=50, top_p=0.95,
+                              cp_do_sample=1, cp_temperature=0.9, cp_top_k=50, cp_top_p=0.95), 1280)
+    # the 1.7B shape at the two batch sizes (variants of the batch-32 and
+    # batch-256 workloads above; not among the five configurations)
+    if idx == 6:
+        b = 32
+        lens = [int(v) for v in randint(b, 5, 0x4C454E, 64, 512)]
+        eos = [int(v) for v in randint(b, 5, 0x454F53, 50, 250)]
+        rows = _rows(b, 250)
+        for r in range(b):
+            rows[r].force_eos_at_frame = eos[r]
+        return Workload("1.7B bf16 b32 prompt U[64,512] 250 frames greedy forced EOS", DIMS_17B, BF16, 5, b,
+                        lens, [64] * b, 250, rows, 768)
+    if idx == 7:
+        b = 256
+        return Workload("1.7B bf16 b256 prompt256 1024 frames T0.9 k50 p0.95", DIMS_17B, BF16, 6, b,
                         [256] * b, [64] * b, 1024,
                         _rows(b, 1024, do_sample=1, temperature=0.9, top_k=50, top_p=0.95,
                               cp_do_sample=1, cp_temperature=0.9, cp_top_k=50, cp_top_p=0.95), 1280)

@@ -113,6 +113,24 @@ def test_full_size_workload(q3, idx):
     print(f"workload {idx}: frames {g.frames[rows].tolist()} reasons {g.reasons[rows].tolist()} {s}")
 
 
+@pytest.mark.parametrize("idx,upto", [(6, None), (7, 48)])
+def test_full_size_17b_batches(q3, idx, upto):
+    """The 1.7B shape (talker hidden 2048, FFN 6144, 2048->1024 predictor
+    projection) at batch 32 and batch 256, full size, in the benchmark's
+    launch configuration: rows 0 and B-1 against the oracle (batch 256: over
+    the first 48 frames), properties of every row."""
+    wl = synth.workload(idx)
+    w = synth.make_weights(wl.dims, wl.dtype, wl.weight_seed)
+    inp = synth.make_inputs(wl)
+    rows = [0, wl.batch - 1]
+    g = run_gpu(wl, q3.to_device_weights(w), inp, cap_rows=rows, expect_path=q3.Q3_PATH_GRAPH)
+    check_run_properties(wl, g)
+    s = compare(wl, w, inp, g, upto=upto)
+    s.pop("details", None)
+    assert s["checked"] >= 0.5 * s["decisions"], s
+    print(f"workload {idx}: frames {g.frames[rows].tolist()} reasons {g.reasons[rows].tolist()} {s}")
+
+
 def test_capacity_and_state_errors(q3):
     wl = small_workload(synth.DIMS_SMALL, BF16)
     w = small_weights(wl, 1.0)
@@ -223,23 +241,30 @@ def test_cluster_kernel_chunked_and_repeatable(q3):
     assert np.array_equal(a.cp_logits, c.cp_logits, equal_nan=True)
 
 
-def test_cluster_kernel_wait_timeout(q3):
-    """A device-side wait that runs out: one cross-cluster exchange is never
-    written (test-only config field), every wait on it gives up after the
-    configured 2 ms, the step returns Q3_ERR_TIMEOUT and the handle can be
-    destroyed; a fresh handle on the same GPU then matches the oracle."""
-    wl = _single_row(small_workload(synth.DIMS_CL, BF16, frames=6), 0)
+@pytest.mark.parametrize("path", ["frame", "cluster"])
+def test_batch1_wait_timeout(q3, path):
+    """A device-side wait that runs out, on each single-launch path: the
+    readers of one phase (frame kernel) or one cross-cluster exchange (cluster
+    kernel) wait for words nobody writes (test-only config field), every wait
+    gives up after the configured 2 ms, the step returns Q3_ERR_TIMEOUT and the
+    handle can be destroyed; a fresh handle on the same GPU then matches the
+    oracle."""
+    if path == "frame":
+        dims, p, inject = synth.DIMS_SMALL, q3.Q3_PATH_FRAME, 3
+    else:
+        dims, p, inject = synth.DIMS_CL, q3.Q3_PATH_CLUSTER, 3
+    wl = _single_row(small_workload(dims, BF16, frames=6), 0)
     w = small_weights(wl)
-    inp = _single_inputs(synth.make_inputs(small_workload(synth.DIMS_CL, BF16, frames=6)), 0)
+    inp = _single_inputs(synth.make_inputs(small_workload(dims, BF16, frames=6)), 0)
     dw = q3.to_device_weights(w)
-    q = q3.Q3TTS(wl.dims, wl.dtype, dw, 1, wl.max_ctx, 8, step_path=q3.Q3_PATH_CLUSTER, wait_limit_us=2000,
-                 inject_timeout=3)
+    q = q3.Q3TTS(wl.dims, wl.dtype, dw, 1, wl.max_ctx, 8, step_path=p, wait_limit_us=2000, inject_timeout=inject)
+    assert q.step_path(1) == p
     q.prefill(inp["prompt"], inp["prompt_offsets"], inp["text"], inp["text_offsets"], inp["tts_pad"], wl.rows)
     rc, codes, frames, reasons = q.step_frames(2, check=False)
     assert rc == q3.Q3_ERR_TIMEOUT, rc
     assert frames[0] == 0 and reasons[0] == q3.Q3_RUNNING
     q.close()
-    g = run_gpu(wl, dw, inp, cap_rows=[0], step_path=q3.Q3_PATH_CLUSTER, expect_path=q3.Q3_PATH_CLUSTER)
+    g = run_gpu(wl, dw, inp, cap_rows=[0], step_path=p, expect_path=p)
     compare(wl, w, inp, g)
 
 
