@@ -311,3 +311,188 @@ def sample_logits_noalloc(logits, talker: bool, params, sel_index, step: int, no
     if check and rc:
         raise Q3Error(rc, "q3tts_sample_logits_noalloc failed")
     return ids[:n] if check else (rc, ids[:n])
+
+
+# ---------------------------------------------------------------- codec decoder (q3codec.h)
+CODEC_EXPORTS = ("q3codec_workspace_bytes", "q3codec_create", "q3codec_samples_per_frame", "q3codec_decode_window",
+                 "q3codec_decode", "q3codec_stream_reset", "q3codec_stream_push", "q3codec_window_kernel_count",
+                 "q3codec_last_error", "q3codec_destroy")
+CODEC_MAX_BLOCKS = 4
+
+
+class CodecConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("n_codebooks", "codebook_size", "codebook_dim", "hidden", "n_layers",
+                                            "n_heads", "head_dim", "ffn", "window")] + \
+              [(n, ctypes.c_float) for n in ("rope_theta", "rms_eps", "ln_eps")] + \
+              [(n, ctypes.c_int) for n in ("n_up", "up_ffn", "dac_channels", "n_blocks")] + \
+              [("strides", ctypes.c_int * CODEC_MAX_BLOCKS)] + \
+              [(n, ctypes.c_int) for n in ("dtype", "max_frames", "tc_min_tokens")]
+
+
+CODEC_KEYS = ("codebooks", "proj_sem", "proj_ac", "attn_norm", "wqkv", "wo", "ls_attn", "mlp_norm", "wgu", "wd",
+              "ls_mlp", "final_norm", "up_w", "up_b", "dw_w", "dw_b", "ln_w", "ln_b", "fc1_w", "fc1_b", "fc2_w",
+              "fc2_b", "gamma", "in_w", "in_b")
+CODEC_BLOCK_KEYS = ("snake_a", "snake_b", "tconv_w", "tconv_b")
+CODEC_UNIT_KEYS = ("a1", "b1", "w1", "c1", "a2", "b2", "w2", "c2")
+
+
+class CodecWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in CODEC_KEYS] + \
+              [("blk", (ctypes.c_void_p * 4) * CODEC_MAX_BLOCKS),
+               ("unit", ((ctypes.c_void_p * 8) * 3) * CODEC_MAX_BLOCKS)] + \
+              [(n, ctypes.c_void_p) for n in ("out_a", "out_b", "out_w", "out_bias")]
+
+
+def _codec_lib():
+    L = lib()
+    if not getattr(L, "_codec_ready", False):
+        vp, i32 = ctypes.c_void_p, ctypes.c_int
+        L.q3codec_workspace_bytes.restype = ctypes.c_size_t
+        L.q3codec_workspace_bytes.argtypes = [ctypes.POINTER(CodecConfig)]
+        L.q3codec_create.argtypes = [ctypes.POINTER(CodecConfig), ctypes.POINTER(CodecWeights), vp, ctypes.c_size_t,
+                                     vp, ctypes.POINTER(vp)]
+        L.q3codec_samples_per_frame.argtypes = [vp]
+        L.q3codec_decode_window.argtypes = [vp, vp, i32, i32, vp]
+        L.q3codec_decode.argtypes = [vp, vp, i32, vp]
+        L.q3codec_stream_reset.argtypes = [vp]
+        L.q3codec_stream_push.argtypes = [vp, vp, i32, i32, vp, ctypes.c_long, ctypes.POINTER(ctypes.c_long)]
+        L.q3codec_window_kernel_count.argtypes = [vp]
+        L.q3codec_last_error.restype = ctypes.c_char_p
+        L.q3codec_last_error.argtypes = [vp]
+        L.q3codec_destroy.argtypes = [vp]
+        L._codec_ready = True
+    return L
+
+
+def make_codec_config(dims, dtype: int, max_frames: int, tc_min_tokens: int = 0) -> CodecConfig:
+    c = CodecConfig()
+    for f, _ in CodecConfig._fields_:
+        if f == "strides":
+            for i, s in enumerate(dims.strides):
+                c.strides[i] = s
+        elif f == "n_blocks":
+            c.n_blocks = len(dims.strides)
+        elif f == "dtype":
+            c.dtype = dtype
+        elif f == "max_frames":
+            c.max_frames = max_frames
+        elif f == "tc_min_tokens":
+            c.tc_min_tokens = tc_min_tokens
+        else:
+            setattr(c, f, getattr(dims, f))
+    return c
+
+
+def codec_to_device(w: dict, device="cuda") -> dict:
+    """Host decoder weights (synth layout) -> device tensors of the same layout."""
+    import torch
+
+    def dev(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            t = t.view(torch.bfloat16)
+        return t.to(device)
+    out = {k: dev(v) for k, v in w.items() if k != "blocks"}
+    out["blocks"] = [{k: ([{kk: dev(vv) for kk, vv in u.items()} for u in v] if k == "units" else dev(v))
+                      for k, v in b.items()} for b in w["blocks"]]
+    return out
+
+
+class Q3Codec:
+    """Codec decoder handle: borrowed device weights, a workspace and a stream."""
+
+    def __init__(self, dims, dtype: int, device_weights: dict, max_frames: int = 325, stream=None,
+                 tc_min_tokens: int = 0):
+        import torch
+        if len(dims.strides) > CODEC_MAX_BLOCKS:
+            raise ValueError("at most 4 vocoder blocks")
+        self._dw = device_weights
+        self.dims, self.dtype = dims, dtype
+        self.cfg = make_codec_config(dims, dtype, max_frames, tc_min_tokens)
+        L = _codec_lib()
+        nbytes = L.q3codec_workspace_bytes(ctypes.byref(self.cfg))
+        if nbytes == 0:
+            raise Q3Error(Q3_ERR_ARG, "invalid codec configuration")
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        w = CodecWeights()
+        for k in CODEC_KEYS + ("out_a", "out_b", "out_w", "out_bias"):
+            setattr(w, k, _ptr(device_weights[k]))
+        for b, blk in enumerate(device_weights["blocks"]):
+            for i, k in enumerate(CODEC_BLOCK_KEYS):
+                w.blk[b][i] = _ptr(blk[k])
+            for u, unit in enumerate(blk["units"]):
+                for i, k in enumerate(CODEC_UNIT_KEYS):
+                    w.unit[b][u][i] = _ptr(unit[k])
+        self._w = w
+        h = ctypes.c_void_p()
+        rc = L.q3codec_create(ctypes.byref(self.cfg), ctypes.byref(w), self.workspace.data_ptr(), nbytes,
+                              self.stream.cuda_stream, ctypes.byref(h))
+        if rc:
+            raise Q3Error(rc, "q3codec_create failed")
+        self.h = h.value
+        self.spf = L.q3codec_samples_per_frame(self.h)
+
+    def _check(self, rc):
+        if rc:
+            raise Q3Error(rc, _codec_lib().q3codec_last_error(self.h).decode())
+
+    def close(self):
+        if getattr(self, "h", None):
+            _codec_lib().q3codec_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _codes(self, codes):
+        if hasattr(codes, "data_ptr"):
+            return codes
+        return np.ascontiguousarray(codes, dtype=np.int32)
+
+    def decode_window(self, codes, keep_from: int = 0, out=None, check=True):
+        """codes [T, n_codebooks] int32 (numpy or torch, host or cuda) -> samples of
+        frames keep_from..T-1 (numpy float32 unless `out` is given)."""
+        codes = self._codes(codes)
+        T = int(codes.shape[0])
+        wav = np.empty((T - keep_from) * self.spf, np.float32) if out is None else out
+        rc = _codec_lib().q3codec_decode_window(self.h, _ptr(codes), T, keep_from, _ptr(wav))
+        if check:
+            self._check(rc)
+            return wav
+        return rc, wav
+
+    def decode(self, codes, out=None, check=True):
+        """A whole request on the 300/25 chunk grid."""
+        codes = self._codes(codes)
+        T = int(codes.shape[0])
+        wav = np.empty(T * self.spf, np.float32) if out is None else out
+        rc = _codec_lib().q3codec_decode(self.h, _ptr(codes), T, _ptr(wav))
+        if check:
+            self._check(rc)
+            return wav
+        return rc, wav
+
+    def stream_reset(self):
+        self._check(_codec_lib().q3codec_stream_reset(self.h))
+
+    def stream_push(self, codes, final=False, capacity=None, check=True):
+        """Append host codes [n, n_codebooks]; returns the samples sent by the
+        decodes that became due (numpy float32, possibly empty)."""
+        codes = np.ascontiguousarray(codes, dtype=np.int32).reshape(-1, self.dims.n_codebooks)
+        n = codes.shape[0]
+        cap = capacity if capacity is not None else (n + 2 * 325) * self.spf
+        buf = np.empty(max(cap, 1), np.float32)
+        got = ctypes.c_long(0)
+        rc = _codec_lib().q3codec_stream_push(self.h, codes.ctypes.data if n else None, n, int(final),
+                                              buf.ctypes.data, cap, ctypes.byref(got))
+        if check:
+            self._check(rc)
+            return buf[:got.value]
+        return rc, buf[:got.value]
+
+    def kernel_count(self) -> int:
+        return _codec_lib().q3codec_window_kernel_count(self.h)

@@ -11,7 +11,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libq3tts.so")
 SOURCES = ["linear.cu", "gemm_tc.cu", "attention.cu", "sampler.cu", "loop.cu", "persist.cu", "cluster_step.cu", "q3tts.cu",
-           "noalloc.cu"]
+           "noalloc.cu", "codec.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include"), "-I" + CSRC]
@@ -34,7 +34,7 @@ def _stale(target: str, deps) -> bool:
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
-    headers.append(os.path.join(ROOT, "include", "q3tts.h"))
+    headers += [os.path.join(ROOT, "include", f) for f in ("q3tts.h", "q3codec.h")]
     procs, objs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)

@@ -1,5 +1,5 @@
-"""The C-ABI library loads and exports every entry point include/q3tts.h
-declares (CPU only: no compute call is made)."""
+"""The C-ABI library loads and exports every entry point include/q3tts.h and
+include/q3codec.h declare (CPU only: no compute call is made)."""
 import ctypes
 import os
 import re
@@ -9,10 +9,10 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def declared_symbols():
-    src = open(os.path.join(ROOT, "include", "q3tts.h")).read()
+def declared_symbols(header="q3tts.h", prefix="q3tts_"):
+    src = open(os.path.join(ROOT, "include", header)).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(q3tts_[a-z_0-9]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(" + prefix + r"[a-z_0-9]+)\s*\(", src)))
 
 
 def test_header_declares_the_boundary():
@@ -30,6 +30,35 @@ def test_library_exports_every_declared_symbol():
     missing = [n for n in declared_symbols() if not hasattr(lib, n)]
     assert not missing, missing
     assert set(declared_symbols()) >= set(q3.EXPORTS)
+    codec = declared_symbols("q3codec.h", "q3codec_")
+    assert set(codec) == set(q3.CODEC_EXPORTS), (codec, q3.CODEC_EXPORTS)
+    missing = [n for n in codec if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_codec_workspace_and_config_validation():
+    """The decoder's configuration is checked before anything is sized: head
+    width 64, widths in multiples of 8, vocoder channels that halve evenly."""
+    import dataclasses
+    import speech_lm_decode_gb300 as q3
+    import synth.codec as sc
+    L = q3._codec_lib()
+    c = q3.make_codec_config(sc.CODEC_FULL, q3.Q3_BF16, 325)
+    n = L.q3codec_workspace_bytes(ctypes.byref(c))
+    # at least the last vocoder stage's activations: 325 frames x 1920 samples x 96 channels, fp32, twice
+    assert n > 2 * 325 * 1920 * 96 * 4
+    for bad in (dataclasses.replace(sc.CODEC_FULL, head_dim=128), dataclasses.replace(sc.CODEC_FULL, ffn=1001),
+                dataclasses.replace(sc.CODEC_FULL, dac_channels=1000), dataclasses.replace(sc.CODEC_FULL, n_up=3),
+                dataclasses.replace(sc.CODEC_FULL, strides=(8, 5, 4, 3, 2))):
+        cb = q3.make_codec_config(bad, q3.Q3_BF16, 325) if len(bad.strides) <= 4 else None
+        if cb is None:
+            continue
+        assert L.q3codec_workspace_bytes(ctypes.byref(cb)) == 0, bad
+    cb = q3.make_codec_config(sc.CODEC_FULL, q3.Q3_BF16, 0)
+    assert L.q3codec_workspace_bytes(ctypes.byref(cb)) == 0
+    h = ctypes.c_void_p()
+    w = q3.CodecWeights()
+    assert L.q3codec_create(ctypes.byref(c), ctypes.byref(w), None, 0, None, ctypes.byref(h)) == q3.Q3_ERR_ARG
 
 
 def test_workspace_size_and_config_validation():
