@@ -498,6 +498,83 @@ __global__ void __launch_bounds__(ab::NT, 2) attn_bulk_kernel(const float* __res
     }
 }
 
+// Short caches (the code predictor's 16 positions): one warp per (token, kv
+// head), lane l holding dims 4l..4l+3 of each q head; positions are walked in
+// order with the online softmax kept identically in every lane.  The fixed
+// cost of a bulk-staged CTA (barriers, copy latency, block merge) would
+// exceed this work many times over.
+template <int GQ>
+__global__ void __launch_bounds__(256) attn_short_kernel(const float* __restrict__ qkv, int ldq, int M, int nq, int nkv,
+                                                         const bf16* __restrict__ Kc, const bf16* __restrict__ Vc,
+                                                         int cap, const int* __restrict__ tok_row,
+                                                         const int* __restrict__ tok_pos, float* __restrict__ out,
+                                                         int ldo, bf16* __restrict__ hi, bf16* __restrict__ lo,
+                                                         int* __restrict__ err) {
+    const int lane = threadIdx.x & 31;
+    const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (item >= M * nkv) return;
+    const int m = item / nkv, g = item - m * nkv;
+    const int pos = tok_pos[m];
+    float acc[GQ][4];
+    float res[GQ][4];
+    if (pos >= 0 && pos < cap) {
+        const float scale = 0.08838834764831845f;  // 1/sqrt(128)
+        float q[GQ][4], mx[GQ], l[GQ];
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) {
+            const float4 qv = *reinterpret_cast<const float4*>(qkv + (size_t)m * ldq + (size_t)(g * GQ + hh) * HD + 4 * lane);
+            q[hh][0] = qv.x * scale; q[hh][1] = qv.y * scale; q[hh][2] = qv.z * scale; q[hh][3] = qv.w * scale;
+            mx[hh] = -INFINITY; l[hh] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[hh][i] = 0.f;
+        }
+        const size_t base = ((size_t)tok_row[m] * nkv + g) * cap * HD + 4 * lane;
+        for (int j = 0; j <= pos; ++j) {
+            const uint2 kr = *reinterpret_cast<const uint2*>(Kc + base + (size_t)j * HD);
+            const uint2 vr = *reinterpret_cast<const uint2*>(Vc + base + (size_t)j * HD);
+            const float k[4] = {__uint_as_float(kr.x << 16), __uint_as_float(kr.x & 0xffff0000u),
+                                __uint_as_float(kr.y << 16), __uint_as_float(kr.y & 0xffff0000u)};
+            const float v[4] = {__uint_as_float(vr.x << 16), __uint_as_float(vr.x & 0xffff0000u),
+                                __uint_as_float(vr.y << 16), __uint_as_float(vr.y & 0xffff0000u)};
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh) {
+                const float sc = warp_sum(fmaf(q[hh][0], k[0], fmaf(q[hh][1], k[1], fmaf(q[hh][2], k[2], q[hh][3] * k[3]))));
+                const float mn = fmaxf(mx[hh], sc);
+                const float cf = expf(mx[hh] - mn);
+                const float p = expf(sc - mn);
+                l[hh] = l[hh] * cf + p;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[hh][i] = fmaf(p, v[i], acc[hh][i] * cf);
+                mx[hh] = mn;
+            }
+        }
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) res[hh][i] = acc[hh][i] / l[hh];
+    } else {
+        if (pos >= cap && lane == 0) atomicOr(err, ERRB_BOUNDS);
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) res[hh][i] = 0.f;
+    }
+#pragma unroll
+    for (int hh = 0; hh < GQ; ++hh) {
+        const size_t o = (size_t)(g * GQ + hh) * HD + 4 * lane;
+        if (hi) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const bf16 hv = __float2bfloat16_rn(res[hh][i]);
+                hi[(size_t)m * nq * HD + o + i] = hv;
+                lo[(size_t)m * nq * HD + o + i] = __float2bfloat16_rn(res[hh][i] - __bfloat162float(hv));
+            }
+        } else {
+            *reinterpret_cast<float4*>(out + (size_t)m * ldo + o) = make_float4(res[hh][0], res[hh][1], res[hh][2], res[hh][3]);
+        }
+    }
+}
+
 template <int GQ>
 static cudaError_t attention_bulk(const float* qkv, int ldq, int M, int nq, int nkv, const bf16* Kc, const bf16* Vc,
                                   int cap, const int* tok_row, const int* tok_pos, int n_splits, float* pm, float* pl,
@@ -547,6 +624,11 @@ cudaError_t launch_attention(int dtype, const float* qkv, int ldq, int M, int nq
         if (!tc_fits(*split, M, nq * HD)) return cudaErrorInvalidValue;
         hi = (bf16*)split->base;
         lo = hi + (size_t)M * nq * HD;
+    }
+    if (dtype == Q3_BF16 && nq == 2 * nkv && cap <= 64 && ldo % 4 == 0) {
+        attn_short_kernel<2><<<(M * nkv + 7) / 8, 256, 0, st>>>(qkv, ldq, M, nq, nkv, (const bf16*)Kc, (const bf16*)Vc,
+                                                                cap, tok_row, tok_pos, out, ldo, hi, lo, err);
+        return cudaGetLastError();
     }
     if (dtype == Q3_BF16 && nq == 2 * nkv)
         return attention_bulk<2>(qkv, ldq, M, nq, nkv, (const bf16*)Kc, (const bf16*)Vc, cap, tok_row, tok_pos,

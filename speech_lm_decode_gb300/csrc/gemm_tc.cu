@@ -191,22 +191,49 @@ __global__ void __launch_bounds__(128, 1) umma_linear_kernel(const __grid_consta
     tc_fence_after();
     const uint32_t tmem = s.tmem;
     bool ok = true;
+    int issued = 0, committed = 0;   // stages the producer issued / the MMA issuer committed
+    // Programmatic dependent launch: the next launch in the stream may start
+    // its own setup once every CTA of this grid has started, and this grid
+    // touches nothing the previous kernel writes before griddepcontrol.wait
+    // returns (the previous grid complete, its writes visible).  Only the
+    // weights, which no kernel writes, are read before that.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0 && lane == 0) {
-        // producer: K slices of W (and of the up half) and of X
+        // producer: K slices of W (and of the up half) and of X; the first
+        // ring's worth of W is requested before the previous kernel is done
         const unsigned bytes = (unsigned)((BM * (GATED ? 2 : 1) + 2 * NT) * BK * sizeof(bf16));
-        for (int kb = 0; kb < nk && ok; ++kb) {
+        const int pre = min(nk, STAGES);
+        issued = pre;
+        for (int kb = 0; kb < pre; ++kb) {
+            mb_expect_tx(&s.full[kb], bytes);
+            const int kx = (kb0 + kb) * BK;
+            tma_2d(s.a[kb], &tmW, kx, n0, &s.full[kb]);
+            if (GATED) tma_2d(s.a2[kb], &tmW, kx, F + n0, &s.full[kb]);
+        }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        for (int kb = 0; kb < pre; ++kb) {
+            const int kx = (kb0 + kb) * BK;
+            tma_2d(s.b[kb], &tmX, kx, m0, &s.full[kb]);
+            tma_2d(s.b2[kb], &tmX2, kx, m0, &s.full[kb]);
+        }
+        for (int kb = pre; kb < nk && ok; ++kb) {
             const int st = kb % STAGES;
             const unsigned round = kb / STAGES;
-            if (round > 0 && !mb_wait(&s.empty[st], (round - 1) & 1, err)) { ok = false; break; }
+            if (!mb_wait(&s.empty[st], (round - 1) & 1, err)) { ok = false; break; }
             mb_expect_tx(&s.full[st], bytes);
             const int kx = (kb0 + kb) * BK;
             tma_2d(s.a[st], &tmW, kx, n0, &s.full[st]);
             if (GATED) tma_2d(s.a2[st], &tmW, kx, F + n0, &s.full[st]);
             tma_2d(s.b[st], &tmX, kx, m0, &s.full[st]);
             tma_2d(s.b2[st], &tmX2, kx, m0, &s.full[st]);
+            issued = kb + 1;
         }
-    } else if (warp == 1 && lane == 0) {
+    } else {
+        // everyone else starts its bounded waits only once the previous grid is done
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
+    if (warp == 1 && lane == 0) {
         // MMA issuer
         for (int kb = 0; kb < nk && ok; ++kb) {
             const int st = kb % STAGES;
@@ -227,6 +254,7 @@ __global__ void __launch_bounds__(128, 1) umma_linear_kernel(const __grid_consta
                 }
             }
             umma_commit(&s.empty[st]);
+            committed = kb + 1;
         }
         if (ok) umma_commit(&s.done);
     }
@@ -325,6 +353,16 @@ __global__ void __launch_bounds__(128, 1) umma_linear_kernel(const __grid_consta
             }
             finish(kz * per + cl, v, u);
         }
+    }
+    if (!have) {
+        // a wait ran out: nothing may still be writing this CTA's shared memory
+        // or tensor memory when it leaves (bounded waits for the copies the
+        // producer issued and for the MMAs behind the last commit)
+        if (warp == 0 && lane == 0)
+            for (int kb = max(0, issued - STAGES); kb < issued; ++kb)
+                mb_wait(&s.full[kb % STAGES], (kb / STAGES) & 1, err);
+        if (warp == 1 && lane == 0 && committed > 0)
+            mb_wait(&s.empty[(committed - 1) % STAGES], ((committed - 1) / STAGES) & 1, err);
     }
     tc_fence_before();
     __syncthreads();
@@ -476,13 +514,17 @@ cudaError_t launch_tc(const void* W, int N, int K, const float* X, int ldx, int 
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = ks;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // may overlap the previous kernel's tail (the kernel waits for it before
+    // reading anything it writes)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     bf16* ghi = nullptr;
     bf16* glo = nullptr;
     if (gsplit) {

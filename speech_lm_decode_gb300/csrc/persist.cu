@@ -740,15 +740,18 @@ struct Consumer {
                 }
             }
         } else if (!tok) {
+            // up to 12 words per thread in flight at once: one L2 round trip
+            // for inputs up to 3072 wide (attention output, SiLU(g)*u)
             const unsigned e = ep[g.src_buf];
+            constexpr int NW = 12;
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 const Word* src = g.src + (size_t)m * g.src_ld;
-                for (int i0 = tid; i0 < K && good; i0 += 4 * 256) {
-                    Word w[4];
-                    good = ll_poll<4>(w, src, i0, 256, K, e, P);
+                for (int i0 = tid; i0 < K && good; i0 += NW * 256) {
+                    Word w[NW];
+                    good = ll_poll<NW>(w, src, i0, 256, K, e, P);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
+                    for (int q = 0; q < NW; ++q)
                         if (i0 + q * 256 < K) put_x(m, i0 + q * 256, val_of(w[q]));
                 }
             }
