@@ -7,11 +7,14 @@ the next talker input is assembled, the 28-layer talker runs and codebook 0
 is selected.  Metric: 16-code frames per second (frames emitted by all rows).
 
 Default workload: 0.6B-shaped model in bf16, batch 1, 128-row prompt, 64 text
-rows then tts_pad, 100 greedy frames (the latency path).  --workload 3/4/5
-select the 1.7B batch-1, batch-32 and batch-256 workloads.  With one rank the
-line also carries "batches": the batch-32 and batch-256 workloads (4 and 5)
-timed in the same run over a short window of steps, each with its HBM and
-tensor-pipe fractions (--no-batches skips them).
+rows then tts_pad, 100 greedy frames (the latency path).  --workload 3..7
+select the 1.7B batch-1, the 0.6B batch-32 and batch-256, and the 1.7B
+batch-32 and batch-256 workloads.  With one rank and a batch-1 workload the
+line also carries "batches": workloads 4..7 (--batches) timed in the same run,
+each over its whole request after 3 warm-up steps, with HBM and tensor-pipe
+fractions, prefill time and time to the first frame (--no-batches skips
+them); and "codec": one 325-frame window of the full-size codec decoder
+(--no-codec skips it).
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle instead.
 """
@@ -48,6 +51,7 @@ def parse():
                    help="batch-1 step path (the library's default when auto)")
     p.add_argument("--cpu-frames", type=int, default=0, help="oracle frames timed for the CPU baseline (0: auto)")
     p.add_argument("--no-batches", action="store_true", help="skip the batch entries")
+    p.add_argument("--no-codec", action="store_true", help="skip the codec-decoder entry")
     p.add_argument("--batches", type=lambda v: [int(x) for x in v.split(",") if x], default=[4, 5, 6, 7],
                    help="workloads of the batch entries (4, 5: batch 32 / 256 of the 0.6B shape; 6, 7: 1.7B)")
     p.add_argument("--batch-steps", type=int, default=0,
@@ -206,6 +210,81 @@ def peaks():
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
     except OSError:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---------------------------------------------------------------- codec decoder
+def codec_flops(d) -> float:
+    """Algorithmic FLOPs (2 per multiply-add) of decoding one frame: every
+    weight use once (convolutions as their multiply-adds)."""
+    D, F, F2, Dc = d.hidden, d.ffn, d.up_ffn, d.codebook_dim
+    f = 2 * D * Dc + d.n_layers * (3 * D * D + D * D + 2 * F * D + D * F)
+    n = 1
+    for _ in range(d.n_up):
+        f += n * 2 * D * D
+        n *= 2
+        f += n * 2 * F2 * D
+    C = d.dac_channels
+    f += n * C * 7 * D
+    for s in d.strides:
+        Co = C // 2
+        f += n * s * Co * 2 * C
+        n *= s
+        C = Co
+        f += 3 * n * (7 * C * C + C * C)
+    f += n * 7 * C
+    return 2.0 * f
+
+
+def run_codec(args, pk, pk_kind):
+    """One 325-frame window (a 300-frame chunk + 25 frames of context) of the
+    full-size decoder, device-resident codes: median of timed decodes."""
+    import torch
+    import speech_lm_decode_gb300 as q3
+    import synth.codec as sc
+    d = sc.CODEC_FULL
+    T = 325
+    w = sc.make_codec_weights(d, synth.BF16, 3)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    dec = q3.Q3Codec(d, synth.BF16, q3.codec_to_device(w, dev), max_frames=T, stream=stream)
+    codes = torch.from_numpy(sc.make_codes(d, T, 4)).to(dev)
+    out = torch.empty(T * dec.spf, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        dec.decode_window(codes, out=out)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    clocks = ClockSampler(dev.index)
+    with clocks:
+        for _ in range(7):
+            torch.cuda.synchronize(dev)
+            ev0.record(stream)
+            dec.decode_window(codes, out=out)
+            ev1.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(ev0.elapsed_time(ev1))
+    ms = statistics.median(times)
+    fl = codec_flops(d) * T
+    ach = fl / (ms / 1000.0) / 1e12
+    res = {"workload": f"codec decoder, one {T}-frame window (300-frame chunk + 25 frames of context), bf16, "
+                       f"{dec.spf} samples per frame",
+           "ms_per_window": ms, "frames_per_s": T / (ms / 1000.0), "samples_per_s": T * dec.spf / (ms / 1000.0),
+           "real_time_factor": (T * 0.08) / (ms / 1000.0),
+           "tensor": {"achieved": ach, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                      "frac": ach / pk["bf16_tflops_sustained"], "flops_per_window": fl,
+                      "peak_kind": pk_kind + " (sustained)",
+                      "note": "one bf16 product per weight use; the MMAs run the fp32 operand as bf16 high + low "
+                              "parts, twice that work"},
+           "gpu_launches_per_window": dec.kernel_count(), "clocks": clocks.summary()}
+    dec.close()
+    if not args.no_cpu_baseline:
+        import oracle.codec as oc
+        ora = oc.Decoder(d, w)
+        t0 = time.perf_counter()
+        ora.decode_window(sc.make_codes(d, 3, 4))
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": 3 / dt, "unit": "frames/s", "cores": omp_threads(), "kind": "oracle",
+                               "sample": f"a 3-frame window of the same decoder, {dt:.1f} s"}
+    return res
 
 
 # ---------------------------------------------------------------- oracle (CPU baseline / reference arm)
@@ -491,6 +570,8 @@ def main():
             torch.cuda.empty_cache()
         w = synth.make_weights(wl.dims, wl.dtype, wl.weight_seed) if not args.no_cpu_baseline else None
         inp = synth.make_inputs(wl) if not args.no_cpu_baseline else None
+    if not args.no_codec and world == 1 and wl.batch == 1:
+        line["codec"] = run_codec(args, pk, pk_kind)
     if not args.no_cpu_baseline and world == 1:
         n = args.cpu_frames or (20 if wl.dims.hidden <= 1024 else 10)
         rate, done, dt, _ = oracle_rate(wl, w, inp, n)
