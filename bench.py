@@ -52,6 +52,9 @@ def parse():
     p.add_argument("--cpu-frames", type=int, default=0, help="oracle frames timed for the CPU baseline (0: auto)")
     p.add_argument("--no-batches", action="store_true", help="skip the batch entries")
     p.add_argument("--no-codec", action="store_true", help="skip the codec-decoder entry")
+    p.add_argument("--profile-case", action="store_true",
+                   help="no benchmark: prefill and 6 steps of the workload with 4 talker layers and a "
+                        "context of 320 (full-size launch shapes on a small device footprint, for ncu)")
     p.add_argument("--batches", type=lambda v: [int(x) for x in v.split(",") if x], default=[4, 5, 6, 7],
                    help="workloads of the batch entries (4, 5: batch 32 / 256 of the 0.6B shape; 6, 7: 1.7B)")
     p.add_argument("--batch-steps", type=int, default=0,
@@ -470,8 +473,33 @@ def run_ours(args, wl, rank, world):
     return res, w, inp
 
 
+def profile_case(args):
+    """The workload's launches at full width and batch on a small footprint:
+    4 talker layers, a 320-position cache, a prefill and 6 steps."""
+    import dataclasses
+    import torch
+    import speech_lm_decode_gb300 as q3
+    wl = synth.workload(args.workload)
+    wl = dataclasses.replace(wl, dims=dataclasses.replace(wl.dims, n_layers=4), frames=12,
+                             max_ctx=max(wl.prompt_lens) + 64,
+                             rows=[dataclasses.replace(r, max_frames=12) for r in wl.rows])
+    dev = torch.device("cuda", 0)
+    w = synth.make_weights(wl.dims, wl.dtype, wl.weight_seed)
+    inp = synth.make_inputs(wl)
+    q = q3.Q3TTS(wl.dims, wl.dtype, q3.to_device_weights(w, dev), wl.batch, wl.max_ctx, max(wl.n_text))
+    d_inp = {k: (torch.from_numpy(v).to(dev) if k in ("prompt", "text", "tts_pad") else v) for k, v in inp.items()}
+    q.prefill(d_inp["prompt"], inp["prompt_offsets"], d_inp["text"], inp["text_offsets"], d_inp["tts_pad"], wl.rows)
+    _, frames, _ = q.step_frames(6)
+    torch.cuda.synchronize()
+    q.close()
+    print("profile case done:", wl.name, "with 4 talker layers,", int(frames.sum()), "frames")
+
+
 def main():
     args = parse()
+    if args.profile_case:
+        profile_case(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     wl = synth.workload(args.workload)

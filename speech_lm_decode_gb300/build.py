@@ -61,6 +61,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def build_calibration() -> str:
+    """The GEMM shape calibration tool (calibrate_gemm.cu; not part of the
+    library): gemm_tc.cu and linear.cu compiled with Q3_GEMM_CALIBRATION."""
+    os.makedirs(BUILD, exist_ok=True)
+    out = os.path.join(BUILD, "calibrate_gemm")
+    srcs = [os.path.join(HERE, "calibrate_gemm.cu"), os.path.join(CSRC, "gemm_tc.cu"), os.path.join(CSRC, "linear.cu")]
+    subprocess.check_call([nvcc()] + ARCH + FLAGS + ["-DQ3_GEMM_CALIBRATION", "-o", out] + srcs + ["-lcuda"])
+    return out
+
+
 if __name__ == "__main__":
     build(force="--force" in sys.argv, verbose="-v" in sys.argv)
     print(LIB)

@@ -529,23 +529,35 @@ __global__ void __launch_bounds__(256) attn_short_kernel(const float* __restrict
             for (int i = 0; i < 4; ++i) acc[hh][i] = 0.f;
         }
         const size_t base = ((size_t)tok_row[m] * nkv + g) * cap * HD + 4 * lane;
-        for (int j = 0; j <= pos; ++j) {
-            const uint2 kr = *reinterpret_cast<const uint2*>(Kc + base + (size_t)j * HD);
-            const uint2 vr = *reinterpret_cast<const uint2*>(Vc + base + (size_t)j * HD);
-            const float k[4] = {__uint_as_float(kr.x << 16), __uint_as_float(kr.x & 0xffff0000u),
-                                __uint_as_float(kr.y << 16), __uint_as_float(kr.y & 0xffff0000u)};
-            const float v[4] = {__uint_as_float(vr.x << 16), __uint_as_float(vr.x & 0xffff0000u),
-                                __uint_as_float(vr.y << 16), __uint_as_float(vr.y & 0xffff0000u)};
+        // eight positions' loads in flight before their arithmetic
+        constexpr int U = 8;
+        for (int j0 = 0; j0 <= pos; j0 += U) {
+            uint2 kr[U], vr[U];
 #pragma unroll
-            for (int hh = 0; hh < GQ; ++hh) {
-                const float sc = warp_sum(fmaf(q[hh][0], k[0], fmaf(q[hh][1], k[1], fmaf(q[hh][2], k[2], q[hh][3] * k[3]))));
-                const float mn = fmaxf(mx[hh], sc);
-                const float cf = expf(mx[hh] - mn);
-                const float p = expf(sc - mn);
-                l[hh] = l[hh] * cf + p;
+            for (int u = 0; u < U; ++u) {
+                if (j0 + u <= pos) {
+                    kr[u] = *reinterpret_cast<const uint2*>(Kc + base + (size_t)(j0 + u) * HD);
+                    vr[u] = *reinterpret_cast<const uint2*>(Vc + base + (size_t)(j0 + u) * HD);
+                }
+            }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) acc[hh][i] = fmaf(p, v[i], acc[hh][i] * cf);
-                mx[hh] = mn;
+            for (int u = 0; u < U; ++u) {
+                if (j0 + u > pos) break;   // uniform over the warp (one token per warp)
+                const float k[4] = {__uint_as_float(kr[u].x << 16), __uint_as_float(kr[u].x & 0xffff0000u),
+                                    __uint_as_float(kr[u].y << 16), __uint_as_float(kr[u].y & 0xffff0000u)};
+                const float v[4] = {__uint_as_float(vr[u].x << 16), __uint_as_float(vr[u].x & 0xffff0000u),
+                                    __uint_as_float(vr[u].y << 16), __uint_as_float(vr[u].y & 0xffff0000u)};
+#pragma unroll
+                for (int hh = 0; hh < GQ; ++hh) {
+                    const float sc = warp_sum(fmaf(q[hh][0], k[0], fmaf(q[hh][1], k[1], fmaf(q[hh][2], k[2], q[hh][3] * k[3]))));
+                    const float mn = fmaxf(mx[hh], sc);
+                    const float cf = expf(mx[hh] - mn);
+                    const float p = expf(sc - mn);
+                    l[hh] = l[hh] * cf + p;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[hh][i] = fmaf(p, v[i], acc[hh][i] * cf);
+                    mx[hh] = mn;
+                }
             }
         }
 #pragma unroll

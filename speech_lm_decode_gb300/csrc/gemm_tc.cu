@@ -192,12 +192,11 @@ __global__ void __launch_bounds__(128, 1) umma_linear_kernel(const __grid_consta
     const uint32_t tmem = s.tmem;
     bool ok = true;
     int issued = 0, committed = 0;   // stages the producer issued / the MMA issuer committed
-    // Programmatic dependent launch: the next launch in the stream may start
-    // its own setup once every CTA of this grid has started, and this grid
-    // touches nothing the previous kernel writes before griddepcontrol.wait
-    // returns (the previous grid complete, its writes visible).  Only the
-    // weights, which no kernel writes, are read before that.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Programmatic dependent launch: this grid touches nothing the previous
+    // kernel writes before griddepcontrol.wait returns (the previous grid
+    // complete, its writes visible); only the weights, which no kernel
+    // writes, are read before that.  The next launch may start once every CTA
+    // of this grid has finished its main loop (below).
 
     if (warp == 0 && lane == 0) {
         // producer: K slices of W (and of the up half) and of X; the first
@@ -261,6 +260,8 @@ __global__ void __launch_bounds__(128, 1) umma_linear_kernel(const __grid_consta
     __syncwarp();
     // epilogue: warp w owns TMEM lanes 32w..32w+31 (weight rows n0+32w..)
     const bool have = __all_sync(0xffffffffu, mb_wait(&s.done, 0, err));
+    // the operand stream is done: the next kernel may set up and request its weights
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     tc_fence_after();
     const int row = warp * 32 + lane;
     const int n = n0 + row;
@@ -454,15 +455,22 @@ int resident_ctas(int ks) {
     return ks == 1 ? device_sm_count() : cluster_capacity<NT, GATED>(ks) * ks;
 }
 
-// Cost of an NT-wide tile shape split ks ways: each CTA streams its operand
-// bytes at a rate limited by its in-flight ring, so the time goes with the
-// waves times the K blocks (stage bytes) of one CTA.  Returns the best ks and
-// its cost.
+// Time (microseconds) of an NT-wide tile shape split ks ways, a model fitted
+// to CUDA-event timings of this kernel on the GB300 over the projection shapes
+// of the frame loop and the prefill (M = 16..8192 tokens, N = 1024..6144
+// rows, K = 1024..6144; every tile width and split): each CTA streams its
+// operands at about 80 GB/s (its ring in flight), a wave costs 0.5 us more,
+// and a split's reduction pushes the fp32 accumulator through distributed
+// shared memory at about 20 GB/s per CTA.  Clusters of 2 / 4 / 8 CTAs keep at
+// most 136 / 112 / 96 CTAs busy (fewer if the occupancy query says so).
+// Over the calibration set this picks within 2 % of the best shape on
+// average (worst 17 %).  Returns the best ks and its cost.
 template <int NT, bool GATED>
 double best_split(int nrows, int M, int K, int* ks_out) {
     constexpr int H2 = GATED ? 2 : 1;
     constexpr size_t stage = (size_t)(BM * H2 + 2 * NT) * BK * sizeof(bf16);
     constexpr size_t ring = (size_t)stages_for(NT, GATED) * stage;
+    constexpr double per_wave_us = 0.5, stream_bytes_per_us = 80e3, reduce_bytes_per_us = 20e3;
     const int tiles = ((nrows + BM - 1) / BM) * ((M + NT - 1) / NT);
     const int nk = (K + BK - 1) / BK;
     double best = 1e300;
@@ -471,12 +479,13 @@ double best_split(int nrows, int M, int K, int* ks_out) {
         if (ks > 1 && ks > nk / 2) continue;
         const int per = (NT / 16 + ks - 1) / ks * 16;
         if (ks > 1 && (size_t)ks * H2 * BM * (per + 4) * sizeof(float) > ring) continue;   // inbox must fit
-        const int res = resident_ctas<NT, GATED>(ks);
+        int res = resident_ctas<NT, GATED>(ks);
         if (res <= 0) continue;
+        if (ks > 1) res = std::min(res, ks == 2 ? 136 : ks == 4 ? 112 : 96);
         const int kbs = (nk + ks - 1) / ks;
         const int waves = (tiles * ks + res - 1) / res;
-        // a split adds its reduction: about one more stage of traffic
-        const double cost = (double)waves * (kbs + (ks > 1 ? 1 : 0)) * (double)stage;
+        double cost = waves * (per_wave_us + kbs * (double)stage / stream_bytes_per_us);
+        if (ks > 1) cost += waves * ((double)H2 * BM * NT * sizeof(float) / reduce_bytes_per_us);
         if (cost < best) { best = cost; *ks_out = ks; }
     }
     return best;
@@ -536,9 +545,23 @@ cudaError_t launch_tc(const void* W, int N, int K, const float* X, int ldx, int 
                               accumulate, F, G, ldg, ghi, glo, kbs, err);
 }
 
+}  // namespace
+
+#ifdef Q3_GEMM_CALIBRATION
+// Calibration builds only (calibrate_gemm.cu times every tile width and split
+// the model chooses among): a forced shape, and whether a shape is legal.
+int g_force_nt = -1, g_force_ks = 1;
+bool tc_shape_ok(int NT, int ks, bool gated, int K);
+#endif
+
+namespace {
+
 // Tile width and K split of least cost among the widths the tokens allow.
 template <bool GATED>
 void pick_shape(int nrows, int M, int K, int* nt, int* ks) {
+#ifdef Q3_GEMM_CALIBRATION
+    if (g_force_nt > 0) { *nt = g_force_nt; *ks = g_force_ks; return; }
+#endif
     double best = 1e300;
     for (int w : {128, 64, 32}) {
         if (w > 32 && w > ((M + 31) / 32) * 32) continue;
@@ -552,6 +575,25 @@ void pick_shape(int nrows, int M, int K, int* nt, int* ks) {
 }  // namespace
 
 bool tc_available() { return encode_fn() != nullptr; }
+
+#ifdef Q3_GEMM_CALIBRATION
+// the split-K inbox must fit the ring, every split needs two K blocks, and the
+// cluster shape must be able to run
+bool tc_shape_ok(int NT, int ks, bool gated, int K) {
+    const int nk = (K + BK - 1) / BK;
+    if (ks > 1 && ks > nk / 2) return false;
+    if (ks == 1) return true;
+    const int H2 = gated ? 2 : 1;
+    const int per = (NT / 16 + ks - 1) / ks * 16;
+    const int st = NT == 128 ? stages_for(128, gated) : NT == 64 ? stages_for(64, gated) : stages_for(32, gated);
+    const size_t stage = (size_t)(BM * H2 + 2 * NT) * BK * 2;
+    if ((size_t)ks * H2 * BM * (per + 4) * 4 > (size_t)st * stage) return false;
+    const int cap = NT == 128 ? (gated ? cluster_capacity<128, true>(ks) : cluster_capacity<128, false>(ks))
+                  : NT == 64 ? (gated ? cluster_capacity<64, true>(ks) : cluster_capacity<64, false>(ks))
+                             : (gated ? cluster_capacity<32, true>(ks) : cluster_capacity<32, false>(ks));
+    return cap > 0;
+}
+#endif
 
 cudaError_t launch_linear_tc(const void* W, int N, int K, const float* X, int ldx, int M, float* Y, int ldy,
                              const float* bias, int accumulate, const TcScratch& tc, int* err, cudaStream_t st) {
