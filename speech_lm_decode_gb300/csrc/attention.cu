@@ -9,6 +9,7 @@
 // section 2), causal softmax over positions 0..pos.
 #include "common.cuh"
 #include "kernels.h"
+#include "pdl.cuh"
 
 namespace q3 {
 
@@ -22,6 +23,8 @@ __global__ void qk_rope_kv_kernel(float* __restrict__ qkv, int ldq, int nq, int 
                                   const float* __restrict__ kn, float eps, const float2* __restrict__ rope,
                                   int rope_rows, T* __restrict__ Kc, T* __restrict__ Vc, int cap,
                                   const int* __restrict__ tok_row, const int* __restrict__ tok_pos, int* err) {
+    pdl_wait();
+    pdl_trigger();
     const int m = blockIdx.x;
     const int pos = tok_pos[m];
     if (pos < 0) return;
@@ -71,10 +74,10 @@ cudaError_t launch_qk_rope_kv(int dtype, float* qkv, int ldq, int M, int nq, int
     if (M <= 0) return cudaSuccess;
     const int threads = 32 * (nq + nkv);
     if (dtype == Q3_BF16)
-        qk_rope_kv_kernel<bf16><<<M, threads, 0, st>>>(qkv, ldq, nq, nkv, q_norm, k_norm, eps, (const float2*)rope_cs,
+        launch_pdl(qk_rope_kv_kernel<bf16>, M, threads, 0, st, qkv, ldq, nq, nkv, q_norm, k_norm, eps, (const float2*)rope_cs,
                                                        rope_rows, (bf16*)Kc, (bf16*)Vc, cap, tok_row, tok_pos, err);
     else
-        qk_rope_kv_kernel<float><<<M, threads, 0, st>>>(qkv, ldq, nq, nkv, q_norm, k_norm, eps,
+        launch_pdl(qk_rope_kv_kernel<float>, M, threads, 0, st, qkv, ldq, nq, nkv, q_norm, k_norm, eps,
                                                         (const float2*)rope_cs, rope_rows, (float*)Kc, (float*)Vc, cap,
                                                         tok_row, tok_pos, err);
     return cudaGetLastError();
@@ -93,6 +96,8 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const float* __restrict
                                                          const int* __restrict__ tok_pos, int n_splits,
                                                          float* __restrict__ pm, float* __restrict__ pl,
                                                          float* __restrict__ pacc) {
+    pdl_wait();
+    pdl_trigger();
     const int split = blockIdx.x, g = blockIdx.y, m = blockIdx.z;
     const int pos = tok_pos[m];
     if (pos < 0) return;
@@ -212,6 +217,8 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restri
                                                            const float* __restrict__ pacc, int n_splits, int nq,
                                                            const int* __restrict__ tok_pos, float* __restrict__ out,
                                                            int ldo, bf16* __restrict__ hi, bf16* __restrict__ lo) {
+    pdl_wait();
+    pdl_trigger();
     const int m = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
     float res = 0.f;
     if (tok_pos[m] >= 0) {
@@ -297,6 +304,8 @@ __global__ void __launch_bounds__(ab::NT, 2) attn_bulk_kernel(const float* __res
                                                               float* __restrict__ pacc, float* __restrict__ out,
                                                               int ldo, bf16* __restrict__ hi, bf16* __restrict__ lo,
                                                               int* __restrict__ err) {
+    pdl_wait();
+    pdl_trigger();
     using namespace ab;
     extern __shared__ __align__(128) unsigned char ab_smem[];
     bf16* sK = reinterpret_cast<bf16*>(ab_smem);
@@ -510,6 +519,8 @@ __global__ void __launch_bounds__(256) attn_short_kernel(const float* __restrict
                                                          const int* __restrict__ tok_pos, float* __restrict__ out,
                                                          int ldo, bf16* __restrict__ hi, bf16* __restrict__ lo,
                                                          int* __restrict__ err) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (item >= M * nkv) return;
@@ -598,12 +609,12 @@ static cudaError_t attention_bulk(const float* qkv, int ldq, int M, int nq, int 
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    attn_bulk_kernel<GQ><<<dim3(n_splits, nkv, M), ab::NT, ab::SMEM, st>>>(qkv, ldq, nq, nkv, Kc, Vc, cap, tok_row,
+    launch_pdl(attn_bulk_kernel<GQ>, dim3(n_splits, nkv, M), ab::NT, ab::SMEM, st, qkv, ldq, nq, nkv, Kc, Vc, cap, tok_row,
                                                                           tok_pos, n_splits, pm, pl, pacc, out, ldo,
                                                                           hi, lo, err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || n_splits == 1) return e;
-    attn_combine_kernel<<<dim3(M, nq), 128, 0, st>>>(pm, pl, pacc, n_splits, nq, tok_pos, out, ldo, hi, lo);
+    launch_pdl(attn_combine_kernel, dim3(M, nq), 128, 0, st, pm, pl, pacc, n_splits, nq, tok_pos, out, ldo, hi, lo);
     return cudaGetLastError();
 }
 
@@ -614,14 +625,14 @@ static cudaError_t attention_impl(const float* qkv, int ldq, int M, int nq, int 
     dim3 grid(n_splits, nkv, M);
     const int gq = nq / nkv;
     switch (gq) {
-        case 1: attn_split_kernel<T, 1><<<grid, 128, 0, st>>>(qkv, ldq, nq, nkv, Kc, Vc, cap, tok_row, tok_pos, n_splits, pm, pl, pacc); break;
-        case 2: attn_split_kernel<T, 2><<<grid, 128, 0, st>>>(qkv, ldq, nq, nkv, Kc, Vc, cap, tok_row, tok_pos, n_splits, pm, pl, pacc); break;
-        case 4: attn_split_kernel<T, 4><<<grid, 128, 0, st>>>(qkv, ldq, nq, nkv, Kc, Vc, cap, tok_row, tok_pos, n_splits, pm, pl, pacc); break;
+        case 1: launch_pdl(attn_split_kernel<T, 1>, grid, 128, 0, st, qkv, ldq, nq, nkv, Kc, Vc, cap, tok_row, tok_pos, n_splits, pm, pl, pacc); break;
+        case 2: launch_pdl(attn_split_kernel<T, 2>, grid, 128, 0, st, qkv, ldq, nq, nkv, Kc, Vc, cap, tok_row, tok_pos, n_splits, pm, pl, pacc); break;
+        case 4: launch_pdl(attn_split_kernel<T, 4>, grid, 128, 0, st, qkv, ldq, nq, nkv, Kc, Vc, cap, tok_row, tok_pos, n_splits, pm, pl, pacc); break;
         default: return cudaErrorInvalidValue;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    attn_combine_kernel<<<dim3(M, nq), 128, 0, st>>>(pm, pl, pacc, n_splits, nq, tok_pos, out, ldo, hi, lo);
+    launch_pdl(attn_combine_kernel, dim3(M, nq), 128, 0, st, pm, pl, pacc, n_splits, nq, tok_pos, out, ldo, hi, lo);
     return cudaGetLastError();
 }
 
@@ -638,7 +649,7 @@ cudaError_t launch_attention(int dtype, const float* qkv, int ldq, int M, int nq
         lo = hi + (size_t)M * nq * HD;
     }
     if (dtype == Q3_BF16 && nq == 2 * nkv && cap <= 64 && ldo % 4 == 0) {
-        attn_short_kernel<2><<<(M * nkv + 7) / 8, 256, 0, st>>>(qkv, ldq, M, nq, nkv, (const bf16*)Kc, (const bf16*)Vc,
+        launch_pdl(attn_short_kernel<2>, (M * nkv + 7) / 8, 256, 0, st, qkv, ldq, M, nq, nkv, (const bf16*)Kc, (const bf16*)Vc,
                                                                 cap, tok_row, tok_pos, out, ldo, hi, lo, err);
         return cudaGetLastError();
     }
@@ -698,6 +709,8 @@ __global__ void __launch_bounds__(256) prefill_attn_kernel(const float* __restri
                                                            int cap, const int4* __restrict__ tiles,
                                                            float* __restrict__ out, int ldo, bf16* __restrict__ ohi,
                                                            bf16* __restrict__ olo) {
+    pdl_wait();
+    pdl_trigger();
     using namespace pa;
     constexpr int GQ = 2;
     __shared__ __align__(16) bf16 sK[KB][KP];
@@ -869,10 +882,10 @@ cudaError_t launch_prefill_attention(int dtype, const float* qkv, int ldq, int M
     }
     dim3 grid(n_tiles, nkv);
     if (dtype == Q3_BF16)
-        prefill_attn_kernel<bf16><<<grid, 256, 0, st>>>(qkv, ldq, nq, nkv, (const bf16*)Kc, (const bf16*)Vc, cap,
+        launch_pdl(prefill_attn_kernel<bf16>, grid, 256, 0, st, qkv, ldq, nq, nkv, (const bf16*)Kc, (const bf16*)Vc, cap,
                                                           tiles, out, ldo, hi, lo);
     else
-        prefill_attn_kernel<float><<<grid, 256, 0, st>>>(qkv, ldq, nq, nkv, (const float*)Kc, (const float*)Vc, cap,
+        launch_pdl(prefill_attn_kernel<float>, grid, 256, 0, st, qkv, ldq, nq, nkv, (const float*)Kc, (const float*)Vc, cap,
                                                            tiles, out, ldo, hi, lo);
     return cudaGetLastError();
 }

@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "pdl.cuh"
 
 #include <algorithm>
 
@@ -298,7 +299,62 @@ __global__ void __launch_bounds__(128, 1) umma_linear_kernel(const __grid_consta
             }
         }
     };
-    if (ks == 1) {
+    // Plain outputs go through the drained ring as a [NT][BM] fp32 tile: the
+    // residual (accumulate) comes in and the result goes out with coalesced
+    // 16-byte accesses, every load in flight at once, instead of one L2 round
+    // trip per 16 columns of each thread's row.
+    bool staged = false;
+    if constexpr (!GATED) {
+        const bool fits = ks == 1 && ldy % 4 == 0 && ((uintptr_t)Y & 15) == 0;
+        staged = __syncthreads_and(have && fits) != 0;
+    }
+    if (staged) {
+        float* tile = reinterpret_cast<float*>(s.a);   // [NT][BM], ring drained
+        const int mrows = min(NT, M - m0), ncols = min(BM, N - n0);
+        constexpr int C4 = BM / 4;
+        if (accumulate) {
+            for (int i = threadIdx.x; i < NT * C4; i += 128) {
+                const int m = i / C4, c = (i - m * C4) * 4;
+                if (m >= mrows) continue;
+                const float* src = Y + (size_t)(m0 + m) * ldy + n0 + c;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (c + 3 < ncols) {
+                    v = *reinterpret_cast<const float4*>(src);
+                } else {
+                    if (c < ncols) v.x = src[0];
+                    if (c + 1 < ncols) v.y = src[1];
+                    if (c + 2 < ncols) v.z = src[2];
+                }
+                *reinterpret_cast<float4*>(tile + m * BM + c) = v;
+            }
+            __syncthreads();
+        }
+        const float bn = (bias && n < N) ? bias[n] : 0.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < NT; c0 += 16) {
+            float v[16];
+            tmem_ld16(lane_base + c0, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                float* t = tile + (c0 + j) * BM + row;
+                *t = accumulate ? *t + v[j] + bn : v[j] + bn;
+            }
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < NT * C4; i += 128) {
+            const int m = i / C4, c = (i - m * C4) * 4;
+            if (m >= mrows) continue;
+            float* dst = Y + (size_t)(m0 + m) * ldy + n0 + c;
+            const float4 v = *reinterpret_cast<const float4*>(tile + m * BM + c);
+            if (c + 3 < ncols) {
+                *reinterpret_cast<float4*>(dst) = v;
+            } else {
+                if (c < ncols) dst[0] = v.x;
+                if (c + 1 < ncols) dst[1] = v.y;
+                if (c + 2 < ncols) dst[2] = v.z;
+            }
+        }
+    } else if (ks == 1) {
         if (have) {
 #pragma unroll 1
             for (int c0 = 0; c0 < NT; c0 += 16) {
@@ -400,6 +456,8 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int ld, int 
 // (K and ldx are multiples of 8, so the float4 reads are aligned).
 __global__ void split_kernel(const float* __restrict__ X, int ldx, int M, int K, bf16* __restrict__ hi,
                              bf16* __restrict__ lo) {
+    pdl_wait();
+    pdl_trigger();
     const int m = blockIdx.y;
     const int k = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (m >= M || k >= K) return;
@@ -499,7 +557,7 @@ cudaError_t launch_tc(const void* W, int N, int K, const float* X, int ldx, int 
     bf16* hi = (bf16*)tc.base;
     bf16* lo = hi + (size_t)M * K;
     // X = NULL: the producer of the operand wrote hi / lo itself
-    if (X) split_kernel<<<dim3((K + 1023) / 1024, M), 256, 0, st>>>(X, ldx, M, K, hi, lo);
+    if (X) launch_pdl(split_kernel, dim3((K + 1023) / 1024, M), 256, 0, st, X, ldx, M, K, hi, lo);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap mw, mx, mx2;

@@ -13,6 +13,23 @@ struct RowState;
 // SMs of the current device (looked up once per device).
 int device_sm_count();
 
+// Launch `k` allowing programmatic dependent launch (it may overlap the tail of
+// the previous kernel in the stream); `k` must start with pdl_wait().
+template <typename... K, typename... A>
+inline cudaError_t launch_pdl(void (*k)(K...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, A&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, static_cast<A&&>(args)...);
+}
+
 // The draw settings every selection needs: temperature > 0 where the draw
 // samples, and (talker chain) a positive repetition penalty.
 inline bool sampling_ok(const q3tts_sampling& s, bool talker) {

@@ -9,6 +9,7 @@
 // weights (gemm_tc.cu) and a shared-memory tiled CUDA-core GEMM otherwise.
 #include "common.cuh"
 #include "kernels.h"
+#include "pdl.cuh"
 
 namespace q3 {
 
@@ -18,6 +19,8 @@ __global__ void __launch_bounds__(128) gemv_kernel(const T* __restrict__ W, int 
                                                    const float* __restrict__ X, int ldx, float* __restrict__ Y,
                                                    int ldy, const float* __restrict__ bias, int accumulate, int F,
                                                    float* __restrict__ G, int ldg) {
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = (blockIdx.x * 4 + warp) * R;
     if (n0 >= N) return;
@@ -78,6 +81,8 @@ __global__ void __launch_bounds__(256) gemm_tiled(const T* __restrict__ W, int N
                                                   const float* __restrict__ X, int ldx, int M,
                                                   float* __restrict__ Y, int ldy, const float* __restrict__ bias,
                                                   int accumulate, int F, float* __restrict__ G, int ldg) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float xs[TBK][TBM + 4];
     __shared__ float ws[TBK][TBN + 4];
     __shared__ float us[GATED ? TBK : 1][TBN + 4];
@@ -143,8 +148,8 @@ static cudaError_t linear_impl(const T* W, int N, int K, const float* X, int ldx
         dim3 grid((N + rows_per_block - 1) / rows_per_block);
 #define GEMV_CASE(MM)                                                                                           \
     case MM:                                                                                                     \
-        if (two) gemv_kernel<T, MM, 2, GATED><<<grid, 128, 0, st>>>(W, N, K, X, ldx, Y, ldy, bias, accumulate, F, G, ldg); \
-        else gemv_kernel<T, MM, 1, GATED><<<grid, 128, 0, st>>>(W, N, K, X, ldx, Y, ldy, bias, accumulate, F, G, ldg);     \
+        if (two) launch_pdl(gemv_kernel<T, MM, 2, GATED>, grid, 128, 0, st, W, N, K, X, ldx, Y, ldy, bias, accumulate, F, G, ldg); \
+        else launch_pdl(gemv_kernel<T, MM, 1, GATED>, grid, 128, 0, st, W, N, K, X, ldx, Y, ldy, bias, accumulate, F, G, ldg);     \
         break;
         switch (M) {
             GEMV_CASE(1) GEMV_CASE(2) GEMV_CASE(3) GEMV_CASE(4) GEMV_CASE(5) GEMV_CASE(6) GEMV_CASE(7) GEMV_CASE(8)
@@ -152,7 +157,7 @@ static cudaError_t linear_impl(const T* W, int N, int K, const float* X, int ldx
 #undef GEMV_CASE
     } else {
         dim3 grid((N + TBN - 1) / TBN, (M + TBM - 1) / TBM);
-        gemm_tiled<T, GATED><<<grid, 256, 0, st>>>(W, N, K, X, ldx, M, Y, ldy, bias, accumulate, F, G, ldg);
+        launch_pdl(gemm_tiled<T, GATED>, grid, 256, 0, st, W, N, K, X, ldx, M, Y, ldy, bias, accumulate, F, G, ldg);
     }
     return cudaGetLastError();
 }
@@ -201,6 +206,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
                                                       int n, float eps, float* __restrict__ out, int ldo,
                                                       float* __restrict__ hout, int ldh, const int* __restrict__ out_row,
                                                       bf16* __restrict__ hi, bf16* __restrict__ lo) {
+    pdl_wait();
+    pdl_trigger();
     const int m = blockIdx.x;
     const int orow = out_row ? out_row[m] : m;
     if (orow < 0) return;
@@ -234,7 +241,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
 cudaError_t launch_rmsnorm(const float* x, int ldx, int M, const float* w, int n, float eps, float* out, int ldo,
                            float* hout, int ldh, const int* out_row, cudaStream_t st) {
     if (M <= 0) return cudaSuccess;
-    rmsnorm_kernel<<<M, 256, 0, st>>>(x, ldx, w, n, eps, out, ldo, hout, ldh, out_row, nullptr, nullptr);
+    launch_pdl(rmsnorm_kernel, M, 256, 0, st, x, ldx, w, n, eps, out, ldo, hout, ldh, out_row, nullptr, nullptr);
     return cudaGetLastError();
 }
 
@@ -243,7 +250,7 @@ cudaError_t launch_rmsnorm_split(const float* x, int ldx, int M, const float* w,
     if (M <= 0) return cudaSuccess;
     if (!tc_fits(tc, M, n)) return cudaErrorInvalidValue;
     bf16* hi = (bf16*)tc.base;
-    rmsnorm_kernel<<<M, 256, 0, st>>>(x, ldx, w, n, eps, nullptr, 0, nullptr, 0, nullptr, hi, hi + (size_t)M * n);
+    launch_pdl(rmsnorm_kernel, M, 256, 0, st, x, ldx, w, n, eps, nullptr, 0, nullptr, 0, nullptr, hi, hi + (size_t)M * n);
     return cudaGetLastError();
 }
 

@@ -8,6 +8,7 @@
 // table[s-1](code_s) at position s+1 (ncnn discussion 6798, section 1).
 #include "common.cuh"
 #include "kernels.h"
+#include "pdl.cuh"
 
 #include <algorithm>
 
@@ -17,6 +18,8 @@ namespace q3 {
 // prefill tokens (b, 0), (b, 1); predictor step s token (b, s+1).  Finished
 // rows get position -1 (skipped by the KV append and attention).
 __global__ void prepare_step_kernel(RowState* rs, int B, int* t_row, int* t_pos, int* c_row, int* c_pos, int G1) {
+    pdl_wait();
+    pdl_trigger();
     for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += gridDim.x * blockDim.x) {
         const bool live = !rs[b].finished;
         t_row[b] = b;
@@ -32,7 +35,7 @@ __global__ void prepare_step_kernel(RowState* rs, int B, int* t_row, int* t_pos,
 
 cudaError_t launch_prepare_step(RowState* rs, int B, int* t_row, int* t_pos, int* c_row, int* c_pos, int G1,
                                 cudaStream_t st) {
-    prepare_step_kernel<<<(B + 127) / 128, 128, 0, st>>>(rs, B, t_row, t_pos, c_row, c_pos, G1);
+    launch_pdl(prepare_step_kernel, (B + 127) / 128, 128, 0, st, rs, B, t_row, t_pos, c_row, c_pos, G1);
     return cudaGetLastError();
 }
 
@@ -43,6 +46,8 @@ __global__ void __launch_bounds__(256) talker_embed_kernel(const RowState* __res
                                                            const float* __restrict__ text,
                                                            const float* __restrict__ pad, float* __restrict__ x,
                                                            int eos, int* err) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x;
     const RowState& s = rs[b];
     float* xr = x + (size_t)b * H;
@@ -83,10 +88,10 @@ cudaError_t launch_talker_embed(int dtype, const RowState* rs, int B, const void
                                 int H, int V, int cpV, int G, const int32_t* codes_ws, int frames_cap,
                                 const float* text, const float* pad, float* x, int eos, int* err, cudaStream_t st) {
     if (dtype == Q3_BF16)
-        talker_embed_kernel<bf16><<<B, 256, 0, st>>>(rs, (const bf16*)codec_emb, (const bf16*)cp_emb, H, V, cpV, G,
+        launch_pdl(talker_embed_kernel<bf16>, B, 256, 0, st, rs, (const bf16*)codec_emb, (const bf16*)cp_emb, H, V, cpV, G,
                                                      codes_ws, frames_cap, text, pad, x, eos, err);
     else
-        talker_embed_kernel<float><<<B, 256, 0, st>>>(rs, (const float*)codec_emb, (const float*)cp_emb, H, V, cpV, G,
+        launch_pdl(talker_embed_kernel<float>, B, 256, 0, st, rs, (const float*)codec_emb, (const float*)cp_emb, H, V, cpV, G,
                                                       codes_ws, frames_cap, text, pad, x, eos, err);
     return cudaGetLastError();
 }
@@ -97,6 +102,8 @@ __global__ void __launch_bounds__(256) cp_embed_prefill_kernel(const RowState* _
                                                                const T* __restrict__ cemb, int H, int V,
                                                                int32_t* codes_ws, int frames_cap,
                                                                float* __restrict__ dst, int* err) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x;
     const RowState& s = rs[b];
     if (s.finished) return;
@@ -118,10 +125,10 @@ __global__ void __launch_bounds__(256) cp_embed_prefill_kernel(const RowState* _
 cudaError_t launch_cp_embed_prefill(int dtype, RowState* rs, int B, const float* h, const void* codec_emb, int H,
                                     int V, int32_t* codes_ws, int frames_cap, float* dst, int* err, cudaStream_t st) {
     if (dtype == Q3_BF16)
-        cp_embed_prefill_kernel<bf16><<<B, 256, 0, st>>>(rs, h, (const bf16*)codec_emb, H, V, codes_ws, frames_cap,
+        launch_pdl(cp_embed_prefill_kernel<bf16>, B, 256, 0, st, rs, h, (const bf16*)codec_emb, H, V, codes_ws, frames_cap,
                                                          dst, err);
     else
-        cp_embed_prefill_kernel<float><<<B, 256, 0, st>>>(rs, h, (const float*)codec_emb, H, V, codes_ws, frames_cap,
+        launch_pdl(cp_embed_prefill_kernel<float>, B, 256, 0, st, rs, h, (const float*)codec_emb, H, V, codes_ws, frames_cap,
                                                           dst, err);
     return cudaGetLastError();
 }
@@ -131,6 +138,8 @@ __global__ void __launch_bounds__(256) cp_embed_step_kernel(const RowState* __re
                                                             int H, int cpV, int s_idx,
                                                             const int32_t* __restrict__ codes_ws, int frames_cap,
                                                             float* __restrict__ dst, int* err) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x;
     const RowState& s = rs[b];
     if (s.finished) return;
@@ -147,10 +156,10 @@ __global__ void __launch_bounds__(256) cp_embed_step_kernel(const RowState* __re
 cudaError_t launch_cp_embed_step(int dtype, const RowState* rs, int B, const void* cp_emb, int H, int cpV, int s,
                                  const int32_t* codes_ws, int frames_cap, float* dst, int* err, cudaStream_t st) {
     if (dtype == Q3_BF16)
-        cp_embed_step_kernel<bf16><<<B, 256, 0, st>>>(rs, (const bf16*)cp_emb, H, cpV, s, codes_ws, frames_cap, dst,
+        launch_pdl(cp_embed_step_kernel<bf16>, B, 256, 0, st, rs, (const bf16*)cp_emb, H, cpV, s, codes_ws, frames_cap, dst,
                                                       err);
     else
-        cp_embed_step_kernel<float><<<B, 256, 0, st>>>(rs, (const float*)cp_emb, H, cpV, s, codes_ws, frames_cap, dst,
+        launch_pdl(cp_embed_step_kernel<float>, B, 256, 0, st, rs, (const float*)cp_emb, H, cpV, s, codes_ws, frames_cap, dst,
                                                        err);
     return cudaGetLastError();
 }

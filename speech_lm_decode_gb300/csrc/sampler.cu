@@ -2,6 +2,7 @@
 // processors and the draw themselves are in sampler.cuh.
 #include "sampler.cuh"
 #include "kernels.h"
+#include "pdl.cuh"
 
 namespace q3 {
 
@@ -12,6 +13,8 @@ __global__ void __launch_bounds__(ST) talker_sample_kernel(const float* __restri
                                                            const q3tts_sampling* __restrict__ P, int eos, int sup_lo,
                                                            int sup_hi, int advance_pos, int* err, float* cap_logits,
                                                            const int* cap_slot, int cap_T) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(16) unsigned char smraw[];
     SampSmem& sm = *reinterpret_cast<SampSmem*>(smraw);
     const int b = blockIdx.x;
@@ -49,6 +52,8 @@ __global__ void __launch_bounds__(ST) cp_sample_kernel(const float* __restrict__
                                                        const q3tts_sampling* __restrict__ P, int s_idx,
                                                        int32_t* codes_ws, int frames_cap, int* err, float* cap_logits,
                                                        const int* cap_slot, int cap_T, int G) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(16) unsigned char smraw[];
     SampSmem& sm = *reinterpret_cast<SampSmem*>(smraw);
     const int b = blockIdx.x;
@@ -111,7 +116,7 @@ cudaError_t sampler_init() {
 cudaError_t launch_talker_sample(const float* logits, int V, int B, RowState* rs, const q3tts_sampling* P, int eos,
                                  int sup_lo, int sup_hi, int advance_pos, int* err, float* cap_logits,
                                  const int* cap_slot, int cap_T, cudaStream_t st) {
-    talker_sample_kernel<<<B, ST, sizeof(SampSmem), st>>>(logits, V, rs, P, eos, sup_lo, sup_hi, advance_pos, err,
+    launch_pdl(talker_sample_kernel, B, ST, sizeof(SampSmem), st, logits, V, rs, P, eos, sup_lo, sup_hi, advance_pos, err,
                                                           cap_logits, cap_slot, cap_T);
     return cudaGetLastError();
 }
@@ -119,7 +124,7 @@ cudaError_t launch_talker_sample(const float* logits, int V, int B, RowState* rs
 cudaError_t launch_cp_sample(const float* logits, int V, int B, RowState* rs, const q3tts_sampling* P, int s,
                              int32_t* codes_ws, int frames_cap, int* err, float* cap_logits, const int* cap_slot,
                              int cap_T, int n_groups, cudaStream_t st) {
-    cp_sample_kernel<<<B, ST, sizeof(SampSmem), st>>>(logits, V, rs, P, s, codes_ws, frames_cap, err, cap_logits,
+    launch_pdl(cp_sample_kernel, B, ST, sizeof(SampSmem), st, logits, V, rs, P, s, codes_ws, frames_cap, err, cap_logits,
                                                       cap_slot, cap_T, n_groups);
     return cudaGetLastError();
 }
