@@ -7,6 +7,8 @@
 // (same page, section "对照结果"), GQA where q head h reads kv head
 // h / (nq/nkv) (repeat_interleave over heads, ncnn discussion 6798,
 // section 2), causal softmax over positions 0..pos.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "pdl.cuh"
@@ -751,21 +753,45 @@ __global__ void __launch_bounds__(256) prefill_attn_kernel(const float* __restri
     for (int kb0 = 0; kb0 <= last; kb0 += KB) {
         const int nk = min(KB, last + 1 - kb0);
         __syncthreads();   // the previous block's K / V are no longer read
-        // stage K [pos][dim] and V^T [dim][pos] (bf16); positions past nk are zero
-        for (int i = tid; i < KB * (HD / 8); i += 256) {
-            const int j = i / (HD / 8), c = (i % (HD / 8)) * 8;
-            float kv[8], vv[8];
-            if (j < nk) {
-                load8(Kc + base + (size_t)(kb0 + j) * HD + c, kv);
-                load8(Vc + base + (size_t)(kb0 + j) * HD + c, vv);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) kv[e] = vv[e] = 0.f;
+        // stage K [pos][dim] and V^T [dim][pos] (bf16); positions past nk are
+        // zero.  K: consecutive threads take consecutive 8-dim pieces of a row
+        // (16-byte stores, conflict-free); V: consecutive threads take
+        // consecutive positions, so the transposed 2-byte stores of a warp hit
+        // consecutive addresses of one V^T row.
+        if constexpr (std::is_same<T, bf16>::value) {
+            for (int i = tid; i < KB * (HD / 8); i += 256) {
+                const int j = i / (HD / 8), c = (i % (HD / 8)) * 8;
+                uint4 kv = make_uint4(0u, 0u, 0u, 0u);
+                if (j < nk) kv = *reinterpret_cast<const uint4*>(Kc + base + (size_t)(kb0 + j) * HD + c);
+                *reinterpret_cast<uint4*>(&sK[j][c]) = kv;
             }
+            for (int i = tid; i < KB * (HD / 8); i += 256) {
+                const int j = i % KB, c = (i / KB) * 8;
+                uint4 vv = make_uint4(0u, 0u, 0u, 0u);
+                if (j < nk) vv = *reinterpret_cast<const uint4*>(Vc + base + (size_t)(kb0 + j) * HD + c);
+                const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                sK[j][c + e] = __float2bfloat16_rn(kv[e]);
-                sVt[c + e][j] = __float2bfloat16_rn(vv[e]);
+                for (int e = 0; e < 4; ++e) {
+                    sVt[c + 2 * e][j] = __ushort_as_bfloat16((unsigned short)(w[e] & 0xffffu));
+                    sVt[c + 2 * e + 1][j] = __ushort_as_bfloat16((unsigned short)(w[e] >> 16));
+                }
+            }
+        } else {
+            for (int i = tid; i < KB * (HD / 8); i += 256) {
+                const int j = i / (HD / 8), c = (i % (HD / 8)) * 8;
+                float kv[8], vv[8];
+                if (j < nk) {
+                    load8(Kc + base + (size_t)(kb0 + j) * HD + c, kv);
+                    load8(Vc + base + (size_t)(kb0 + j) * HD + c, vv);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) kv[e] = vv[e] = 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    sK[j][c + e] = __float2bfloat16_rn(kv[e]);
+                    sVt[c + e][j] = __float2bfloat16_rn(vv[e]);
+                }
             }
         }
         __syncthreads();

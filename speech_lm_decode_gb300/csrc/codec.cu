@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "pdl.cuh"
 #include "q3codec.h"
 
 using namespace q3;
@@ -69,6 +70,8 @@ __global__ void repeat_kernel(const float* __restrict__ b, int C, int s, float* 
 template <typename T>
 __global__ void dequant_kernel(const int32_t* __restrict__ codes, int NQ, int V, int Dc, const T* __restrict__ cb,
                                float* __restrict__ zs, float* __restrict__ za, int* __restrict__ err) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x;
     __shared__ int cs[32];
     if (threadIdx.x < NQ) {
@@ -87,6 +90,8 @@ __global__ void dequant_kernel(const int32_t* __restrict__ codes, int NQ, int V,
 
 // rotate-half RoPE on q and k of qkv [T][3D] at the frame index (head_dim 64)
 __global__ void rope64_kernel(float* __restrict__ qkv, int D, float theta) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x;
     const int H = D / 64;
     for (int i = threadIdx.x; i < 2 * H * 32; i += blockDim.x) {
@@ -104,6 +109,8 @@ __global__ void rope64_kernel(float* __restrict__ qkv, int D, float theta) {
 // causal window attention, one (frame, head) per block of 128 threads
 __global__ void __launch_bounds__(128) window_attn_kernel(const float* __restrict__ qkv, int D, int W,
                                                           float* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x, h = blockIdx.y;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int s0 = max(0, t - W + 1), n = t - s0 + 1;
@@ -137,6 +144,8 @@ __global__ void __launch_bounds__(128) window_attn_kernel(const float* __restric
 // x[m][c] += g[c] * y[m][c]
 __global__ void scale_add_kernel(float* __restrict__ x, const float* __restrict__ y, const float* __restrict__ g,
                                  size_t n, int C) {
+    pdl_wait();
+    pdl_trigger();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
         x[i] = fmaf(g[i % C], y[i], x[i]);
 }
@@ -148,6 +157,8 @@ __global__ void __launch_bounds__(256) dwconv_ln_kernel(const float* __restrict_
                                                         const float* __restrict__ lw, const float* __restrict__ lb,
                                                         float eps, float* __restrict__ out, bf16* __restrict__ hi,
                                                         bf16* __restrict__ lo) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x;
     extern __shared__ float dv[];   // [C]
     __shared__ float red[8];
@@ -189,6 +200,8 @@ __global__ void __launch_bounds__(256) dwconv_ln_kernel(const float* __restrict_
 // exact GELU of h, written as fp32 (in place allowed) or as the bf16 parts
 __global__ void gelu_kernel(const float* h, size_t n, float* out, bf16* __restrict__ hi,
                             bf16* __restrict__ lo) {
+    pdl_wait();
+    pdl_trigger();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const float v = h[i];
         const float y = 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
@@ -209,6 +222,8 @@ __global__ void gelu_kernel(const float* h, size_t n, float* out, bf16* __restri
 __global__ void gather_kernel(const float* __restrict__ x, int M, int Cin, int K, int d, int rev,
                               const float2* __restrict__ ab, float* __restrict__ out, bf16* __restrict__ hi,
                               bf16* __restrict__ lo) {
+    pdl_wait();
+    pdl_trigger();
     const int C4 = Cin >> 2;
     const size_t per_row = (size_t)K * C4;
     const size_t n = (size_t)M * per_row;
@@ -245,6 +260,8 @@ __global__ void gather_kernel(const float* __restrict__ x, int M, int Cin, int K
 template <typename T>
 __global__ void out_conv_kernel(const float* __restrict__ x, int M, int C, const float2* __restrict__ ab,
                                 const T* __restrict__ w, const float* __restrict__ b, float* __restrict__ wav) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int m = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (m >= M) return;
@@ -433,12 +450,12 @@ public:
     int gather(const float* x, int M, int Cin, int K, int d, int rev, const float2* ab, float** X) {
         const size_t n = (size_t)M * K * (Cin / 4);
         if (split(M, K * Cin)) {
-            gather_kernel<<<grid_for(n, 256), 256, 0, h->st>>>(x, M, Cin, K, d, rev, ab, nullptr, hi(),
+            launch_pdl(gather_kernel, grid_for(n, 256), 256, 0, h->st, x, M, Cin, K, d, rev, ab, nullptr, hi(),
                                                                lo(M, K * Cin));
             *X = nullptr;
         } else {
             float* col = h->p<float>(h->col);
-            gather_kernel<<<grid_for(n, 256), 256, 0, h->st>>>(x, M, Cin, K, d, rev, ab, col, nullptr, nullptr);
+            launch_pdl(gather_kernel, grid_for(n, 256), 256, 0, h->st, x, M, Cin, K, d, rev, ab, col, nullptr, nullptr);
             *X = col;
         }
         ++launches;
@@ -465,10 +482,10 @@ public:
         const q3codec_weights& w = h->w;
         // SplitRVQ dequantisation and the two output projections
         if (c.dtype == Q3_BF16)
-            dequant_kernel<bf16><<<T, 256, 0, h->st>>>(codes_dev, NQ, c.codebook_size, Dc, (const bf16*)w.codebooks,
+            launch_pdl(dequant_kernel<bf16>, T, 256, 0, h->st, codes_dev, NQ, c.codebook_size, Dc, (const bf16*)w.codebooks,
                                                        zs, za, h->errp());
         else
-            dequant_kernel<float><<<T, 256, 0, h->st>>>(codes_dev, NQ, c.codebook_size, Dc, (const float*)w.codebooks,
+            launch_pdl(dequant_kernel<float>, T, 256, 0, h->st, codes_dev, NQ, c.codebook_size, Dc, (const float*)w.codebooks,
                                                         zs, za, h->errp());
         ++launches;
         CC(cudaGetLastError());
@@ -483,8 +500,8 @@ public:
             const char* wd = (const char*)w.wd + (size_t)l * D * F * e;
             if ((r = norm(x, T, (const float*)w.attn_norm + (size_t)l * D, op))) return r;
             if ((r = linear(wqkv, 3 * D, D, split(T, D) ? nullptr : op, T, qkv, nullptr, 0))) return r;
-            rope64_kernel<<<T, 256, 0, h->st>>>(qkv, D, c.rope_theta);
-            window_attn_kernel<<<dim3(T, c.n_heads), 128, std::min(T, c.window) * sizeof(float), h->st>>>(
+            launch_pdl(rope64_kernel, T, 256, 0, h->st, qkv, D, c.rope_theta);
+            launch_pdl(window_attn_kernel, dim3(T, c.n_heads), 128, std::min(T, c.window) * sizeof(float), h->st, 
                 qkv, D, c.window, att);
             launches += 2;
             CC(cudaGetLastError());
@@ -511,7 +528,7 @@ public:
             const int F2 = c.up_ffn;
             const bool sp = split(n, D);
             float* nrm = h->p<float>(h->col);
-            dwconv_ln_kernel<<<n, 256, D * sizeof(float), h->st>>>(
+            launch_pdl(dwconv_ln_kernel, n, 256, D * sizeof(float), h->st, 
                 A, D, (const float*)w.dw_w + (size_t)u * D * 7, (const float*)w.dw_b + (size_t)u * D,
                 (const float*)w.ln_w + (size_t)u * D, (const float*)w.ln_b + (size_t)u * D, c.ln_eps,
                 sp ? nullptr : nrm, sp ? hi() : nullptr, sp ? lo(n, D) : nullptr);
@@ -520,7 +537,7 @@ public:
             if ((r = linear((const char*)w.fc1_w + (size_t)u * F2 * D * e, F2, D, sp ? nullptr : nrm, n, B,
                             (const float*)w.fc1_b + (size_t)u * F2, 0))) return r;
             const bool sp2 = split(n, F2);
-            gelu_kernel<<<grid_for((size_t)n * F2, 256), 256, 0, h->st>>>(B, (size_t)n * F2, B, sp2 ? hi() : nullptr,
+            launch_pdl(gelu_kernel, grid_for((size_t)n * F2, 256), 256, 0, h->st, B, (size_t)n * F2, B, sp2 ? hi() : nullptr,
                                                                           sp2 ? lo(n, F2) : nullptr);
             ++launches;
             CC(cudaGetLastError());
@@ -555,10 +572,10 @@ public:
         }
         const int warps = 8;
         if (c.dtype == Q3_BF16)
-            out_conv_kernel<bf16><<<(n + warps - 1) / warps, 32 * warps, 0, h->st>>>(
+            launch_pdl(out_conv_kernel<bf16>, (n + warps - 1) / warps, 32 * warps, 0, h->st, 
                 A, n, C, snk + h->snk_out, (const bf16*)w.out_w, (const float*)w.out_bias, wav);
         else
-            out_conv_kernel<float><<<(n + warps - 1) / warps, 32 * warps, 0, h->st>>>(
+            launch_pdl(out_conv_kernel<float>, (n + warps - 1) / warps, 32 * warps, 0, h->st, 
                 A, n, C, snk + h->snk_out, (const float*)w.out_w, (const float*)w.out_bias, wav);
         ++launches;
         CC(cudaGetLastError());
@@ -576,7 +593,7 @@ private:
         return Q3_OK;
     }
     int scale_add(float* x, const float* y, const float* g, size_t n, int C) {
-        scale_add_kernel<<<grid_for(n, 256), 256, 0, h->st>>>(x, y, g, n, C);
+        launch_pdl(scale_add_kernel, grid_for(n, 256), 256, 0, h->st, x, y, g, n, C);
         ++launches;
         CC(cudaGetLastError());
         return Q3_OK;
