@@ -52,6 +52,8 @@ def parse():
     p.add_argument("--cpu-frames", type=int, default=0, help="oracle frames timed for the CPU baseline (0: auto)")
     p.add_argument("--no-batches", action="store_true", help="skip the batch entries")
     p.add_argument("--no-codec", action="store_true", help="skip the codec-decoder entry")
+    p.add_argument("--codec-only", action="store_true",
+                   help="no benchmark line: three decodes of the full-size codec window (for ncu launch lists)")
     p.add_argument("--profile-case", action="store_true",
                    help="no benchmark: prefill and 6 steps of the workload with 4 talker layers and a "
                         "context of 320 (full-size launch shapes on a small device footprint, for ncu)")
@@ -438,11 +440,35 @@ def run_ours(args, wl, rank, world):
         pre.append(ev0.elapsed_time(ev1))
         ttff.append(ev0.elapsed_time(ev2))
     prefill_ms, ttff_ms = statistics.median(pre), statistics.median(ttff)
+    # time to the first audio at batch 1 (the pages' first-packet latency):
+    # prefill, 4 steps (the first streamed decode comes after 4 frames), and
+    # the full-size codec decoder on those 4 frames; median of 3
+    ttfa_ms = None
+    if wl.batch == 1 and not getattr(args, "no_codec", False) and wl.frames >= 4:
+        import synth.codec as sc
+        dcodec = sc.CODEC_FULL
+        dec = q3.Q3Codec(dcodec, synth.BF16, q3.codec_to_device(sc.make_codec_weights(dcodec, synth.BF16, 3), dev),
+                         max_frames=16, stream=stream)
+        wav = torch.empty(4 * dec.spf, dtype=torch.float32, device=dev)
+        first = codes_dev.view(-1)[: 4 * wl.dims.n_groups]
+        ta = []
+        for _ in range(3):
+            barrier()
+            ev0.record(stream)
+            prefill()
+            q.step_frames(4, codes_out=first)
+            dec.decode_window(first.view(4, wl.dims.n_groups), out=wav, check=False)
+            ev2 = torch.cuda.Event(enable_timing=True)
+            ev2.record(stream)
+            barrier()
+            ta.append(ev0.elapsed_time(ev2))
+        ttfa_ms = statistics.median(ta)
+        dec.close()
     (max_ms,), (all_frames,) = job_totals([total_ms], [total_frames], dev)
     res = dict(ms=max_ms, frames=all_frames, local_frames=total_frames, steps=timed_steps,
                wbytes=wbytes_total, kvbytes=kvbytes_total, kernels_per_step=kernels_per_step,
                clocks=clocks.summary(), local_ms=total_ms, flops=flops_total, ctx=(ctx_lo, ctx_hi),
-               step_path=step_path, prefill_ms=prefill_ms, ttff_ms=ttff_ms)
+               step_path=step_path, prefill_ms=prefill_ms, ttff_ms=ttff_ms, ttfa_ms=ttfa_ms)
 
     # e2e: the whole request through the C ABI from pinned host buffers, one call per step,
     # codes read back to pinned host memory after every step
@@ -499,6 +525,22 @@ def main():
     args = parse()
     if args.profile_case:
         profile_case(args)
+        return
+    if args.codec_only:
+        import torch
+        import speech_lm_decode_gb300 as q3
+        import synth.codec as sc
+        dev = torch.device("cuda", 0)
+        d = sc.CODEC_FULL
+        dec = q3.Q3Codec(d, synth.BF16, q3.codec_to_device(sc.make_codec_weights(d, synth.BF16, 3), dev),
+                         max_frames=325)
+        codes = torch.from_numpy(sc.make_codes(d, 325, 4)).to(dev)
+        out = torch.empty(325 * dec.spf, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            dec.decode_window(codes, out=out)
+        torch.cuda.synchronize()
+        print("codec windows done:", dec.kernel_count(), "launches per window")
+        dec.close()
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -560,6 +602,7 @@ def main():
                          "traffic": traffic, "algorithmic_bytes_per_step": bytes_total / max(res["steps"], 1)},
             "step_path": res["step_path"],
             "prefill_ms": res["prefill_ms"], "time_to_first_frame_ms": res["ttff_ms"],
+            "time_to_first_audio_ms": res["ttfa_ms"],
             "gpu_launches": res["kernels_per_step"] * res["steps"],
             "clocks": res["clocks"]}
     if "e2e" in res:
