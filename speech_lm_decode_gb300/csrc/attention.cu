@@ -600,6 +600,152 @@ __global__ void __launch_bounds__(256) attn_short_kernel(const float* __restrict
     }
 }
 
+// Decode steps over short caches with QK-norm, RoPE and the cache append
+// fused in (one token per row in the launch): one warp per (token, kv head)
+// normalises and rotates the group's q heads and its k head (lane l holds
+// elements l, l+32, l+64, l+96, so the RoPE pairs (j, j+64) stay in the
+// lane), rounds k and v to the cache type and appends them at the token's
+// position, then attends over positions 0..pos (the new position from its
+// registers, which equal what it stored), eight positions' loads in flight.
+template <int GQ>
+__global__ void __launch_bounds__(256) attn_short_fused_kernel(
+    const float* __restrict__ qkv, int ldq, int M, int nq, int nkv, const float* __restrict__ qn,
+    const float* __restrict__ kn, float eps, const float2* __restrict__ rope, int rope_rows, bf16* __restrict__ Kc,
+    bf16* __restrict__ Vc, int cap, const int* __restrict__ tok_row, const int* __restrict__ tok_pos,
+    float* __restrict__ out, int ldo, bf16* __restrict__ hi, bf16* __restrict__ lo, int* __restrict__ err) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (item >= M * nkv) return;
+    const int m = item / nkv, g = item - m * nkv;
+    const int pos = tok_pos[m];
+    float res[GQ][4];
+#pragma unroll
+    for (int hh = 0; hh < GQ; ++hh)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) res[hh][i] = 0.f;
+    if (pos >= 0 && pos < cap && pos < rope_rows) {
+        const float* t = qkv + (size_t)m * ldq;
+        const float2 cs0 = rope[(size_t)pos * (HD / 2) + lane];
+        const float2 cs1 = rope[(size_t)pos * (HD / 2) + lane + 32];
+        // RMSNorm over the head (weight wn) then rotate-half RoPE at pos
+        auto norm_rope = [&](const float* src, const float* wn, float (&e)[4]) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) e[i] = src[lane + 32 * i];
+            const float ss = warp_sum(e[0] * e[0] + e[1] * e[1] + e[2] * e[2] + e[3] * e[3]);
+            const float r = 1.0f / sqrtf(ss / (float)HD + eps);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) e[i] = e[i] * r * wn[lane + 32 * i];
+            float a = e[0], b = e[2];
+            e[0] = a * cs0.x - b * cs0.y;
+            e[2] = b * cs0.x + a * cs0.y;
+            a = e[1]; b = e[3];
+            e[1] = a * cs1.x - b * cs1.y;
+            e[3] = b * cs1.x + a * cs1.y;
+        };
+        const float scale = 0.08838834764831845f;  // 1/sqrt(128)
+        float q[GQ][4];
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) {
+            norm_rope(t + (size_t)(g * GQ + hh) * HD, qn, q[hh]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) q[hh][i] *= scale;
+        }
+        float kn4[4], kcur[4], vcur[4];
+        norm_rope(t + (size_t)(nq + g) * HD, kn, kn4);
+        const float* vs = t + (size_t)(nq + nkv + g) * HD;
+        const size_t base = ((size_t)tok_row[m] * nkv + g) * cap * HD;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const bf16 kb = __float2bfloat16_rn(kn4[i]), vb = __float2bfloat16_rn(vs[lane + 32 * i]);
+            Kc[base + (size_t)pos * HD + lane + 32 * i] = kb;
+            Vc[base + (size_t)pos * HD + lane + 32 * i] = vb;
+            kcur[i] = __bfloat162float(kb);
+            vcur[i] = __bfloat162float(vb);
+        }
+        float mx[GQ], l[GQ], acc[GQ][4];
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) {
+            mx[hh] = -INFINITY; l[hh] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[hh][i] = 0.f;
+        }
+        constexpr int U = 8;
+        for (int j0 = 0; j0 <= pos; j0 += U) {
+            float kr[U][4], vr[U][4];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = j0 + u;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (j < pos) {
+                        kr[u][i] = __bfloat162float(Kc[base + (size_t)j * HD + lane + 32 * i]);
+                        vr[u][i] = __bfloat162float(Vc[base + (size_t)j * HD + lane + 32 * i]);
+                    } else {
+                        kr[u][i] = kcur[i];
+                        vr[u][i] = vcur[i];
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (j0 + u > pos) break;   // uniform over the warp (one token per warp)
+#pragma unroll
+                for (int hh = 0; hh < GQ; ++hh) {
+                    const float sc = warp_sum(fmaf(q[hh][0], kr[u][0], fmaf(q[hh][1], kr[u][1],
+                                                   fmaf(q[hh][2], kr[u][2], q[hh][3] * kr[u][3]))));
+                    const float mn = fmaxf(mx[hh], sc);
+                    const float cf = expf(mx[hh] - mn);
+                    const float p = expf(sc - mn);
+                    l[hh] = l[hh] * cf + p;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[hh][i] = fmaf(p, vr[u][i], acc[hh][i] * cf);
+                    mx[hh] = mn;
+                }
+            }
+        }
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) res[hh][i] = acc[hh][i] / l[hh];
+    } else if (pos >= 0 && lane == 0) {
+        atomicOr(err, ERRB_BOUNDS);
+    }
+#pragma unroll
+    for (int hh = 0; hh < GQ; ++hh) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const size_t o = (size_t)(g * GQ + hh) * HD + lane + 32 * i;
+            if (hi) {
+                const bf16 hv = __float2bfloat16_rn(res[hh][i]);
+                hi[(size_t)m * nq * HD + o] = hv;
+                lo[(size_t)m * nq * HD + o] = __float2bfloat16_rn(res[hh][i] - __bfloat162float(hv));
+            } else {
+                out[(size_t)m * ldo + o] = res[hh][i];
+            }
+        }
+    }
+}
+
+cudaError_t launch_attention_short_fused(const float* qkv, int ldq, int M, int nq, int nkv, const float* q_norm,
+                                         const float* k_norm, float eps, const float* rope_cs, int rope_rows,
+                                         void* Kc, void* Vc, int cap, const int* tok_row, const int* tok_pos,
+                                         float* out, int ldo, int* err, cudaStream_t st, const TcScratch* split) {
+    if (M <= 0) return cudaSuccess;
+    if (nq != 2 * nkv || cap > 64) return cudaErrorInvalidValue;
+    bf16* hi = nullptr;
+    bf16* lo = nullptr;
+    if (split) {
+        if (!tc_fits(*split, M, nq * HD)) return cudaErrorInvalidValue;
+        hi = (bf16*)split->base;
+        lo = hi + (size_t)M * nq * HD;
+    }
+    launch_pdl(attn_short_fused_kernel<2>, (M * nkv + 7) / 8, 256, 0, st, qkv, ldq, M, nq, nkv, q_norm, k_norm, eps,
+               (const float2*)rope_cs, rope_rows, (bf16*)Kc, (bf16*)Vc, cap, tok_row, tok_pos, out, ldo, hi, lo, err);
+    return cudaGetLastError();
+}
+
 template <int GQ>
 static cudaError_t attention_bulk(const float* qkv, int ldq, int M, int nq, int nkv, const bf16* Kc, const bf16* Vc,
                                   int cap, const int* tok_row, const int* tok_pos, int n_splits, float* pm, float* pl,

@@ -100,6 +100,16 @@ cudaError_t launch_attention(int dtype, const float* qkv, int ldq, int M, int nq
                              float* part_m, float* part_l, float* part_acc, float* out, int ldo, int* err,
                              cudaStream_t st, const TcScratch* split = nullptr);
 
+// Decode step over short bf16 caches (cap <= 64, two q heads per kv head)
+// with QK-norm, RoPE and the K/V append of launch_qk_rope_kv fused in; every
+// token of the launch must belong to a different row.  Output as in
+// launch_attention.
+cudaError_t launch_attention_short_fused(const float* qkv, int ldq, int M, int nq, int nkv, const float* q_norm,
+                                         const float* k_norm, float eps, const float* rope_cs, int rope_rows,
+                                         void* Kc, void* Vc, int cap, const int* tok_row, const int* tok_pos,
+                                         float* out, int ldo, int* err, cudaStream_t st,
+                                         const TcScratch* split = nullptr);
+
 // Causal attention of prompt tokens, tiled: tiles[t] = {first token, tokens
 // (1..64, consecutive positions of one row), row, position of the first};
 // every token of a tile attends to positions 0..its own of its row's cache

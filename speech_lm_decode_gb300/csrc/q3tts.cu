@@ -269,9 +269,11 @@ void invalidate_graph(q3tts* h) {
 
 // One decoder stack over M tokens (talker or predictor), residual x [M][H].
 // tiles / n_tiles: prompt tokens of a prefill chunk, whose attention runs tiled
-// (bf16 caches); NULL for decode steps.
+// (bf16 caches); NULL for decode steps.  single: every token belongs to a
+// different row (a decode step), so short bf16 caches take the attention with
+// QK-norm, RoPE and the cache append fused in.
 int enqueue_layers(q3tts* h, bool talker, int M, float* x, const int* trow, const int* tpos,
-                   const int4* tiles = nullptr, int n_tiles = 0) {
+                   const int4* tiles = nullptr, int n_tiles = 0, bool single = false) {
     const q3tts_config& c = h->c;
     const q3tts_block_weights& bw = talker ? h->w.talker : h->w.cp;
     const int L = talker ? c.n_layers : c.cp_layers;
@@ -308,14 +310,24 @@ int enqueue_layers(q3tts* h, bool talker, int M, float* x, const int* trow, cons
                               nullptr, h->st)); debug_wait(h, "launch_rmsnorm");
         }
         CK(launch_linear(c.dtype, wqkv, nqkv, H, presplit ? nullptr : opA, H, M, qkv, nqkv, nullptr, 0, h->tc(), h->err(), h->st)); debug_wait(h, "launch_linear");
-        CK(launch_qk_rope_kv(c.dtype, qkv, nqkv, M, nq, nkv, (const float*)bw.q_norm + (size_t)l * hd,
-                             (const float*)bw.k_norm + (size_t)l * hd, eps, h->p<float>(h->L.rope), h->L.rope_rows,
-                             Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos, h->err(), h->st)); debug_wait(h, "launch_qk_rope_kv");
-        if (tiles && c.dtype == Q3_BF16) {
+        const bool fused = single && !tiles && c.dtype == Q3_BF16 && nq == 2 * nkv && cap <= 64;
+        if (fused) {
+            CK(launch_attention_short_fused(qkv, nqkv, M, nq, nkv, (const float*)bw.q_norm + (size_t)l * hd,
+                                            (const float*)bw.k_norm + (size_t)l * hd, eps, h->p<float>(h->L.rope),
+                                            h->L.rope_rows, Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos, opA,
+                                            nq * hd, h->err(), h->st, presplit_o ? &tcs : nullptr));
+            debug_wait(h, "launch_attention_short_fused");
+        } else {
+            CK(launch_qk_rope_kv(c.dtype, qkv, nqkv, M, nq, nkv, (const float*)bw.q_norm + (size_t)l * hd,
+                                 (const float*)bw.k_norm + (size_t)l * hd, eps, h->p<float>(h->L.rope),
+                                 h->L.rope_rows, Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos, h->err(),
+                                 h->st)); debug_wait(h, "launch_qk_rope_kv");
+        }
+        if (!fused && tiles && c.dtype == Q3_BF16) {
             CK(launch_prefill_attention(c.dtype, qkv, nqkv, M, nq, nkv, Kc + l * kv_layer, Vc + l * kv_layer, cap,
                                         tiles, n_tiles, opA, nq * hd, h->st, presplit_o ? &tcs : nullptr));
             debug_wait(h, "launch_prefill_attention");
-        } else {
+        } else if (!fused) {
             CK(launch_attention(c.dtype, qkv, nqkv, M, nq, nkv, Kc + l * kv_layer, Vc + l * kv_layer, cap, trow, tpos,
                                 splits, h->p<float>(h->L.pm), h->p<float>(h->L.pl), h->p<float>(h->L.pacc), opA,
                                 nq * hd, h->err(), h->st, presplit_o ? &tcs : nullptr));
@@ -393,7 +405,8 @@ int enqueue_step(q3tts* h) {
         CK(launch_cp_embed_step(c.dtype, rs, B, h->w.cp_emb, c.hidden, c.cp_vocab, s, codes, h->L.frames_cap, tok,
                                 h->err(), h->st)); debug_wait(h, "launch_cp_embed_step");
         if ((r = enqueue_cp_input(h, B))) return r;
-        if ((r = enqueue_layers(h, false, B, cx, c_row + (size_t)s * 2 * B, c_pos + (size_t)s * 2 * B))) return r;
+        if ((r = enqueue_layers(h, false, B, cx, c_row + (size_t)s * 2 * B, c_pos + (size_t)s * 2 * B, nullptr, 0,
+                                true))) return r;
         CK(launch_rmsnorm(cx, c.cp_hidden, B, (const float*)h->w.cp.final_norm, c.cp_hidden, c.rms_eps, opA,
                           c.cp_hidden, nullptr, 0, nullptr, h->st)); debug_wait(h, "launch_rmsnorm");
         const char* head = (const char*)h->w.cp_heads + (size_t)s * c.cp_vocab * c.cp_hidden * e;
@@ -407,7 +420,7 @@ int enqueue_step(q3tts* h) {
     CK(launch_talker_embed(c.dtype, rs, B, h->w.codec_emb, h->w.cp_emb, c.hidden, c.codec_vocab, c.cp_vocab,
                            c.n_groups, codes, h->L.frames_cap, h->p<float>(h->L.text), h->p<float>(h->L.pad), x,
                            c.eos_id, h->err(), h->st)); debug_wait(h, "launch_talker_embed");
-    if ((r = enqueue_layers(h, true, B, x, t_row, t_pos))) return r;
+    if ((r = enqueue_layers(h, true, B, x, t_row, t_pos, nullptr, 0, true))) return r;
     CK(launch_rmsnorm(x, c.hidden, B, (const float*)h->w.talker.final_norm, c.hidden, c.rms_eps, opA,
                       c.hidden, h->p<float>(h->L.h), c.hidden, nullptr, h->st)); debug_wait(h, "launch_rmsnorm");
     float* logits = h->p<float>(h->L.logits);
