@@ -31,8 +31,9 @@
 //
 // Weights are streamed, not waited for: a producer warp per CTA walks the
 // same schedule and copies the CTA's next weight windows (32 KB, one bulk
-// copy each) from a packed image into a 3-slot ring ahead of the chain, and
-// prefetches later ones into L2.  The packed image (built once at handle
+// copy each) from a packed image into a 3-slot ring ahead of the chain
+// (prefetching later windows into L2 as well, PF_WINDOWS > 0, measured
+// slower and is compiled out).  The packed image (built once at handle
 // creation) stores each CTA's slice of every matrix in mma.m16n8k16 fragment
 // order, so a warp reads one 16-byte word per lane per 16x16 weight tile.
 // GEMV rows run on the tensor cores: A = 16 weight rows, B = the input's
