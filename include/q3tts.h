@@ -106,6 +106,16 @@ typedef struct {
     int text_vocab;     /* text side (q3tts_text_embed): BPE vocabulary
                            (151936 upstream); 0 = no text path                */
     int text_hidden;    /* width of the text embedding (2048)                 */
+    int separate_projections; /* 1: q, k, v and gate, up as separate products
+                           (the layout of a model loaded without stacking,
+                           Mizuoto "Qwen3-TTS" page, section "速度", fast mode
+                           off); 0: stacked q/k/v and gate/up weights in one
+                           product each.  The weights are the same stacked
+                           arrays either way.  Per-layer kernels only (batch
+                           > 1, prefill, Q3_PATH_GRAPH); every output row is
+                           the same dot product in both, so results differ
+                           only where the tensor-core tile / K-split choice,
+                           which depends on the product's width, differs      */
 } q3tts_config;
 
 /* step_path values */

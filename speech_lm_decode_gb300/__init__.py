@@ -39,10 +39,11 @@ class Config(ctypes.Structure):
               [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)] + \
               [(n, ctypes.c_int) for n in ("dtype", "max_batch", "max_ctx", "max_text", "step_path", "tc_min_tokens",
                                            "debug_sync", "wait_limit_us", "inject_timeout", "text_vocab",
-                                           "text_hidden")]
+                                           "text_hidden", "separate_projections")]
 
 # execution fields of the config (everything else comes from the model dims)
-EXEC_FIELDS = ("step_path", "tc_min_tokens", "debug_sync", "wait_limit_us", "inject_timeout")
+EXEC_FIELDS = ("step_path", "tc_min_tokens", "debug_sync", "wait_limit_us", "inject_timeout",
+               "separate_projections")
 
 
 class BlockWeights(ctypes.Structure):
@@ -98,7 +99,8 @@ def lib():
 
 
 def make_config(dims, dtype: int, max_batch: int, max_ctx: int, max_text: int, **exec_opts) -> Config:
-    """exec_opts: step_path, tc_min_tokens, debug_sync, wait_limit_us, inject_timeout (default 0)."""
+    """exec_opts: step_path, tc_min_tokens, debug_sync, wait_limit_us, inject_timeout,
+    separate_projections (default 0)."""
     unknown = set(exec_opts) - set(EXEC_FIELDS)
     if unknown:
         raise ValueError(f"unknown config options {sorted(unknown)}")

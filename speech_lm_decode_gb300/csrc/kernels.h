@@ -154,6 +154,9 @@ cudaError_t launch_cp_embed_step(int dtype, const RowState* rs, int B, const voi
 cudaError_t launch_text_gather(int dtype, const void* emb, const int32_t* ids, int n, int vocab, int width, float* out,
                                int* err, cudaStream_t st);
 cudaError_t launch_silu(float* x, long n, cudaStream_t st);
+// g[m][f] = silu(g[m][f]) * u[m][f] for the separate gate / up products
+// (g and u [M][F] fp32 with leading dimension F).
+cudaError_t launch_silu_mul(float* g, const float* u, long n, cudaStream_t st);
 
 // dst[b*pitch + j*G + q] = codes of frame f0+j of row b (-1 past the buffer).
 cudaError_t launch_pack_codes(const int32_t* codes_ws, int frames_cap, long f0, int n, int G, int B, int32_t* dst,

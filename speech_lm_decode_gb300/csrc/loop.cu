@@ -210,6 +210,17 @@ __global__ void silu_kernel(float* __restrict__ x, long n) {
     }
 }
 
+// SiLU(g) * u for the separate gate / up products, in place over g (the same
+// expression as the stacked product's epilogue)
+__global__ void silu_mul_kernel(float* __restrict__ g, const float* __restrict__ u, long n) {
+    pdl_wait();
+    pdl_trigger();
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+        const float v = g[i];
+        g[i] = v / (1.0f + expf(-v)) * u[i];
+    }
+}
+
 cudaError_t launch_text_gather(int dtype, const void* emb, const int32_t* ids, int n, int vocab, int width, float* out,
                                int* err, cudaStream_t st) {
     if (n <= 0) return cudaSuccess;
@@ -224,6 +235,13 @@ cudaError_t launch_silu(float* x, long n, cudaStream_t st) {
     if (n <= 0) return cudaSuccess;
     const int blocks = (int)std::min<long>((n + 255) / 256, 4L * device_sm_count());
     silu_kernel<<<blocks, 256, 0, st>>>(x, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_silu_mul(float* g, const float* u, long n, cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    const int blocks = (int)std::min<long>((n + 255) / 256, 4L * device_sm_count());
+    launch_pdl(silu_mul_kernel, blocks, 256, 0, st, g, u, n);
     return cudaGetLastError();
 }
 

@@ -122,7 +122,10 @@ Layout make_layout(const q3tts_config& c) {
     L.tcs = c.dtype == Q3_BF16 ? take((size_t)L.mmax * std::max(L.kA, L.kB) * 4) : take(256);
     // a second one: the SiLU(g)*u operand of the down projection, written while the
     // gate/up projection still reads the first
-    L.tcs2 = c.dtype == Q3_BF16 ? take((size_t)L.mmax * std::max(L.kA, L.kB) * 4) : take(256);
+    // (also the up product's fp32 output [mmax][F] when q/k/v and gate/up run
+    // as separate products)
+    L.tcs2 = c.dtype == Q3_BF16 || c.separate_projections ? take((size_t)L.mmax * std::max(L.kA, L.kB) * 4)
+                                                          : take(256);
     // cluster step kernel (batch 1): packed weight image, exchange words, parameters
     L.cl = c.step_path == Q3_PATH_CLUSTER && cl_unsupported(c)[0] == 0;
     if (L.cl) {
@@ -159,6 +162,7 @@ bool config_ok(const q3tts_config* c, std::string* why) {
     if (c->step_path < Q3_PATH_AUTO || c->step_path > Q3_PATH_CLUSTER) return bad("step_path out of range");
     if (c->wait_limit_us < 0 || c->inject_timeout < 0 || c->debug_sync < 0 || c->debug_sync > 1)
         return bad("bad wait_limit_us / inject_timeout / debug_sync");
+    if (c->separate_projections < 0 || c->separate_projections > 1) return bad("separate_projections must be 0 or 1");
     if (c->step_path == Q3_PATH_CLUSTER && cl_unsupported(*c)[0] != 0) return bad("cluster kernel: unsupported shape");
     if (c->text_vocab < 0 || c->text_hidden < 0 || (c->text_vocab > 0) != (c->text_hidden > 0) ||
         (c->text_hidden > 0 && c->text_hidden % 8))
@@ -309,7 +313,17 @@ int enqueue_layers(q3tts* h, bool talker, int M, float* x, const int* trow, cons
             CK(launch_rmsnorm(x, H, M, (const float*)bw.attn_norm + (size_t)l * H, H, eps, opA, H, nullptr, 0,
                               nullptr, h->st)); debug_wait(h, "launch_rmsnorm");
         }
-        CK(launch_linear(c.dtype, wqkv, nqkv, H, presplit ? nullptr : opA, H, M, qkv, nqkv, nullptr, 0, h->tc(), h->err(), h->st)); debug_wait(h, "launch_linear");
+        if (c.separate_projections) {
+            // q, k and v rows as three products into their columns of qkv
+            const int part[4] = {0, nq * hd, (nq + nkv) * hd, nqkv};
+            for (int i = 0; i < 3; ++i) {
+                CK(launch_linear(c.dtype, wqkv + (size_t)part[i] * H * e, part[i + 1] - part[i], H,
+                                 presplit ? nullptr : opA, H, M, qkv + part[i], nqkv, nullptr, 0, h->tc(), h->err(),
+                                 h->st)); debug_wait(h, "launch_linear");
+            }
+        } else {
+            CK(launch_linear(c.dtype, wqkv, nqkv, H, presplit ? nullptr : opA, H, M, qkv, nqkv, nullptr, 0, h->tc(), h->err(), h->st)); debug_wait(h, "launch_linear");
+        }
         const bool fused = single && !tiles && c.dtype == Q3_BF16 && nq == 2 * nkv && cap <= 64;
         if (fused) {
             CK(launch_attention_short_fused(qkv, nqkv, M, nq, nkv, (const float*)bw.q_norm + (size_t)l * hd,
@@ -341,10 +355,23 @@ int enqueue_layers(q3tts* h, bool talker, int M, float* x, const int* trow, cons
             CK(launch_rmsnorm(x, H, M, (const float*)bw.mlp_norm + (size_t)l * H, H, eps, opA, H, nullptr, 0,
                               nullptr, h->st)); debug_wait(h, "launch_rmsnorm");
         }
-        CK(launch_linear_gated(c.dtype, wgu, F, H, presplit ? nullptr : opA, H, M, opB, F, tcs, h->err(), h->st,
-                               presplit_d ? &tcs2 : nullptr)); debug_wait(h, "launch_linear_gated");
-        CK(launch_linear(c.dtype, wd, H, F, presplit_d ? nullptr : opB, F, M, x, H, nullptr, 1, presplit_d ? tcs2 : tcs,
-                         h->err(), h->st)); debug_wait(h, "launch_linear");
+        if (c.separate_projections) {
+            // gate into opB, up into the second scratch (as fp32 [M][F]), then
+            // SiLU(g) * u in place: the down projection reads opB
+            float* up = h->p<float>(h->L.tcs2);
+            CK(launch_linear(c.dtype, wgu, F, H, presplit ? nullptr : opA, H, M, opB, F, nullptr, 0, tcs, h->err(),
+                             h->st)); debug_wait(h, "launch_linear");
+            CK(launch_linear(c.dtype, wgu + (size_t)F * H * e, F, H, presplit ? nullptr : opA, H, M, up, F, nullptr,
+                             0, tcs, h->err(), h->st)); debug_wait(h, "launch_linear");
+            CK(launch_silu_mul(opB, up, (long)M * F, h->st)); debug_wait(h, "launch_silu_mul");
+            CK(launch_linear(c.dtype, wd, H, F, opB, F, M, x, H, nullptr, 1, tcs, h->err(), h->st));
+            debug_wait(h, "launch_linear");
+        } else {
+            CK(launch_linear_gated(c.dtype, wgu, F, H, presplit ? nullptr : opA, H, M, opB, F, tcs, h->err(), h->st,
+                                   presplit_d ? &tcs2 : nullptr)); debug_wait(h, "launch_linear_gated");
+            CK(launch_linear(c.dtype, wd, H, F, presplit_d ? nullptr : opB, F, M, x, H, nullptr, 1,
+                             presplit_d ? tcs2 : tcs, h->err(), h->st)); debug_wait(h, "launch_linear");
+        }
     }
     return Q3_OK;
 }

@@ -94,8 +94,11 @@ def test_execution_fields_are_validated():
     base = size()
     assert base > 0
     for kw in ({"step_path": 4}, {"step_path": -1}, {"wait_limit_us": -1}, {"inject_timeout": -2},
-               {"debug_sync": 2}):
+               {"debug_sync": 2}, {"separate_projections": 2}, {"separate_projections": -1}):
         assert size(**kw) == 0, kw
+    # separate q/k/v and gate/up products need no more room in bf16 (the up
+    # product reuses the second operand scratch)
+    assert size(separate_projections=1) == base
     for p in (q3.Q3_PATH_GRAPH, q3.Q3_PATH_FRAME):
         assert size(step_path=p) == base
     # the packed image holds every matrix once more (about 1.2 GB for the 0.6B shape)

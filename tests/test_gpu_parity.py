@@ -190,6 +190,26 @@ def test_batch1_paths_parity(q3, dims, dtype, path):
         compare(wl1, w, inp1, g)
 
 
+@pytest.mark.parametrize("dtype", [BF16, F32])
+def test_separate_projections(q3, dtype):
+    """q/k/v and gate/up as separate products (the unstacked layout): parity
+    with the oracle at batch > 1 (tensor-core prefill, GEMV steps), and on the
+    per-layer path without tensor cores the same codes and logits bit for bit
+    as the stacked products (every output row is the same dot product)."""
+    wl = small_workload(synth.DIMS_SMALL, dtype, frames=8)
+    w = small_weights(wl)
+    inp = synth.make_inputs(wl)
+    dw = q3.to_device_weights(w)
+    g = run_gpu(wl, dw, inp, cap_rows=[0, wl.batch - 1], separate_projections=1)
+    compare(wl, w, inp, g)
+    wl1, inp1 = _single_row(wl, 0), _single_inputs(inp, 0)
+    a = run_gpu(wl1, dw, inp1, cap_rows=[0], step_path=q3.Q3_PATH_GRAPH, tc_min_tokens=-1)
+    b = run_gpu(wl1, dw, inp1, cap_rows=[0], step_path=q3.Q3_PATH_GRAPH, tc_min_tokens=-1, separate_projections=1)
+    assert np.array_equal(a.codes, b.codes)
+    assert np.array_equal(a.talker_logits, b.talker_logits, equal_nan=True)
+    assert np.array_equal(a.cp_logits, b.cp_logits, equal_nan=True)
+
+
 def test_frame_kernel_chunked_and_repeatable(q3):
     wl = _single_row(small_workload(synth.DIMS_SMALL, BF16, frames=14), 1)
     w = small_weights(wl)
